@@ -1,0 +1,474 @@
+#!/usr/bin/env python
+"""Benchmark of the Dust per-token weight-gradient estimator on GB300.
+
+One step = one dust_estimate_gW call on the MLP up-projection workload
+(d_in 512, d_out 2048, 16 x 1024 tokens, K = 8 draws, sigma 1e-3, gamma 0,
+Gaussian jitter, bf16 X): centring, credit scan, noise regeneration + reward
+weighting, and the contraction to GW, with inputs resident in HBM.
+
+Metric: token-draws/s = K * T / step time (whole job over all ranks).
+Prints one JSON line (rank 0). `--impl reference` times the fp64 CPU oracle
+on the same workload instead (rank 0 only).
+
+Timing: W warm-up steps, then K timed steps, each bracketed by CUDA events on
+the launching stream with a 256 MB L2 flush between steps (outside the
+events); barrier + synchronize around the timed region; max over ranks.
+A second, profiled pass of the same K steps times every kernel with events
+(dust_profile_*) for the roofline of the dominant kernel.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Dust ĜW token-draws/s at 1 GB300; % tensor-pipe peak (ĝᵀX) and % HBM (noise)"
+UNIT = "token-draws/s"
+WORKLOAD = "mlp_up_512to2048_T16384_K8_gaussian"
+SMI_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--cpu-seconds", type=float, default=15.0,
+                   help="target wall time of the CPU-oracle sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--flags", type=int, default=None,
+                   help="extra dust_estimate_gW flags (e.g. force a path)")
+    return p.parse_args(argv)
+
+
+# --------------------------------------------------------------- ranks ----
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def aggregate(units_per_rank: float, ms_total: float, steps: int, world: int, backend_sync):
+    """Whole-job throughput from each rank's device time: the max over ranks
+    of the timed-region duration, units summed over ranks. `backend_sync`
+    maps a local float to its max over ranks (identity at world size 1)."""
+    ms_max = backend_sync(ms_total)
+    ms_per_step = ms_max / steps
+    value = world * units_per_rank * steps / (ms_max / 1000.0)
+    return value, ms_per_step
+
+
+# -------------------------------------------------------------- clocks ----
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + SMI_QUERY,
+                 "--format=csv,noheader,nounits", "-lms", str(self.period)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        self.t0 = time.time()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def __exit__(self, *exc):
+        self.t1 = time.time()
+        time.sleep(0.1)
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        sm, smax, reasons, n = [], None, set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, line in self.lines:
+            if not (self.t0 <= ts <= self.t1 + 0.05):
+                continue
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            n += 1
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": n}
+
+
+# ------------------------------------------------------------ workload ----
+
+def make_inputs(w, dev):
+    """X (bf16), delta (planted quadratic loss, built with the library's own
+    noise kernel, untimed) and sequence offsets, all resident on `dev`."""
+    import numpy as np
+    import torch
+    import token_perturbation_estimator_gb300 as dust
+    import workloads as wl
+
+    X = torch.from_numpy(wl.make_X(w)).to(dev).to(torch.bfloat16)
+    dplant = torch.from_numpy(wl.make_dplant(w)).to(dev)
+    eps = torch.from_numpy(wl.make_eps(w)).to(dev)
+    a = torch.empty((1, w.T, w.d_out), dtype=torch.float32, device=dev)
+    dot = torch.empty((w.K, w.T), dtype=torch.float64, device=dev)
+    sq = torch.empty((w.K, w.T), dtype=torch.float64, device=dev)
+    for k in range(w.K):
+        dust.dust_noise(a, w.seed, w.kind, k, 1, w.T, w.d_out)
+        dot[k] = (a[0].double() * dplant.double()).sum(dim=1)
+        sq[k] = (a[0].double() ** 2).sum(dim=1)
+    delta = (w.sigma * dot + w.curvature * 0.5 * w.sigma * w.sigma * sq + eps.double()).float()
+    so = torch.from_numpy(wl.seq_offsets(w)).to(dev)
+    del a, dplant
+    return X, delta.contiguous(), so
+
+
+# ---------------------------------------------------------- roofline -----
+
+def roofline_for(stage, ms_per_launch, w, peaks, path):
+    """Roofline of the dominant kernel family. Algorithmic work per launch:
+      weight / fused (Gaussian): 2 transcendental (XU) ops per element-draw
+        (Box-Muller's log, sqrt, sin, cos per channel pair) -> bound "alu"
+        against the XU pipe: 16 ops/clk/SM x 152 SMs x 2.07 GHz;
+      weight / fused (Rademacher): 1 hash word per element-draw, 6 integer
+        ALU ops each -> bound "alu" against 64 int ops/clk/SM x 152 x 2.07 GHz;
+      gemm_tc: 2 T d_in d_out FLOP -> bound "tensor" (measured bf16 peak);
+      gemm_simt: same FLOP on FFMA -> "alu", 256 FLOP/clk/SM x 152 x 2.07 GHz."""
+    sm, clk = 152, 2.07e9
+    s = ms_per_launch / 1000.0
+    if stage in ("weight", "fused"):
+        if w.kind == 1:
+            ops = 2.0 * w.element_draws
+            peak = 16 * sm * clk
+        else:
+            ops = 6.0 * w.element_draws
+            peak = 64 * sm * clk
+        ach = ops / s
+        return {"bound": "alu", "achieved": ach / 1e9, "peak": peak / 1e9, "unit": "Gop/s",
+                "frac": ach / peak, "traffic": None, "kernel": stage,
+                "algorithmic_per_launch": ops,
+                "peak_source": "derived: unit counts x 152 SMs x 2.07 GHz max SM clock"}
+    if stage == "gemm_tc":
+        fl = float(w.gemm_flops)
+        peak = peaks.get("bf16_tflops_sustained", 1694.3) * 1e12
+        ach = fl / s
+        return {"bound": "tensor", "achieved": ach / 1e12, "peak": peak / 1e12,
+                "unit": "TFLOP/s", "frac": ach / peak, "traffic": None, "kernel": stage,
+                "algorithmic_per_launch": fl,
+                "peak_source": "MEASURED_PEAKS.json bf16_tflops_sustained (of measured)"}
+    fl = float(w.gemm_flops)
+    peak = 256 * sm * clk
+    ach = fl / s
+    return {"bound": "alu", "achieved": ach / 1e12, "peak": peak / 1e12, "unit": "TFLOP/s",
+            "frac": ach / peak, "traffic": None, "kernel": stage,
+            "algorithmic_per_launch": fl,
+            "peak_source": "derived: 128 FFMA lanes x 2 FLOP x 152 SMs x 2.07 GHz"}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "fallback": True}
+
+
+def traffic_from_profiles(kernel, lib_stamp):
+    """DRAM bytes per launch from a committed ncu capture, if it was taken on
+    the current build of the kernels (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(kernel)
+    if not e or e.get("build_stamp") != lib_stamp:
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------- cpu leg ----
+
+def cpu_oracle_rate(w, target_s, max_seqs=None):
+    """Time the fp64 oracle on a bounded sample of the workload: whole
+    sequences (all channels, all draws), grown until about target_s."""
+    import numpy as np
+    import oracle
+    import workloads as wl
+
+    X_all = wl.to_bf16_exact(wl.make_X(w))
+    dp_all = wl.make_dplant(w)
+    eps_all = wl.make_eps(w)
+    max_seqs = max_seqs or w.n_seq
+
+    def run(nseq):
+        T = nseq * w.seq_len
+        so = (np.arange(nseq + 1) * w.seq_len).astype(np.int32)
+        delta = oracle.planted_delta(dp_all[:T], w.seed, w.kind, 0, w.K, np.float32(w.sigma),
+                                     w.curvature, eps_all[:, :T]).astype(np.float32)
+        t0 = time.perf_counter()
+        oracle.estimate_gW(X_all[:T], delta, w.d_out, so, w.seed, w.kind, 0,
+                           np.float32(w.sigma), np.float32(w.gamma), 1.0, oracle.CENTER)
+        return time.perf_counter() - t0, T
+
+    t1, T1 = run(1)
+    nseq = int(max(1, min(max_seqs, round(target_s / max(t1, 1e-3)))))
+    if nseq > 1:
+        t1, T1 = run(nseq)
+    return {"value": w.K * T1 / t1, "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": "%d of %d sequences (%d tokens x %d draws x d_out %d x d_in %d), "
+                      "%.1f s" % (T1 // w.seq_len, w.n_seq, T1, w.K, w.d_out, w.d_in, t1)}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np
+    import oracle
+    import workloads as wl
+
+    w = wl.MLP_UP
+    X = wl.to_bf16_exact(wl.make_X(w))
+    dp = wl.make_dplant(w)
+    eps = wl.make_eps(w)
+    # One step = the oracle's whole path on one sequence of the workload.
+    T = w.seq_len
+    so = np.array([0, T], np.int32)
+    delta = oracle.planted_delta(dp[:T], w.seed, w.kind, 0, w.K, np.float32(w.sigma),
+                                 w.curvature, eps[:, :T]).astype(np.float32)
+
+    def step():
+        oracle.estimate_gW(X[:T], delta, w.d_out, so, w.seed, w.kind, 0, np.float32(w.sigma),
+                           np.float32(w.gamma), 1.0, oracle.CENTER)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = w.K * T * args.steps / dt
+    cores = oracle.num_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "sample_tokens_per_step": T,
+                                        "d_in": w.d_in, "d_out": w.d_out, "K": w.K},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": "one %d-token sequence per step, all draws and channels"
+                                   % T},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------- gpu leg ----
+
+def run_gb300(args):
+    import numpy as np
+    import torch
+
+    rank, world, local = dist_env()
+    from __graft_entry__ import build
+    build()
+    import token_perturbation_estimator_gb300 as dust
+    import workloads as wl
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl", device_id=dev)
+        pg = tdist
+
+    def max_over_ranks(x):
+        if pg is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+
+    w = wl.MLP_UP
+    X, delta, so = make_inputs(w, dev)
+    flags = dust.CENTER | (args.flags or 0)
+    path = dust.dust_estimate_gW_path(w.T, w.d_in, w.d_out, w.K, dust.BF16, flags)
+    ws_bytes = dust.dust_estimate_gW_workspace(w.T, w.d_in, w.d_out, w.K, dust.BF16, flags)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    gW = torch.empty((w.d_out, w.d_in), dtype=torch.float32, device=dev)
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)  # 256 MB > L2
+    stream = torch.cuda.current_stream()
+
+    def step():
+        dust.dust_estimate_gW(X, delta, w.d_out, so, w.seed, w.kind, 0, w.sigma, w.gamma, 1.0,
+                              flags, gW=gW, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    st = dust.dust_last_error()
+    if st != dust.OK:
+        raise RuntimeError("device status after warm-up: " + dust.status_string(st))
+
+    # ---- headline timed region
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for k in range(args.steps):
+            flush.zero_()
+            starts[k].record(stream)
+            step()
+            ends[k].record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms_total = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+    value, ms_per_step = aggregate(w.token_draws, ms_total, args.steps, world, max_over_ranks)
+
+    # ---- profiled pass (same steps) for per-kernel times
+    dust.dust_profile_enable(True)
+    dust.dust_profile_read()
+    for k in range(args.steps):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    prof = {k: {"launches": v[0], "total_ms": v[1]} for k, v in dust.dust_profile_read().items()}
+    dust.dust_profile_enable(False)
+    launches_per_step = sum(v["launches"] for v in prof.values()) / args.steps
+    top = max(prof.items(), key=lambda kv: kv[1]["total_ms"])
+    top_ms = top[1]["total_ms"] / top[1]["launches"]
+    peaks = load_peaks()
+    roof = roofline_for(top[0], top_ms, w, peaks, path)
+    stamp_file = os.path.join(ROOT, "token_perturbation_estimator_gb300", "lib",
+                              "libdust_gb300.so.stamp")
+    stamp = open(stamp_file).read().strip() if os.path.exists(stamp_file) else None
+    roof["traffic"] = traffic_from_profiles(top[0], stamp)
+    breakdown = {k: {"launches": v["launches"],
+                     "ms_per_launch": v["total_ms"] / v["launches"],
+                     "share": v["total_ms"] / sum(x["total_ms"] for x in prof.values())}
+                 for k, v in prof.items()}
+
+    # ---- end to end through the host-buffer C ABI entry point
+    Xh = X.cpu().pin_memory()
+    dh = delta.cpu().pin_memory()
+    sh = so.cpu().pin_memory()
+    gh = torch.empty((w.d_out, w.d_in), dtype=torch.float32).pin_memory()
+    Xs, ds, ss = torch.empty_like(X), torch.empty_like(delta), torch.empty_like(so)
+    gs = torch.empty_like(gW)
+
+    def e2e_step():
+        dust.dust_estimate_gW_host(Xh, Xs, dh, ds, sh, ss, gh, gs, w.d_out, w.seed, w.kind, 0,
+                                   w.sigma, w.gamma, 1.0, flags, workspace=ws, stream=stream)
+        stream.synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e2e_s = max_over_ranks(time.perf_counter() - t0)
+    e2e_value = world * w.token_draws * args.e2e_steps / e2e_s
+    h2d = Xh.numel() * Xh.element_size() + dh.numel() * 4 + sh.numel() * 4
+    d2h = gh.numel() * 4
+    # the two results agree (same arguments, deterministic)
+    if not torch.equal(gh, gW.cpu()):
+        raise RuntimeError("host-buffer path disagrees with the device path")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_rate(w, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "d_in": w.d_in, "d_out": w.d_out, "T": w.T,
+                       "n_seq": w.n_seq, "K": w.K, "sigma": w.sigma, "gamma": w.gamma,
+                       "noise": "gaussian", "x_dtype": "bf16", "path": path,
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "flushed (256 MB write) between timed steps"},
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": int(round(launches_per_step * args.steps)),
+            "clocks": clocks.summary(),
+            "breakdown": breakdown,
+            "profiled_ms_per_step": sum(v["total_ms"] for v in prof.values()) / args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gb300(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,260 @@
+/*
+ * dust.h — C ABI of the GB300 (sm_103a) library for Dust's per-token
+ * zeroth-order weight-gradient estimator of one linear layer y_t = W x_t.
+ *
+ * What the library computes ("Dust: every token is a member of the
+ * population", ai.satyajit.si, section "Perturb the activations, not the
+ * weights", the three equations for r_t, g_t and G_W):
+ *
+ *   c[i][t]  = -(delta[i][t] - mean_j delta[j][t])       centred loss reduction
+ *   r[i][t]  = sum_{s >= t, same sequence} gamma^(s-t) c[i][s]   credit scan
+ *   g[t][c]  = -(1 / (K sigma)) sum_i r[i][t] a_t^(i)[c]         output error
+ *   GW[c][j] = scale * sum_t g[t][c] x[t][j]                     weight gradient
+ *
+ * delta[i][t] is the loss change L(perturbed) - L(clean) of draw i at token t,
+ * so the reward (loss reduction) is its negative, as in the page's section
+ * "What the released code actually does" (step 2: reward = clean loss minus
+ * perturbed loss, centred across draws that share a forward). The
+ * contraction is that section's step 7 (an einsum over tokens; `scale`
+ * carries the optional division by the token count).
+ *
+ * The jitter a_t^(i) ~ N(0, I) (or Rademacher +-1) is never stored: it is
+ * regenerated from a counter-based hash, the murmur3 fmix32 family of "RandOpt
+ * Speedrun", section "What was slow, and the fix". This library's definition:
+ *
+ *   fmix32      MurmurHash3's 32-bit finaliser
+ *   seed_key    fmix32(lo32(seed) ^ fmix32(hi32(seed) + 0x9E3779B9))
+ *   draw_key    fmix32(seed_key ^ (2*i + s) * 0x9E3779B9)    (mod 2^32)
+ *   word        fmix32(draw_key(i, s) ^ (t * d_out + c))      (mod 2^32)
+ *   Rademacher  a = +1 if word(i,t,c,0) < 2^31, else -1
+ *   Gaussian    pair p = c & ~1, w0 = word(i,t,p,0), w1 = word(i,t,p,1),
+ *               u1 = 1 - (w0 >> 9) 2^-23, u2 = (w1 >> 9) 2^-23,
+ *               rho = sqrt(-2 ln u1); even c: rho cos(2 pi u2),
+ *               odd c: rho sin(2 pi u2) (the last channel of an odd d_out
+ *               takes the cosine).
+ *   Antithetic  (DUST_ANTITHETIC) draw i uses base draw i >> 1 times
+ *               (-1)^(i & 1): draws 2j and 2j+1 are an opposite-sign pair.
+ * i is the absolute draw index (draw_begin + local index); t is the row of the
+ * flattened token matrix. T * d_out must not exceed 2^32.
+ *
+ * Conventions for every entry point:
+ *  - Pointers marked "device" are device memory of the current device; the
+ *    caller owns every buffer (this library allocates no device memory).
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream). Work is
+ *    enqueued asynchronously on it; no entry point synchronises the device
+ *    except dust_last_error.
+ *  - Argument errors are detected on the host before anything is enqueued;
+ *    the call then returns a non-zero dust_status and launches nothing.
+ *  - A failed launch returns DUST_ERR_CUDA. Device-side errors (a bounded wait
+ *    that ran out) are recorded in a device status word read by
+ *    dust_last_error.
+ *  - Row-major, contiguous layouts unless a leading dimension is given.
+ *  - bf16 is IEEE bfloat16 (1-8-7), stored as uint16.
+ */
+#ifndef DUST_H
+#define DUST_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DUST_OK = 0,
+    DUST_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad enum/flag */
+    DUST_ERR_RANGE = 2,        /* a size beyond a documented limit */
+    DUST_ERR_UNSUPPORTED = 3,  /* valid request this build cannot serve */
+    DUST_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+    DUST_ERR_TIMEOUT = 5,      /* a device-side bounded wait ran out */
+    DUST_ERR_WORKSPACE = 6     /* workspace missing, too small or misaligned */
+} dust_status;
+
+typedef enum {
+    DUST_NOISE_RADEMACHER = 0,
+    DUST_NOISE_GAUSSIAN = 1,
+    DUST_NOISE_RAW_WORDS = 2   /* dust_noise only: the uint32 hash words */
+} dust_noise_kind;
+
+typedef enum {
+    DUST_F32 = 0,
+    DUST_BF16 = 1,
+    DUST_U32 = 2               /* dust_noise with DUST_NOISE_RAW_WORDS only */
+} dust_dtype;
+
+/* Flags (bitwise OR). */
+enum {
+    DUST_CENTER = 1u,          /* centre each token's loss changes over the K draws (K > 1) */
+    DUST_ANTITHETIC = 2u,      /* draws 2j, 2j+1 are an opposite-sign pair (needs even K,
+                                  even draw_begin for the estimator) */
+    DUST_ACCUMULATE = 4u,      /* GW += result instead of GW = result */
+    DUST_FORCE_UNFUSED = 8u,   /* estimator: write g to the workspace, then contract */
+    DUST_FORCE_FUSED = 16u,    /* estimator: produce g tiles inside the contraction
+                                  (DUST_ERR_UNSUPPORTED where that kernel cannot run) */
+    DUST_WORD_STREAM1 = 32u,   /* dust_noise RAW_WORDS: words of stream s = 1 */
+    DUST_FORCE_SIMT = 64u      /* estimator: contraction on CUDA cores (fp32 FFMA) */
+};
+
+/* Contraction paths reported by dust_estimate_gW_path. */
+typedef enum {
+    DUST_PATH_FUSED_TC = 1,    /* fused g-producer + tcgen05 MMA, bf16 in, fp32 accumulate */
+    DUST_PATH_UNFUSED_TC = 2,  /* weighting kernel -> g (bf16) -> tcgen05 GEMM */
+    DUST_PATH_SIMT = 3         /* weighting kernel -> g (fp32 or bf16) -> FFMA GEMM */
+} dust_path;
+
+/* Limits. */
+#define DUST_MAX_DRAWS 8192          /* K and n_draws */
+#define DUST_MAX_COUNTER 4294967296LL /* T * d_out */
+
+/* Human-readable name of a status. Never NULL; static storage. */
+const char* dust_status_string(dust_status s);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int32_t dust_version(void);
+
+/*
+ * dust_noise — materialise the jitter of draws [draw_begin, draw_begin +
+ * n_draws): out[k][t][c] = a_t^(draw_begin+k)[c] ("Perturb the activations,
+ * not the weights": y_t -> y_t + sigma a_t with a_t ~ N(0, I)). Used by tests
+ * and to synthesise inputs; the estimator itself never stores the jitter.
+ *   out       device, [n_draws][T][d_out]; DUST_F32 or DUST_BF16 values
+ *             (Rademacher/Gaussian) or DUST_U32 words (RAW_WORDS; stream 0,
+ *             or stream 1 with DUST_WORD_STREAM1; DUST_ANTITHETIC ignored).
+ *   draw_begin >= 0, n_draws in [0, DUST_MAX_DRAWS], T >= 0, d_out >= 0,
+ *   T * d_out <= 2^32 (else DUST_ERR_RANGE). Empty sizes launch nothing.
+ */
+dust_status dust_noise(void* out, dust_dtype out_dtype, uint64_t seed,
+                       dust_noise_kind kind, int64_t draw_begin, int64_t n_draws,
+                       int64_t T, int64_t d_out, uint32_t flags, void* stream);
+
+/*
+ * dust_jitter_apply — the jittered forward's output perturbation, in place:
+ * y[t][c] += sigma * a_t^(draw)[c] (same section; the jitter is added after
+ * the layer's product, i.e. the split form of "Scaling To Unfathomable
+ * Depth", section "Kernel Recipes").
+ *   y      device, T rows of d_out values with row stride ld_y >= d_out
+ *          (elements); DUST_F32 or DUST_BF16 (bf16 rounded to nearest even).
+ *   kind   DUST_NOISE_RADEMACHER or DUST_NOISE_GAUSSIAN; draw >= 0.
+ */
+dust_status dust_jitter_apply(void* y, dust_dtype y_dtype, int64_t ld_y, int64_t T,
+                              int64_t d_out, uint64_t seed, dust_noise_kind kind,
+                              int64_t draw, float sigma, uint32_t flags, void* stream);
+
+/*
+ * dust_credit_scan_workspace / dust_credit_scan — centring and the reverse
+ * credit scan on their own (the r_t equation; centring as described above).
+ *   delta       device f32 [K][T] loss changes.
+ *   seq_offsets device i32 [n_seq + 1]: 0 = o_0 < o_1 < ... < o_n_seq = T
+ *               (each sequence non-empty); the scan restarts at every
+ *               sequence. n_seq >= 1 when T > 0.
+ *   gamma       credit decay, finite, |gamma| <= 1.
+ *   flags       DUST_CENTER or 0.
+ *   r           device f32 [T][K] (token-major): r[t][i] = r_t^(i).
+ *   workspace   device, >= the size reported by dust_credit_scan_workspace,
+ *               256-byte aligned.
+ */
+dust_status dust_credit_scan_workspace(size_t* bytes, int64_t K, int64_t T);
+dust_status dust_credit_scan(const float* delta, int64_t K, int64_t T,
+                             const int32_t* seq_offsets, int64_t n_seq, float gamma,
+                             uint32_t flags, float* r, void* workspace, size_t ws_bytes,
+                             void* stream);
+
+/*
+ * dust_error_estimate — reward-weighted noise on its own (the g_t equation):
+ * g[t][c] = -(1/(K sigma)) sum_{i<K} r[t][i] a_t^(draw_begin+i)[c].
+ *   r      device f32 [T][K] (the output of dust_credit_scan).
+ *   g      device [T][d_out], DUST_F32 or DUST_BF16 (rounded to nearest even).
+ *   sigma  finite, non-zero.
+ */
+dust_status dust_error_estimate(const float* r, int64_t K, int64_t T, int64_t d_out,
+                                uint64_t seed, dust_noise_kind kind, int64_t draw_begin,
+                                float sigma, uint32_t flags, void* g, dust_dtype g_dtype,
+                                void* stream);
+
+/*
+ * dust_estimate_gW_workspace / dust_estimate_gW — the whole path, delta and X
+ * to the weight gradient GW (the three equations above, in one call).
+ *   X           device [T][d_in], DUST_BF16 (tensor-core path, fp32
+ *               accumulation) or DUST_F32 (CUDA-core fp32 path). 16-byte
+ *               aligned base; for DUST_BF16 the tensor-core paths also need
+ *               d_in % 8 == 0 and d_out % 8 == 0 (otherwise the CUDA-core
+ *               contraction runs).
+ *   delta       device f32 [K][T]; seq_offsets as for dust_credit_scan.
+ *   kind        DUST_NOISE_RADEMACHER or DUST_NOISE_GAUSSIAN.
+ *   draw_begin  absolute index of the first draw (>= 0).
+ *   sigma       finite, non-zero; gamma finite, |gamma| <= 1; scale finite.
+ *   flags       DUST_CENTER, DUST_ANTITHETIC, DUST_ACCUMULATE and at most one
+ *               of DUST_FORCE_UNFUSED / DUST_FORCE_FUSED / DUST_FORCE_SIMT.
+ *   gW          device f32 [d_out][d_in], W's layout; overwritten, or
+ *               accumulated into with DUST_ACCUMULATE.
+ *   workspace   device, >= dust_estimate_gW_workspace(...) bytes, 256-byte
+ *               aligned; contents on entry are ignored.
+ * The result is a deterministic function of the inputs (no floating-point
+ * atomics): two calls with the same arguments give bit-identical gW.
+ */
+dust_status dust_estimate_gW_workspace(size_t* bytes, int64_t T, int64_t d_in,
+                                       int64_t d_out, int64_t K, dust_dtype x_dtype,
+                                       uint32_t flags);
+dust_status dust_estimate_gW(const void* X, dust_dtype x_dtype, int64_t T, int64_t d_in,
+                             const float* delta, int64_t K, int64_t d_out,
+                             const int32_t* seq_offsets, int64_t n_seq, uint64_t seed,
+                             dust_noise_kind kind, int64_t draw_begin, float sigma,
+                             float gamma, float scale, uint32_t flags, float* gW,
+                             void* workspace, size_t ws_bytes, void* stream);
+
+/* The contraction path dust_estimate_gW would take for these arguments
+ * (a dust_path value), or a negative dust_status on invalid arguments. */
+int32_t dust_estimate_gW_path(int64_t T, int64_t d_in, int64_t d_out, int64_t K,
+                              dust_dtype x_dtype, uint32_t flags);
+
+/*
+ * dust_estimate_gW_host — the same computation from HOST buffers: copies
+ * X_host -> X_dev, delta_host -> delta_dev and seq_offsets_host -> seq_dev on
+ * `stream`, runs dust_estimate_gW, and copies gW_dev -> gW_host. With
+ * DUST_ACCUMULATE, gW_host is first copied to gW_dev. Host buffers should be
+ * page-locked (else the copies are synchronous) and must stay valid until
+ * the stream has completed; the caller synchronises before reading gW_host.
+ * Device staging buffers are caller-owned with the sizes of the host ones.
+ */
+dust_status dust_estimate_gW_host(const void* X_host, void* X_dev, dust_dtype x_dtype,
+                                  int64_t T, int64_t d_in, const float* delta_host,
+                                  float* delta_dev, int64_t K, int64_t d_out,
+                                  const int32_t* seq_offsets_host, int32_t* seq_dev,
+                                  int64_t n_seq, uint64_t seed, dust_noise_kind kind,
+                                  int64_t draw_begin, float sigma, float gamma, float scale,
+                                  uint32_t flags, float* gW_host, float* gW_dev,
+                                  void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Per-kernel timing for benchmarks (no counterpart on the pages: this is
+ * measurement plumbing). While enabled, every kernel the library launches is
+ * bracketed by two CUDA events recorded on its stream; dust_profile_read
+ * waits for the recorded events, returns per-kernel launch counts and summed
+ * durations, and clears the record. Process-global state: enable it only in
+ * a single-threaded benchmark. At most 65536 launches are recorded between
+ * reads (later launches are not timed).
+ */
+typedef struct {
+    char name[32];       /* kernel family, e.g. "weight", "gemm_tc", "scan" */
+    int64_t launches;
+    double total_ms;
+} dust_profile_entry;
+
+dust_status dust_profile_enable(int32_t on);
+/* Writes up to max_entries entries; returns how many were written (>= 0) or a
+ * negative dust_status. */
+int32_t dust_profile_read(dust_profile_entry* out, int32_t max_entries);
+
+/*
+ * dust_last_error — synchronise `stream`, then return and clear the device
+ * status word (DUST_OK, or DUST_ERR_TIMEOUT when a kernel's bounded wait ran
+ * out since the last call). DUST_ERR_CUDA if the synchronisation failed.
+ */
+dust_status dust_last_error(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DUST_H */

@@ -1,0 +1,110 @@
+"""The C ABI library loads and exports what include/dust.h declares, and its
+host-side argument checks reject bad calls before touching the GPU (CPU only:
+every call here fails validation, so nothing is enqueued)."""
+import ctypes as C
+
+import pytest
+
+import token_perturbation_estimator_gb300 as dust
+
+NULL = C.c_void_p(0)
+
+
+@pytest.fixture(scope="module")
+def L():
+    from token_perturbation_estimator_gb300 import build
+    build.build()
+    return dust.lib()
+
+
+def test_exports_every_declared_function(L):
+    names = dust.header_functions()
+    assert "dust_estimate_gW" in names and "dust_noise" in names and "dust_jitter_apply" in names
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    for s in range(7):
+        assert dust.status_string(s).startswith("DUST_")
+    assert L.dust_version() >= 100
+
+
+def _ws(L, T, d_in, d_out, K, xd, flags):
+    n = C.c_size_t(0)
+    st = L.dust_estimate_gW_workspace(C.byref(n), T, d_in, d_out, K, xd, flags)
+    return st, n.value
+
+
+def test_workspace_query_validation(L):
+    assert _ws(L, 16384, 512, 2048, 8, dust.BF16, dust.CENTER)[0] == dust.OK
+    assert _ws(L, 16384, 512, 2048, 8, dust.BF16, dust.CENTER)[1] > 0
+    assert _ws(L, 16, 8, 8, 0, dust.BF16, 0)[0] == dust.ERR_INVALID_ARG          # K = 0
+    assert _ws(L, 16, 8, 8, 9000, dust.BF16, 0)[0] == dust.ERR_RANGE             # K too big
+    assert _ws(L, -1, 8, 8, 4, dust.BF16, 0)[0] == dust.ERR_INVALID_ARG
+    assert _ws(L, 16, 8, 8, 4, 7, 0)[0] == dust.ERR_INVALID_ARG                  # dtype
+    assert _ws(L, 16, 8, 8, 3, dust.BF16, dust.ANTITHETIC)[0] == dust.ERR_INVALID_ARG
+    assert _ws(L, 16, 8, 8, 4, dust.BF16, 1 << 20)[0] == dust.ERR_INVALID_ARG    # unknown flag
+    assert _ws(L, 16, 8, 8, 4, dust.BF16,
+               dust.FORCE_FUSED | dust.FORCE_SIMT)[0] == dust.ERR_INVALID_ARG
+    # T * d_out beyond the 32-bit hash counter
+    assert _ws(L, (1 << 20) + 1, 8, 4096, 4, dust.BF16, 0)[0] == dust.ERR_RANGE
+    assert _ws(L, 1 << 20, 8, 4096, 4, dust.BF16, 0)[0] == dust.OK
+
+
+def _est(L, **kw):
+    a = dict(X=NULL, xd=dust.BF16, T=64, d_in=16, delta=NULL, K=4, d_out=16, so=NULL, n_seq=1,
+             seed=0, kind=dust.GAUSSIAN, db=0, sigma=1e-3, gamma=0.0, scale=1.0,
+             flags=dust.CENTER, gW=NULL, ws=NULL, wsb=0)
+    a.update(kw)
+    return L.dust_estimate_gW(a["X"], a["xd"], a["T"], a["d_in"], a["delta"], a["K"],
+                              a["d_out"], a["so"], a["n_seq"], a["seed"], a["kind"], a["db"],
+                              a["sigma"], a["gamma"], a["scale"], a["flags"], a["gW"], a["ws"],
+                              a["wsb"], NULL)
+
+
+def test_estimate_rejects_bad_arguments(L):
+    fake = C.c_void_p(1 << 20)
+    assert _est(L) == dust.ERR_INVALID_ARG                      # null gW
+    assert _est(L, gW=fake) == dust.ERR_INVALID_ARG             # null X / delta
+    assert _est(L, gW=fake, sigma=0.0) == dust.ERR_INVALID_ARG
+    assert _est(L, gW=fake, sigma=float("nan")) == dust.ERR_INVALID_ARG
+    assert _est(L, gW=fake, gamma=1.5) == dust.ERR_INVALID_ARG
+    assert _est(L, gW=fake, kind=dust.RAW_WORDS) == dust.ERR_INVALID_ARG
+    assert _est(L, gW=fake, K=0) == dust.ERR_INVALID_ARG
+    assert _est(L, gW=fake, db=-1) == dust.ERR_INVALID_ARG
+    assert _est(L, gW=fake, db=(1 << 31) - 2) == dust.ERR_RANGE
+    assert _est(L, gW=fake, n_seq=0) == dust.ERR_INVALID_ARG
+    assert _est(L, gW=fake, n_seq=65) == dust.ERR_INVALID_ARG
+    assert _est(L, gW=fake, flags=dust.ANTITHETIC, db=1) == dust.ERR_INVALID_ARG
+    # all pointers present but no workspace
+    assert _est(L, gW=fake, X=fake, delta=fake, so=fake) == dust.ERR_WORKSPACE
+    # misaligned workspace
+    assert _est(L, gW=fake, X=fake, delta=fake, so=fake, ws=C.c_void_p((1 << 20) + 4),
+                wsb=1 << 30) == dust.ERR_WORKSPACE
+    # empty layer: nothing to do, success without touching the device
+    assert _est(L, d_out=0) == dust.OK
+
+
+def test_noise_and_jitter_reject_bad_arguments(L):
+    fake = C.c_void_p(1 << 20)
+    assert L.dust_noise(fake, dust.F32, 0, dust.RAW_WORDS, 0, 1, 4, 4, 0, NULL) == dust.ERR_INVALID_ARG
+    assert L.dust_noise(fake, dust.U32, 0, dust.GAUSSIAN, 0, 1, 4, 4, 0, NULL) == dust.ERR_INVALID_ARG
+    assert L.dust_noise(fake, dust.F32, 0, 9, 0, 1, 4, 4, 0, NULL) == dust.ERR_INVALID_ARG
+    assert L.dust_noise(fake, dust.F32, 0, dust.GAUSSIAN, -1, 1, 4, 4, 0, NULL) == dust.ERR_INVALID_ARG
+    assert L.dust_noise(fake, dust.F32, 0, dust.GAUSSIAN, 0, 1, 1 << 23, 1 << 10, 0, NULL) == dust.ERR_RANGE
+    assert L.dust_noise(NULL, dust.F32, 0, dust.GAUSSIAN, 0, 1, 4, 4, 0, NULL) == dust.ERR_INVALID_ARG
+    assert L.dust_noise(NULL, dust.F32, 0, dust.GAUSSIAN, 0, 0, 4, 4, 0, NULL) == dust.OK
+    assert L.dust_jitter_apply(fake, dust.F32, 3, 4, 4, 0, dust.GAUSSIAN, 0, 1.0, 0, NULL) == dust.ERR_INVALID_ARG
+    assert L.dust_jitter_apply(NULL, dust.F32, 4, 4, 4, 0, dust.GAUSSIAN, 0, 1.0, 0, NULL) == dust.ERR_INVALID_ARG
+    assert L.dust_jitter_apply(fake, dust.U32, 4, 4, 4, 0, dust.GAUSSIAN, 0, 1.0, 0, NULL) == dust.ERR_INVALID_ARG
+
+
+def test_scan_and_weighting_reject_bad_arguments(L):
+    fake = C.c_void_p(1 << 20)
+    assert L.dust_credit_scan(fake, 4, 8, fake, 1, 1.5, 1, fake, fake, 1 << 20, NULL) == dust.ERR_INVALID_ARG
+    assert L.dust_credit_scan(fake, 0, 8, fake, 1, 0.5, 1, fake, fake, 1 << 20, NULL) == dust.ERR_INVALID_ARG
+    assert L.dust_credit_scan(fake, 4, 8, fake, 1, 0.5, 1, fake, NULL, 0, NULL) == dust.ERR_WORKSPACE
+    assert L.dust_error_estimate(fake, 4, 8, 8, 0, dust.GAUSSIAN, 0, 0.0, 0, fake, dust.F32, NULL) == dust.ERR_INVALID_ARG
+    assert L.dust_error_estimate(fake, 3, 8, 8, 0, dust.GAUSSIAN, 0, 1.0, dust.ANTITHETIC, fake, dust.F32, NULL) == dust.ERR_INVALID_ARG
+    assert L.dust_error_estimate(fake, 4, 8, 8, 0, dust.GAUSSIAN, 0, 1.0, 0, fake, dust.U32, NULL) == dust.ERR_INVALID_ARG

@@ -1,0 +1,232 @@
+"""GPU parity of the reward weighting and of the whole estimator (through the
+C ABI) against the fp64 oracle.
+
+Tolerances: g within 1e-5 normwise relative (fp32 output); GW within 1e-5
+relative Frobenius on the fp32 path and 1e-2 with bf16 X (g rounded to bf16
+before the contraction on the tensor-core paths).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import token_perturbation_estimator_gb300 as dust
+import workloads as wl
+from helpers import bf16_round, cuda, offsets_from_lengths, random_lengths, rel_fro
+
+pytestmark = pytest.mark.gpu
+
+
+# ------------------------------------------------------------ weighting --
+
+W_CASES = [
+    # K, T, d_out, kind, draw_begin, flags
+    (1, 1, 1, 0, 0, 0),
+    (4, 9, 7, 1, 0, 0),
+    (8, 100, 256, 1, 8, dust.ANTITHETIC),
+    (3, 257, 300, 0, 5, 0),
+    (64, 64, 1000, 0, 0, 0),
+    (65, 31, 513, 1, 123, 0),
+    (16, 200, 2048, 1, 0, 0),
+    (130, 17, 64, 0, 2, dust.ANTITHETIC),
+]
+
+
+@pytest.mark.parametrize("K,T,d_out,kind,draw_begin,flags", W_CASES)
+def test_error_estimate_parity(K, T, d_out, kind, draw_begin, flags):
+    import torch
+    dev = cuda()
+    rng = np.random.default_rng(K + T + d_out)
+    r = rng.standard_normal((T, K)).astype(np.float32)
+    sigma = 1e-3
+    g = dust.dust_error_estimate(torch.from_numpy(r).to(dev), d_out, 77, kind, draw_begin,
+                                 sigma, flags)
+    want = oracle.error_estimate(r.T, d_out, 77, kind, draw_begin, np.float32(sigma), flags)
+    got = g.cpu().numpy()
+    assert rel_fro(got, want) <= 1e-5
+    gb = dust.dust_error_estimate(torch.from_numpy(r).to(dev), d_out, 77, kind, draw_begin,
+                                  sigma, flags, g_dtype=torch.bfloat16)
+    assert torch.equal(gb, g.to(torch.bfloat16))
+
+
+# -------------------------------------------------------- whole estimator --
+
+def _run(w, X, delta, so, flags, gamma=None, scale=1.0, draw_begin=0):
+    import torch
+    dev = cuda()
+    Xd = torch.from_numpy(X).to(dev)
+    if w.x_dtype == "bf16":
+        Xd = Xd.to(torch.bfloat16)
+    return dust.dust_estimate_gW(Xd, torch.from_numpy(delta).to(dev), w.d_out,
+                                 torch.from_numpy(so).to(dev), w.seed, w.kind, draw_begin,
+                                 w.sigma, w.gamma if gamma is None else gamma, scale, flags)
+
+
+def _inputs(w, planted=True):
+    so = wl.seq_offsets(w)
+    X = wl.make_X(w)
+    if w.x_dtype == "bf16":
+        X = wl.to_bf16_exact(X)
+    if planted:
+        delta = oracle.planted_delta(wl.make_dplant(w), w.seed, w.kind, 0, w.K,
+                                     np.float32(w.sigma), w.curvature,
+                                     wl.make_eps(w)).astype(np.float32)
+    else:
+        delta = wl.marginal_delta(w)
+    return X, delta, so
+
+
+SMALL = [
+    wl.TOY,
+    wl.MLP_UP.scaled(n_seq=3, seq_len=100, d_in=72, d_out=136),
+    wl.QKV_DECAY.scaled(n_seq=2, seq_len=300, d_in=64, d_out=192),
+    wl.SQUARE_R.scaled(n_seq=4, seq_len=64, d_in=128, d_out=128, K=16),
+    wl.SQUARE_G.scaled(n_seq=4, seq_len=64, d_in=120, d_out=40, K=16),
+]
+
+FORCE = [0, dust.FORCE_SIMT, dust.FORCE_UNFUSED, dust.FORCE_FUSED]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+@pytest.mark.parametrize("force", FORCE)
+def test_estimate_gW_small(w, force):
+    X, delta, so = _inputs(w)
+    flags = dust.CENTER | force
+    xd = dust.BF16 if w.x_dtype == "bf16" else dust.F32
+    try:
+        path = dust.dust_estimate_gW_path(w.T, w.d_in, w.d_out, w.K, xd, flags)
+    except dust.DustError as e:
+        assert e.status == dust.ERR_UNSUPPORTED
+        return
+    got = _run(w, X, delta, so, flags).double().cpu().numpy()
+    want = oracle.estimate_gW(X, delta, w.d_out, so, w.seed, w.kind, 0, np.float32(w.sigma),
+                              np.float32(w.gamma), 1.0, oracle.CENTER)
+    tol = 1e-5 if (w.x_dtype == "f32" or path == dust.PATH_SIMT) else 1e-2
+    assert rel_fro(got, want) <= tol, (path, rel_fro(got, want))
+
+
+def test_estimate_matches_brute_force_tiny():
+    import torch
+    dev = cuda()
+    rng = np.random.default_rng(8)
+    lengths = [5, 1, 9, 3]
+    so = offsets_from_lengths(lengths)
+    T, d_in, d_out, K = int(so[-1]), 6, 10, 4
+    X = rng.standard_normal((T, d_in)).astype(np.float32)
+    delta = rng.standard_normal((K, T)).astype(np.float32)
+    for kind in (0, 1):
+        got = dust.dust_estimate_gW(torch.from_numpy(X).to(dev), torch.from_numpy(delta).to(dev),
+                                    d_out, torch.from_numpy(so).to(dev), 3, kind, 2, 0.01, 0.6,
+                                    0.5, dust.CENTER).double().cpu().numpy()
+        want = oracle.bruteforce_gW(X, delta, d_out, so, 3, kind, 2, np.float32(0.01),
+                                    np.float32(0.6), 0.5, oracle.CENTER)
+        assert rel_fro(got, want) <= 1e-5
+
+
+def test_deterministic_and_accumulate():
+    import torch
+    dev = cuda()
+    w = wl.MLP_UP.scaled(n_seq=4, seq_len=256, d_in=128, d_out=256)
+    X, delta, so = _inputs(w, planted=False)
+    a = _run(w, X, delta, so, dust.CENTER)
+    b = _run(w, X, delta, so, dust.CENTER)
+    assert torch.equal(a, b)
+    base = torch.randn_like(a)
+    acc = base.clone()
+    Xd = torch.from_numpy(X).to(dev).to(torch.bfloat16)
+    dust.dust_estimate_gW(Xd, torch.from_numpy(delta).to(dev), w.d_out,
+                          torch.from_numpy(so).to(dev), w.seed, w.kind, 0, w.sigma, w.gamma,
+                          1.0, dust.CENTER | dust.ACCUMULATE, gW=acc)
+    assert torch.allclose(acc, base + a, rtol=1e-6, atol=1e-6 * a.abs().max().item())
+
+
+def test_empty_token_set():
+    import torch
+    dev = cuda()
+    X = torch.empty((0, 16), dtype=torch.bfloat16, device=dev)
+    delta = torch.empty((4, 0), dtype=torch.float32, device=dev)
+    so = torch.zeros(1, dtype=torch.int32, device=dev)
+    gW = torch.full((8, 16), 3.0, device=dev)
+    dust.dust_estimate_gW(X, delta, 8, so, 0, 1, 0, 1e-3, 0.0, 1.0, dust.CENTER, gW=gW)
+    assert torch.count_nonzero(gW).item() == 0
+    gW.fill_(3.0)
+    dust.dust_estimate_gW(X, delta, 8, so, 0, 1, 0, 1e-3, 0.0, 1.0,
+                          dust.CENTER | dust.ACCUMULATE, gW=gW)
+    assert torch.all(gW == 3.0)
+
+
+@pytest.mark.parametrize("gamma", [0.0, 0.9])
+def test_antithetic_cancels_curvature_on_gpu(gamma):
+    """GPU version of the even-order cancellation: with antithetic pairs the
+    curvature term of the planted loss leaves GW unchanged (to rounding)."""
+    import torch
+    dev = cuda()
+    rng = np.random.default_rng(21)
+    T, d_in, d_out, K, sigma = 512, 32, 48, 8, 0.05
+    so = offsets_from_lengths([200, 312])
+    dp = rng.standard_normal((T, d_out))
+    X = rng.standard_normal((T, d_in)).astype(np.float32)
+    f = oracle.ANTITHETIC
+    lin = oracle.planted_delta(dp, 4, 1, 0, K, sigma, curv=0.0, flags=f).astype(np.float32)
+    quad = oracle.planted_delta(dp, 4, 1, 0, K, sigma, curv=1.0, flags=f).astype(np.float32)
+    outs = []
+    for d in (lin, quad):
+        outs.append(dust.dust_estimate_gW(torch.from_numpy(X).to(dev), torch.from_numpy(d).to(dev),
+                                          d_out, torch.from_numpy(so).to(dev), 4, 1, 0, sigma,
+                                          gamma, 1.0, dust.CENTER | dust.ANTITHETIC)
+                    .double().cpu().numpy())
+    assert rel_fro(outs[1], outs[0]) <= 1e-4
+
+
+def test_sequence_sharding_sums_to_whole():
+    """Token sharding by whole sequences (the multi-GPU split): the scan never
+    crosses a sequence and the hash uses global token indices, so per-shard
+    estimates over the shards' rows sum to the unsharded estimate. Emulated
+    here on one GPU with zero-padded shards."""
+    import torch
+    dev = cuda()
+    rng = np.random.default_rng(22)
+    lengths = [100, 60, 150, 90]
+    so = offsets_from_lengths(lengths)
+    T, d_in, d_out, K = int(so[-1]), 24, 40, 6
+    X = rng.standard_normal((T, d_in)).astype(np.float32)
+    delta = rng.standard_normal((K, T)).astype(np.float32)
+    full = dust.dust_estimate_gW(torch.from_numpy(X).to(dev), torch.from_numpy(delta).to(dev),
+                                 d_out, torch.from_numpy(so).to(dev), 9, 1, 0, 0.01, 0.9, 1.0,
+                                 dust.CENTER)
+    acc = torch.zeros_like(full)
+    for lo, hi in ((0, 2), (2, 4)):
+        Xs = np.zeros_like(X)
+        t0, t1 = so[lo], so[hi]
+        Xs[t0:t1] = X[t0:t1]
+        dust.dust_estimate_gW(torch.from_numpy(Xs).to(dev), torch.from_numpy(delta).to(dev),
+                              d_out, torch.from_numpy(so).to(dev), 9, 1, 0, 0.01, 0.9, 1.0,
+                              dust.CENTER | dust.ACCUMULATE, gW=acc)
+    assert rel_fro(acc.cpu().numpy(), full.cpu().numpy()) <= 1e-6
+
+
+# ----------------------------------------------- full sizes, sampled entries --
+
+FULL = [wl.TOY, wl.MLP_UP, wl.QKV_DECAY, wl.SQUARE_R, wl.SQUARE_G]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("w", FULL, ids=lambda w: w.name)
+def test_estimate_gW_full_size_sampled(w):
+    """The measured workloads at full size, in the default launch
+    configuration: 64 sampled GW entries against the oracle, each computed
+    one by one from the full column of g."""
+    planted = w.element_draws <= 1_000_000_000
+    X, delta, so = _inputs(w, planted=planted)
+    got = _run(w, X, delta, so, dust.CENTER).double().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    rng = np.random.default_rng(3)
+    n = 64
+    chan = rng.integers(0, w.d_out, n)
+    col = rng.integers(0, w.d_in, n)
+    chan[:2] = [0, w.d_out - 1]
+    col[:2] = [0, w.d_in - 1]
+    r = oracle.credit(delta, so, np.float32(w.gamma), oracle.CENTER)
+    want = oracle.gW_entries(X, r, w.d_out, chan, col, w.seed, w.kind, 0, np.float32(w.sigma),
+                             1.0, oracle.CENTER)
+    tol = 1e-5 if w.x_dtype == "f32" else 1e-2
+    assert rel_fro(got[chan, col], want) <= tol

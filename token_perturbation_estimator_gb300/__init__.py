@@ -1,0 +1,262 @@
+"""Python binding of the GB300 Dust estimator library (``include/dust.h``).
+
+Argument marshalling only: each function passes raw device pointers, sizes and
+the current CUDA stream to the C ABI of ``lib/libdust_gb300.so``; every step
+of the computation runs in that library's CUDA kernels. PyTorch supplies
+device memory and streams. There is no fallback: if the library is missing
+the import of a function raises.
+
+Functions keep the C names: ``dust_noise``, ``dust_jitter_apply``,
+``dust_credit_scan``, ``dust_error_estimate``, ``dust_estimate_gW``,
+``dust_estimate_gW_host``, ``dust_last_error`` (plus the workspace queries).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import re
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "lib", "libdust_gb300.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "dust.h")
+
+# dust_status
+OK, ERR_INVALID_ARG, ERR_RANGE, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE = range(7)
+# dust_noise_kind
+RADEMACHER, GAUSSIAN, RAW_WORDS = 0, 1, 2
+# dust_dtype
+F32, BF16, U32 = 0, 1, 2
+# flags
+CENTER, ANTITHETIC, ACCUMULATE = 1, 2, 4
+FORCE_UNFUSED, FORCE_FUSED, WORD_STREAM1, FORCE_SIMT = 8, 16, 32, 64
+# dust_path
+PATH_FUSED_TC, PATH_UNFUSED_TC, PATH_SIMT = 1, 2, 3
+
+
+class DustError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__("%s: %s" % (where, status_string(status)))
+
+
+_lib = None
+
+
+def _signatures():
+    i32, i64, u32, u64, f32 = C.c_int32, C.c_int64, C.c_uint32, C.c_uint64, C.c_float
+    P, SZ, PSZ = C.c_void_p, C.c_size_t, C.POINTER(C.c_size_t)
+    return {
+        "dust_status_string": (C.c_char_p, [i32]),
+        "dust_version": (i32, []),
+        "dust_noise": (i32, [P, i32, u64, i32, i64, i64, i64, i64, u32, P]),
+        "dust_jitter_apply": (i32, [P, i32, i64, i64, i64, u64, i32, i64, f32, u32, P]),
+        "dust_credit_scan_workspace": (i32, [PSZ, i64, i64]),
+        "dust_credit_scan": (i32, [P, i64, i64, P, i64, f32, u32, P, P, SZ, P]),
+        "dust_error_estimate": (i32, [P, i64, i64, i64, u64, i32, i64, f32, u32, P, i32, P]),
+        "dust_estimate_gW_workspace": (i32, [PSZ, i64, i64, i64, i64, i32, u32]),
+        "dust_estimate_gW": (i32, [P, i32, i64, i64, P, i64, i64, P, i64, u64, i32, i64, f32,
+                                   f32, f32, u32, P, P, SZ, P]),
+        "dust_estimate_gW_path": (i32, [i64, i64, i64, i64, i32, u32]),
+        "dust_estimate_gW_host": (i32, [P, P, i32, i64, i64, P, P, i64, i64, P, P, i64, u64,
+                                        i32, i64, f32, f32, f32, u32, P, P, P, SZ, P]),
+        "dust_last_error": (i32, [P]),
+        "dust_profile_enable": (i32, [i32]),
+        "dust_profile_read": (i32, [P, i32]),
+    }
+
+
+def lib():
+    """The loaded C library. Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError("libdust_gb300.so is not built (run __graft_entry__.build() or "
+                              "python token_perturbation_estimator_gb300/build.py)")
+        L = C.CDLL(LIB_PATH)
+        for name, (res, args) in _signatures().items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def header_functions():
+    """Names of the functions declared in include/dust.h."""
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dust_[a-zA-Z0-9_]+)\s*\(", text)))
+
+
+def status_string(status: int) -> str:
+    return lib().dust_status_string(int(status)).decode()
+
+
+def _check(st, where):
+    if st != OK:
+        raise DustError(st, where)
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t):
+    return C.c_void_p(t.data_ptr()) if t is not None else C.c_void_p(0)
+
+
+def _dtype_code(t):
+    import torch
+    return {torch.float32: F32, torch.bfloat16: BF16, torch.int32: U32,
+            torch.uint32: U32}[t.dtype]
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("expected a CUDA tensor")
+        if t is not None and not t.is_contiguous():
+            raise ValueError("expected a contiguous tensor")
+
+
+# ------------------------------------------------------------------ calls --
+
+def dust_noise(out, seed, kind, draw_begin, n_draws, T, d_out, flags=0, stream=None):
+    _need_cuda(out)
+    _check(lib().dust_noise(_ptr(out), _dtype_code(out), seed, kind, draw_begin, n_draws, T,
+                            d_out, flags, _stream(stream)), "dust_noise")
+    return out
+
+
+def dust_jitter_apply(y, seed, kind, draw, sigma, flags=0, stream=None):
+    """y: CUDA tensor [T, d_out] (row stride may exceed d_out)."""
+    if not y.is_cuda or y.dim() != 2 or y.stride(1) != 1:
+        raise ValueError("y must be a CUDA [T, d_out] tensor with unit column stride")
+    T, d_out = y.shape
+    _check(lib().dust_jitter_apply(_ptr(y), _dtype_code(y), y.stride(0), T, d_out, seed, kind,
+                                   draw, float(sigma), flags, _stream(stream)),
+           "dust_jitter_apply")
+    return y
+
+
+def dust_credit_scan_workspace(K, T):
+    n = C.c_size_t(0)
+    _check(lib().dust_credit_scan_workspace(C.byref(n), K, T), "dust_credit_scan_workspace")
+    return n.value
+
+
+def _workspace(nbytes, device):
+    import torch
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def dust_credit_scan(delta, seq_offsets, gamma, flags=CENTER, r=None, workspace=None,
+                     stream=None):
+    """delta: f32 [K, T]; seq_offsets: i32 [n_seq+1]; returns r f32 [T, K]."""
+    import torch
+    _need_cuda(delta, seq_offsets)
+    K, T = delta.shape
+    if r is None:
+        r = torch.empty((T, K), dtype=torch.float32, device=delta.device)
+    need = dust_credit_scan_workspace(K, T)
+    if workspace is None:
+        workspace = _workspace(need, delta.device)
+    _check(lib().dust_credit_scan(_ptr(delta), K, T, _ptr(seq_offsets), seq_offsets.numel() - 1,
+                                  float(gamma), flags, _ptr(r), _ptr(workspace),
+                                  workspace.numel(), _stream(stream)), "dust_credit_scan")
+    return r
+
+
+def dust_error_estimate(r, d_out, seed, kind, draw_begin, sigma, flags=0, g=None,
+                        g_dtype=None, stream=None):
+    """r: f32 [T, K]; returns g [T, d_out] (f32 unless g_dtype=torch.bfloat16)."""
+    import torch
+    _need_cuda(r)
+    T, K = r.shape
+    if g is None:
+        g = torch.empty((T, d_out), dtype=g_dtype or torch.float32, device=r.device)
+    _check(lib().dust_error_estimate(_ptr(r), K, T, d_out, seed, kind, draw_begin, float(sigma),
+                                     flags, _ptr(g), _dtype_code(g), _stream(stream)),
+           "dust_error_estimate")
+    return g
+
+
+def dust_estimate_gW_workspace(T, d_in, d_out, K, x_dtype, flags=CENTER):
+    n = C.c_size_t(0)
+    _check(lib().dust_estimate_gW_workspace(C.byref(n), T, d_in, d_out, K, x_dtype, flags),
+           "dust_estimate_gW_workspace")
+    return n.value
+
+
+def dust_estimate_gW_path(T, d_in, d_out, K, x_dtype, flags=CENTER):
+    p = lib().dust_estimate_gW_path(T, d_in, d_out, K, x_dtype, flags)
+    if p < 0:
+        raise DustError(-p, "dust_estimate_gW_path")
+    return p
+
+
+def dust_estimate_gW(X, delta, d_out, seq_offsets, seed, kind, draw_begin, sigma, gamma,
+                     scale=1.0, flags=CENTER, gW=None, workspace=None, stream=None):
+    """X: [T, d_in] bf16 or f32; delta: f32 [K, T]; returns gW f32 [d_out, d_in]."""
+    import torch
+    _need_cuda(X, delta, seq_offsets, gW)
+    T, d_in = X.shape
+    K = delta.shape[0]
+    xd = _dtype_code(X)
+    if gW is None:
+        gW = torch.empty((d_out, d_in), dtype=torch.float32, device=X.device)
+    need = dust_estimate_gW_workspace(T, d_in, d_out, K, xd, flags)
+    if workspace is None:
+        workspace = _workspace(need, X.device)
+    _check(lib().dust_estimate_gW(_ptr(X), xd, T, d_in, _ptr(delta), K, d_out,
+                                  _ptr(seq_offsets), seq_offsets.numel() - 1, seed, kind,
+                                  draw_begin, float(sigma), float(gamma), float(scale), flags,
+                                  _ptr(gW), _ptr(workspace), workspace.numel(),
+                                  _stream(stream)), "dust_estimate_gW")
+    return gW
+
+
+def dust_estimate_gW_host(X_host, X_dev, delta_host, delta_dev, seq_host, seq_dev, gW_host,
+                          gW_dev, d_out, seed, kind, draw_begin, sigma, gamma, scale=1.0,
+                          flags=CENTER, workspace=None, stream=None):
+    """Host-buffer variant: *_host are CPU tensors (pinned for async copies),
+    *_dev are CUDA staging tensors of the same shapes. The caller
+    synchronises the stream before reading gW_host."""
+    T, d_in = X_host.shape
+    K = delta_host.shape[0]
+    xd = _dtype_code(X_host)
+    need = dust_estimate_gW_workspace(T, d_in, d_out, K, xd, flags)
+    if workspace is None:
+        workspace = _workspace(need, X_dev.device)
+    _check(lib().dust_estimate_gW_host(
+        _ptr(X_host), _ptr(X_dev), xd, T, d_in, _ptr(delta_host), _ptr(delta_dev), K, d_out,
+        _ptr(seq_host), _ptr(seq_dev), seq_host.numel() - 1, seed, kind, draw_begin,
+        float(sigma), float(gamma), float(scale), flags, _ptr(gW_host), _ptr(gW_dev),
+        _ptr(workspace), workspace.numel(), _stream(stream)), "dust_estimate_gW_host")
+    return gW_host
+
+
+def dust_last_error(stream=None):
+    return int(lib().dust_last_error(_stream(stream)))
+
+
+class _ProfileEntry(C.Structure):
+    _fields_ = [("name", C.c_char * 32), ("launches", C.c_int64), ("total_ms", C.c_double)]
+
+
+def dust_profile_enable(on=True):
+    _check(lib().dust_profile_enable(1 if on else 0), "dust_profile_enable")
+
+
+def dust_profile_read():
+    """{kernel family: (launches, total_ms)} since the last read."""
+    buf = (_ProfileEntry * 32)()
+    n = lib().dust_profile_read(C.cast(buf, C.c_void_p), 32)
+    if n < 0:
+        raise DustError(-n, "dust_profile_read")
+    return {buf[i].name.decode(): (int(buf[i].launches), float(buf[i].total_ms))
+            for i in range(n)}

@@ -1,0 +1,321 @@
+// C ABI (include/dust.h): argument validation, workspace layout and dispatch.
+// Everything is enqueued on the caller's stream; nothing here allocates
+// device memory or synchronises, except dust_last_error.
+#include <cmath>
+#include <cstring>
+
+#include "../../include/dust.h"
+#include "internal.cuh"
+
+using namespace dust;
+
+namespace {
+
+constexpr uint32_t kKnownFlags = DUST_CENTER | DUST_ANTITHETIC | DUST_ACCUMULATE |
+                                 DUST_FORCE_UNFUSED | DUST_FORCE_FUSED | DUST_WORD_STREAM1 |
+                                 DUST_FORCE_SIMT;
+
+size_t a256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+bool finite(float x) { return std::isfinite(x); }
+
+int popcount3(uint32_t f) {
+    return ((f & DUST_FORCE_UNFUSED) ? 1 : 0) + ((f & DUST_FORCE_FUSED) ? 1 : 0) +
+           ((f & DUST_FORCE_SIMT) ? 1 : 0);
+}
+
+dust_status counter_ok(int64_t T, int64_t d_out) {
+    if (T < 0 || d_out < 0) return DUST_ERR_INVALID_ARG;
+    if (d_out > 0 && T > DUST_MAX_COUNTER / d_out) return DUST_ERR_RANGE;
+    return DUST_OK;
+}
+
+dust_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DUST_OK : DUST_ERR_CUDA; }
+
+// Shape/flag validation shared by the estimator entry points.
+dust_status check_estimate(int64_t T, int64_t d_in, int64_t d_out, int64_t K, dust_dtype x_dtype,
+                           uint32_t flags) {
+    if (T < 0 || d_in < 0 || d_out < 0) return DUST_ERR_INVALID_ARG;
+    if (K < 1) return DUST_ERR_INVALID_ARG;
+    if (K > DUST_MAX_DRAWS) return DUST_ERR_RANGE;
+    if (x_dtype != DUST_F32 && x_dtype != DUST_BF16) return DUST_ERR_INVALID_ARG;
+    if (flags & ~kKnownFlags) return DUST_ERR_INVALID_ARG;
+    if (flags & DUST_WORD_STREAM1) return DUST_ERR_INVALID_ARG;
+    if (popcount3(flags) > 1) return DUST_ERR_INVALID_ARG;
+    if ((flags & DUST_ANTITHETIC) && (K & 1)) return DUST_ERR_INVALID_ARG;
+    dust_status st = counter_ok(T, d_out);
+    if (st != DUST_OK) return st;
+    if (T > 0 && d_in > 0 && T > (int64_t(1) << 40) / d_in) return DUST_ERR_RANGE;
+    return DUST_OK;
+}
+
+int choose_path(int64_t T, int64_t d_in, int64_t d_out, int64_t K, dust_dtype x_dtype,
+                uint32_t flags) {
+    (void)T;
+    (void)d_in;
+    (void)d_out;
+    (void)K;
+    (void)x_dtype;
+    (void)flags;
+    return DUST_PATH_SIMT;
+}
+
+struct Layout {
+    size_t scan = 0, g = 0, gemm = 0, total = 0;
+    int path = DUST_PATH_SIMT;
+    int g_bf16 = 0;
+};
+
+Layout layout(int64_t T, int64_t d_in, int64_t d_out, int64_t K, dust_dtype x_dtype,
+              uint32_t flags) {
+    Layout L;
+    L.path = choose_path(T, d_in, d_out, K, x_dtype, flags);
+    L.scan = a256(scan_workspace_bytes(K, T));
+    L.g_bf16 = 0;
+    L.g = a256(static_cast<size_t>(T) * static_cast<size_t>(d_out) * (L.g_bf16 ? 2 : 4));
+    L.gemm = a256(simt_gemm_workspace_bytes(T, d_in, d_out));
+    L.total = L.scan + L.g + L.gemm;
+    if (L.total == 0) L.total = 256;
+    return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dust_status_string(dust_status s) {
+    switch (s) {
+        case DUST_OK: return "DUST_OK";
+        case DUST_ERR_INVALID_ARG: return "DUST_ERR_INVALID_ARG: invalid argument";
+        case DUST_ERR_RANGE: return "DUST_ERR_RANGE: size beyond a documented limit";
+        case DUST_ERR_UNSUPPORTED: return "DUST_ERR_UNSUPPORTED: not supported by this build";
+        case DUST_ERR_CUDA: return "DUST_ERR_CUDA: a CUDA call or launch failed";
+        case DUST_ERR_TIMEOUT: return "DUST_ERR_TIMEOUT: a device-side bounded wait ran out";
+        case DUST_ERR_WORKSPACE: return "DUST_ERR_WORKSPACE: workspace missing, small or misaligned";
+    }
+    return "unknown dust_status";
+}
+
+int32_t dust_version(void) { return 100; }
+
+dust_status dust_noise(void* out, dust_dtype out_dtype, uint64_t seed, dust_noise_kind kind,
+                       int64_t draw_begin, int64_t n_draws, int64_t T, int64_t d_out,
+                       uint32_t flags, void* stream) {
+    if (draw_begin < 0 || n_draws < 0) return DUST_ERR_INVALID_ARG;
+    if (n_draws > DUST_MAX_DRAWS) return DUST_ERR_RANGE;
+    dust_status st = counter_ok(T, d_out);
+    if (st != DUST_OK) return st;
+    if (flags & ~(DUST_ANTITHETIC | DUST_WORD_STREAM1)) return DUST_ERR_INVALID_ARG;
+    int out_kind;
+    if (kind == DUST_NOISE_RAW_WORDS) {
+        if (out_dtype != DUST_U32) return DUST_ERR_INVALID_ARG;
+        out_kind = 2;
+    } else if (kind == DUST_NOISE_RADEMACHER || kind == DUST_NOISE_GAUSSIAN) {
+        if (out_dtype == DUST_F32) out_kind = 0;
+        else if (out_dtype == DUST_BF16) out_kind = 1;
+        else return DUST_ERR_INVALID_ARG;
+        if (flags & DUST_WORD_STREAM1) return DUST_ERR_INVALID_ARG;
+    } else {
+        return DUST_ERR_INVALID_ARG;
+    }
+    if (draw_begin > (int64_t(1) << 31) - n_draws) return DUST_ERR_RANGE;
+    if (n_draws * T * d_out == 0) return DUST_OK;
+    if (!out) return DUST_ERR_INVALID_ARG;
+    return cuda_status(launch_noise(out, out_kind, seed, static_cast<int>(kind), draw_begin,
+                                    n_draws, T, d_out, flags,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+dust_status dust_jitter_apply(void* y, dust_dtype y_dtype, int64_t ld_y, int64_t T,
+                              int64_t d_out, uint64_t seed, dust_noise_kind kind, int64_t draw,
+                              float sigma, uint32_t flags, void* stream) {
+    dust_status st = counter_ok(T, d_out);
+    if (st != DUST_OK) return st;
+    if (ld_y < d_out || draw < 0) return DUST_ERR_INVALID_ARG;
+    if (draw >= (int64_t(1) << 31)) return DUST_ERR_RANGE;
+    if (kind != DUST_NOISE_RADEMACHER && kind != DUST_NOISE_GAUSSIAN) return DUST_ERR_INVALID_ARG;
+    if (y_dtype != DUST_F32 && y_dtype != DUST_BF16) return DUST_ERR_INVALID_ARG;
+    if (flags & ~DUST_ANTITHETIC) return DUST_ERR_INVALID_ARG;
+    if (!finite(sigma)) return DUST_ERR_INVALID_ARG;
+    if (T * d_out == 0) return DUST_OK;
+    if (!y) return DUST_ERR_INVALID_ARG;
+    return cuda_status(launch_jitter(y, y_dtype == DUST_BF16, ld_y, T, d_out, seed,
+                                     static_cast<int>(kind), draw, sigma, flags,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+dust_status dust_credit_scan_workspace(size_t* bytes, int64_t K, int64_t T) {
+    if (!bytes || K < 1 || T < 0) return DUST_ERR_INVALID_ARG;
+    if (K > DUST_MAX_DRAWS) return DUST_ERR_RANGE;
+    // r lives in the caller's output; the rest in the workspace.
+    *bytes = a256(scan_workspace_bytes(K, T)) + 256;
+    return DUST_OK;
+}
+
+dust_status dust_credit_scan(const float* delta, int64_t K, int64_t T,
+                             const int32_t* seq_offsets, int64_t n_seq, float gamma,
+                             uint32_t flags, float* r, void* workspace, size_t ws_bytes,
+                             void* stream) {
+    if (K < 1 || T < 0 || n_seq < 0) return DUST_ERR_INVALID_ARG;
+    if (K > DUST_MAX_DRAWS) return DUST_ERR_RANGE;
+    if (flags & ~DUST_CENTER) return DUST_ERR_INVALID_ARG;
+    if (!finite(gamma) || std::fabs(gamma) > 1.0f) return DUST_ERR_INVALID_ARG;
+    if (T > 0 && (n_seq < 1 || n_seq > T)) return DUST_ERR_INVALID_ARG;
+    if (T == 0) return DUST_OK;
+    if (!delta || !seq_offsets || !r) return DUST_ERR_INVALID_ARG;
+    size_t need = 0;
+    dust_credit_scan_workspace(&need, K, T);
+    if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
+        return DUST_ERR_WORKSPACE;
+    ScanBuffers b = scan_carve(workspace, K, T);
+    b.r = r;  // scan straight into the caller's output
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_scan(delta, K, T, seq_offsets, n_seq, gamma,
+                                (flags & DUST_CENTER) != 0, b, s);
+    if (e == cudaSuccess) e = launch_scan_fixup(b, K, T, s);
+    return cuda_status(e);
+}
+
+dust_status dust_error_estimate(const float* r, int64_t K, int64_t T, int64_t d_out,
+                                uint64_t seed, dust_noise_kind kind, int64_t draw_begin,
+                                float sigma, uint32_t flags, void* g, dust_dtype g_dtype,
+                                void* stream) {
+    if (K < 1 || draw_begin < 0) return DUST_ERR_INVALID_ARG;
+    if (K > DUST_MAX_DRAWS) return DUST_ERR_RANGE;
+    dust_status st = counter_ok(T, d_out);
+    if (st != DUST_OK) return st;
+    if (kind != DUST_NOISE_RADEMACHER && kind != DUST_NOISE_GAUSSIAN) return DUST_ERR_INVALID_ARG;
+    if (g_dtype != DUST_F32 && g_dtype != DUST_BF16) return DUST_ERR_INVALID_ARG;
+    if (flags & ~(DUST_CENTER | DUST_ANTITHETIC)) return DUST_ERR_INVALID_ARG;
+    if ((flags & DUST_ANTITHETIC) && ((K & 1) || (draw_begin & 1))) return DUST_ERR_INVALID_ARG;
+    if (!finite(sigma) || sigma == 0.0f) return DUST_ERR_INVALID_ARG;
+    if (draw_begin > (int64_t(1) << 31) - K) return DUST_ERR_RANGE;
+    if (T * d_out == 0) return DUST_OK;
+    if (!r || !g) return DUST_ERR_INVALID_ARG;
+    ScanBuffers b{};
+    b.r = const_cast<float*>(r);
+    const float coef = static_cast<float>(-1.0 / (static_cast<double>(K) * sigma));
+    return cuda_status(launch_weight(b, false, K, T, d_out, seed, static_cast<int>(kind),
+                                     draw_begin, coef, (flags & DUST_ANTITHETIC) != 0, g,
+                                     g_dtype == DUST_BF16, static_cast<cudaStream_t>(stream)));
+}
+
+dust_status dust_estimate_gW_workspace(size_t* bytes, int64_t T, int64_t d_in, int64_t d_out,
+                                       int64_t K, dust_dtype x_dtype, uint32_t flags) {
+    if (!bytes) return DUST_ERR_INVALID_ARG;
+    dust_status st = check_estimate(T, d_in, d_out, K, x_dtype, flags);
+    if (st != DUST_OK) return st;
+    *bytes = layout(T, d_in, d_out, K, x_dtype, flags).total;
+    return DUST_OK;
+}
+
+int32_t dust_estimate_gW_path(int64_t T, int64_t d_in, int64_t d_out, int64_t K,
+                              dust_dtype x_dtype, uint32_t flags) {
+    dust_status st = check_estimate(T, d_in, d_out, K, x_dtype, flags);
+    if (st != DUST_OK) return -static_cast<int32_t>(st);
+    return choose_path(T, d_in, d_out, K, x_dtype, flags);
+}
+
+dust_status dust_estimate_gW(const void* X, dust_dtype x_dtype, int64_t T, int64_t d_in,
+                             const float* delta, int64_t K, int64_t d_out,
+                             const int32_t* seq_offsets, int64_t n_seq, uint64_t seed,
+                             dust_noise_kind kind, int64_t draw_begin, float sigma, float gamma,
+                             float scale, uint32_t flags, float* gW, void* workspace,
+                             size_t ws_bytes, void* stream) {
+    dust_status st = check_estimate(T, d_in, d_out, K, x_dtype, flags);
+    if (st != DUST_OK) return st;
+    if (kind != DUST_NOISE_RADEMACHER && kind != DUST_NOISE_GAUSSIAN) return DUST_ERR_INVALID_ARG;
+    if (draw_begin < 0) return DUST_ERR_INVALID_ARG;
+    if (draw_begin > (int64_t(1) << 31) - K) return DUST_ERR_RANGE;
+    if ((flags & DUST_ANTITHETIC) && (draw_begin & 1)) return DUST_ERR_INVALID_ARG;
+    if (!finite(sigma) || sigma == 0.0f) return DUST_ERR_INVALID_ARG;
+    if (!finite(gamma) || std::fabs(gamma) > 1.0f) return DUST_ERR_INVALID_ARG;
+    if (!finite(scale)) return DUST_ERR_INVALID_ARG;
+    if (T > 0 && (n_seq < 1 || n_seq > T)) return DUST_ERR_INVALID_ARG;
+    if (n_seq < 0) return DUST_ERR_INVALID_ARG;
+    if (d_out * d_in == 0) return DUST_OK;
+    if (!gW) return DUST_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool acc = (flags & DUST_ACCUMULATE) != 0;
+    if (T == 0) return acc ? DUST_OK : cuda_status(launch_zero(gW, d_out * d_in, s));
+    if (!X || !delta || !seq_offsets) return DUST_ERR_INVALID_ARG;
+    const size_t esz = (x_dtype == DUST_BF16) ? 2 : 4;
+    if (reinterpret_cast<uintptr_t>(X) % esz) return DUST_ERR_INVALID_ARG;
+    const Layout L = layout(T, d_in, d_out, K, x_dtype, flags);
+    if (!workspace || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255))
+        return DUST_ERR_WORKSPACE;
+
+    char* ws = static_cast<char*>(workspace);
+    ScanBuffers b = scan_carve(ws, K, T);
+    void* g = ws + L.scan;
+    float* part = reinterpret_cast<float*>(ws + L.scan + L.g);
+    const float coef = static_cast<float>(-1.0 / (static_cast<double>(K) * sigma));
+    const bool anti = (flags & DUST_ANTITHETIC) != 0;
+
+    cudaError_t e = launch_scan(delta, K, T, seq_offsets, n_seq, gamma,
+                                (flags & DUST_CENTER) != 0, b, s);
+    if (e != cudaSuccess) return DUST_ERR_CUDA;
+    e = launch_weight(b, true, K, T, d_out, seed, static_cast<int>(kind), draw_begin, coef, anti,
+                      g, L.g_bf16, s);
+    if (e != cudaSuccess) return DUST_ERR_CUDA;
+    e = launch_simt_gemm(g, L.g_bf16, X, x_dtype == DUST_BF16, T, d_in, d_out, scale, acc, gW,
+                         part, s);
+    return cuda_status(e);
+}
+
+dust_status dust_estimate_gW_host(const void* X_host, void* X_dev, dust_dtype x_dtype, int64_t T,
+                                  int64_t d_in, const float* delta_host, float* delta_dev,
+                                  int64_t K, int64_t d_out, const int32_t* seq_offsets_host,
+                                  int32_t* seq_dev, int64_t n_seq, uint64_t seed,
+                                  dust_noise_kind kind, int64_t draw_begin, float sigma,
+                                  float gamma, float scale, uint32_t flags, float* gW_host,
+                                  float* gW_dev, void* workspace, size_t ws_bytes,
+                                  void* stream) {
+    dust_status st = check_estimate(T, d_in, d_out, K, x_dtype, flags);
+    if (st != DUST_OK) return st;
+    if (n_seq < 0 || (T > 0 && n_seq < 1)) return DUST_ERR_INVALID_ARG;
+    if (d_out * d_in > 0 && (!gW_host || !gW_dev)) return DUST_ERR_INVALID_ARG;
+    if (T > 0 && (!X_host || !X_dev || !delta_host || !delta_dev || !seq_offsets_host ||
+                  !seq_dev))
+        return DUST_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t esz = (x_dtype == DUST_BF16) ? 2 : 4;
+    const size_t gw_bytes = sizeof(float) * static_cast<size_t>(d_out * d_in);
+    if (T > 0) {
+        if (cudaMemcpyAsync(X_dev, X_host, esz * static_cast<size_t>(T * d_in),
+                            cudaMemcpyHostToDevice, s) != cudaSuccess ||
+            cudaMemcpyAsync(delta_dev, delta_host, sizeof(float) * static_cast<size_t>(K * T),
+                            cudaMemcpyHostToDevice, s) != cudaSuccess ||
+            cudaMemcpyAsync(seq_dev, seq_offsets_host, sizeof(int32_t) * (n_seq + 1),
+                            cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return DUST_ERR_CUDA;
+    }
+    if ((flags & DUST_ACCUMULATE) && gw_bytes &&
+        cudaMemcpyAsync(gW_dev, gW_host, gw_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return DUST_ERR_CUDA;
+    st = dust_estimate_gW(X_dev, x_dtype, T, d_in, delta_dev, K, d_out, seq_dev, n_seq, seed,
+                          kind, draw_begin, sigma, gamma, scale, flags, gW_dev, workspace,
+                          ws_bytes, stream);
+    if (st != DUST_OK) return st;
+    if (gw_bytes &&
+        cudaMemcpyAsync(gW_host, gW_dev, gw_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return DUST_ERR_CUDA;
+    return DUST_OK;
+}
+
+dust_status dust_last_error(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return DUST_ERR_CUDA;
+    unsigned int* w = status_word();
+    if (!w) return DUST_ERR_CUDA;
+    unsigned int v = 0;
+    if (cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return DUST_ERR_CUDA;
+    if (v != 0) {
+        const unsigned int z = 0;
+        if (cudaMemcpy(w, &z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess)
+            return DUST_ERR_CUDA;
+    }
+    return static_cast<dust_status>(v);
+}
+
+}  // extern "C"

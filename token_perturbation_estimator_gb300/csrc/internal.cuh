@@ -1,0 +1,95 @@
+// Internal launch interfaces shared by the library's translation units.
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace dust {
+
+// Device address of the status word that kernels with bounded waits set when
+// a wait runs out (0 = ok, otherwise a dust_status value). Looked up once per
+// device; read and cleared by dust_last_error. nullptr if the lookup failed.
+unsigned int* status_word();
+
+// Kernel families timed by dust_profile_read.
+enum Stage {
+    kStageScanLocal, kStageScanCarry, kStageScanFixup, kStageWeight, kStageGemmSimt,
+    kStageReduce, kStageGemmTc, kStageFused, kStageNoise, kStageJitter, kStageZero, kStageCount
+};
+
+// Brackets the launches issued during its lifetime with profiling events
+// (no-op unless profiling is enabled).
+struct ProfScope {
+    ProfScope(int stage, cudaStream_t s);
+    ~ProfScope();
+    ProfScope(const ProfScope&) = delete;
+    ProfScope& operator=(const ProfScope&) = delete;
+    int stage;
+    cudaStream_t s;
+    int slot;
+};
+
+// Token chunk of the credit scan (one CTA, 32 lanes x 8 tokens).
+constexpr int kScanChunk = 256;
+
+// Everything one estimator call needs, resolved on the host.
+struct EstimateArgs {
+    const void* X;
+    int x_bf16;
+    int64_t T, d_in, d_out, K;
+    const float* delta;
+    const int32_t* seq_offsets;
+    int64_t n_seq;
+    uint64_t seed;
+    int kind;
+    int64_t draw_begin;
+    float sigma, gamma, scale;
+    uint32_t flags;
+    float* gW;
+};
+
+// Workspace of the credit scan. All pointers are device memory.
+struct ScanBuffers {
+    float* r;       // [T][K] local (chunk) scan, or final after fix-up
+    float* P;       // [T] product of the decay from t to its chunk's end
+    float* A;       // [n_chunks][K] chunk summary: local r at the chunk start
+    float* B;       // [n_chunks]   chunk summary: decay product over the chunk
+    float* carry;   // [n_chunks][K] true r at the first token after the chunk
+    int64_t n_chunks;
+};
+
+size_t scan_workspace_bytes(int64_t K, int64_t T);
+ScanBuffers scan_carve(void* ws, int64_t K, int64_t T);
+
+cudaError_t launch_noise(void* out, int out_kind /*0 f32, 1 bf16, 2 u32*/, uint64_t seed,
+                         int kind, int64_t draw_begin, int64_t n_draws, int64_t T,
+                         int64_t d_out, uint32_t flags, cudaStream_t s);
+cudaError_t launch_jitter(void* y, int y_bf16, int64_t ld_y, int64_t T, int64_t d_out,
+                          uint64_t seed, int kind, int64_t draw, float sigma, uint32_t flags,
+                          cudaStream_t s);
+
+// Centring + chunk-local scan + chunk carries. After it, r holds chunk-local
+// values; the true r is r[t][i] + P[t] * carry[t / kScanChunk][i].
+cudaError_t launch_scan(const float* delta, int64_t K, int64_t T, const int32_t* seq_offsets,
+                        int64_t n_seq, float gamma, bool center, const ScanBuffers& b,
+                        cudaStream_t s);
+cudaError_t launch_scan_fixup(const ScanBuffers& b, int64_t K, int64_t T, cudaStream_t s);
+
+// g[t][c] = coef * sum_i r[t][i] a_t^(draw_begin+i)[c]; with `fix` the scan
+// fix-up is applied while staging r.
+cudaError_t launch_weight(const ScanBuffers& b, bool fix, int64_t K, int64_t T, int64_t d_out,
+                          uint64_t seed, int kind, int64_t draw_begin, float coef,
+                          bool anti, void* g, int g_bf16, cudaStream_t s);
+
+// CUDA-core contraction: partial[s][c][j] = sum_{t in slice s} g[t][c] x[t][j]
+// followed by gW = scale * sum_s partial (+ gW).
+size_t simt_gemm_workspace_bytes(int64_t T, int64_t d_in, int64_t d_out);
+cudaError_t launch_simt_gemm(const void* g, int g_bf16, const void* X, int x_bf16, int64_t T,
+                             int64_t d_in, int64_t d_out, float scale, bool accumulate,
+                             float* gW, float* partials, cudaStream_t s);
+
+// Fill gW with zeros (T == 0) unless accumulating.
+cudaError_t launch_zero(float* p, int64_t n, cudaStream_t s);
+
+}  // namespace dust

@@ -1,0 +1,162 @@
+// CUDA-core contraction GW[c][j] = scale * sum_t g[t][c] x[t][j] ("Dust: every
+// token is a member of the population", section "Perturb the activations, not
+// the weights", the G_W equation), in fp32 FFMA. It serves the fp32 path and
+// shapes the tensor-core kernels do not take. Deterministic: the token range
+// is cut into fixed slices whose fp32 partials are summed in slice order.
+#include "internal.cuh"
+
+namespace dust {
+
+namespace {
+
+constexpr int kBM = 64, kBN = 64, kBK = 16;
+
+__device__ __forceinline__ float ld(const float* p) { return *p; }
+__device__ __forceinline__ float ld(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+
+template <typename TG, typename TX>
+__global__ void __launch_bounds__(256) k_gemm_simt(const TG* __restrict__ g,
+                                                   const TX* __restrict__ X, int64_t T,
+                                                   int64_t d_in, int64_t d_out, int64_t slice,
+                                                   float* __restrict__ out, float scale,
+                                                   int mode) {
+    __shared__ float sg[kBK][kBM];
+    __shared__ float sx[kBK][kBN];
+    const int tid = threadIdx.x;
+    const int ty = tid >> 4, tx = tid & 15;
+    const int64_t cb = static_cast<int64_t>(blockIdx.y) * kBM;
+    const int64_t jb = static_cast<int64_t>(blockIdx.x) * kBN;
+    const int64_t s = blockIdx.z;
+    const int64_t t_lo = s * slice;
+    const int64_t t_hi = (t_lo + slice < T) ? t_lo + slice : T;
+
+    float acc[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) acc[a][b] = 0.0f;
+
+    for (int64_t t0 = t_lo; t0 < t_hi; t0 += kBK) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int e = tid * 4 + q;
+            const int tt = e / kBM, cc = e % kBM;
+            const int64_t t = t0 + tt;
+            float vg = 0.0f, vx = 0.0f;
+            if (t < t_hi) {
+                if (cb + cc < d_out) vg = ld(g + t * d_out + cb + cc);
+                if (jb + cc < d_in) vx = ld(X + t * d_in + jb + cc);
+            }
+            sg[tt][cc] = vg;
+            sx[tt][cc] = vx;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < kBK; ++k) {
+            float a[4], b[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                a[q] = sg[k][ty * 4 + q];
+                b[q] = sx[k][tx * 4 + q];
+            }
+#pragma unroll
+            for (int p = 0; p < 4; ++p)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[p][q] = fmaf(a[p], b[q], acc[p][q]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const int64_t c = cb + ty * 4 + p;
+        if (c >= d_out) continue;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int64_t j = jb + tx * 4 + q;
+            if (j >= d_in) continue;
+            if (mode == 0) {
+                out[(s * d_out + c) * d_in + j] = acc[p][q];
+            } else if (mode == 1) {
+                out[c * d_in + j] = scale * acc[p][q];
+            } else {
+                out[c * d_in + j] += scale * acc[p][q];
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256) k_reduce(const float* __restrict__ part, int64_t S,
+                                                int64_t n, float scale, int accumulate,
+                                                float* __restrict__ gW) {
+    for (int64_t q = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; q < n;
+         q += (int64_t)gridDim.x * blockDim.x) {
+        float v = 0.0f;
+        for (int64_t s = 0; s < S; ++s) v += part[s * n + q];
+        gW[q] = accumulate ? gW[q] + scale * v : scale * v;
+    }
+}
+
+int64_t slices_for(int64_t T, int64_t d_in, int64_t d_out) {
+    const int64_t tiles = ((d_out + kBM - 1) / kBM) * ((d_in + kBN - 1) / kBN);
+    int64_t S = (2 * 152 + tiles - 1) / tiles;
+    const int64_t max_s = (T + 63) / 64;
+    if (S > max_s) S = max_s;
+    if (S > 64) S = 64;
+    return S < 1 ? 1 : S;
+}
+
+template <typename TG, typename TX>
+cudaError_t run(const void* g, const void* X, int64_t T, int64_t d_in, int64_t d_out,
+                float scale, bool accumulate, float* gW, float* partials, cudaStream_t s) {
+    const int64_t S = slices_for(T, d_in, d_out);
+    int64_t slice = (T + S - 1) / S;
+    slice = (slice + kBK - 1) / kBK * kBK;
+    const int64_t S_used = (T + slice - 1) / slice;
+    dim3 grid(static_cast<unsigned>((d_in + kBN - 1) / kBN),
+              static_cast<unsigned>((d_out + kBM - 1) / kBM), static_cast<unsigned>(S_used));
+    if (S_used == 1) {
+        ProfScope ps(kStageGemmSimt, s);
+        k_gemm_simt<TG, TX><<<grid, 256, 0, s>>>(static_cast<const TG*>(g),
+                                                 static_cast<const TX*>(X), T, d_in, d_out,
+                                                 slice, gW, scale, accumulate ? 2 : 1);
+        return cudaGetLastError();
+    }
+    {
+        ProfScope ps(kStageGemmSimt, s);
+        k_gemm_simt<TG, TX><<<grid, 256, 0, s>>>(static_cast<const TG*>(g),
+                                                 static_cast<const TX*>(X), T, d_in, d_out,
+                                                 slice, partials, scale, 0);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t n = d_out * d_in;
+    int64_t rg = (n + 255) / 256;
+    if (rg > 152 * 16) rg = 152 * 16;
+    ProfScope ps(kStageReduce, s);
+    k_reduce<<<static_cast<unsigned>(rg), 256, 0, s>>>(partials, S_used, n, scale,
+                                                       accumulate ? 1 : 0, gW);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t simt_gemm_workspace_bytes(int64_t T, int64_t d_in, int64_t d_out) {
+    const int64_t S = slices_for(T, d_in, d_out);
+    return S > 1 ? sizeof(float) * static_cast<size_t>(S * d_out * d_in) : 0;
+}
+
+cudaError_t launch_simt_gemm(const void* g, int g_bf16, const void* X, int x_bf16, int64_t T,
+                             int64_t d_in, int64_t d_out, float scale, bool accumulate,
+                             float* gW, float* partials, cudaStream_t s) {
+    if (d_in == 0 || d_out == 0) return cudaSuccess;
+    if (g_bf16 && x_bf16)
+        return run<__nv_bfloat16, __nv_bfloat16>(g, X, T, d_in, d_out, scale, accumulate, gW,
+                                                 partials, s);
+    if (!g_bf16 && !x_bf16)
+        return run<float, float>(g, X, T, d_in, d_out, scale, accumulate, gW, partials, s);
+    if (g_bf16)
+        return run<__nv_bfloat16, float>(g, X, T, d_in, d_out, scale, accumulate, gW, partials, s);
+    return run<float, __nv_bfloat16>(g, X, T, d_in, d_out, scale, accumulate, gW, partials, s);
+}
+
+}  // namespace dust

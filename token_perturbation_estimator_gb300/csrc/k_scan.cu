@@ -1,0 +1,229 @@
+// Centring of the loss reductions and the segmented reverse credit scan
+//   r[t] = c[t] + m[t] * r[t+1],  m[t] = 0 at a sequence's last token, else gamma,
+// ("Dust: every token is a member of the population", section "Perturb the
+// activations, not the weights", the r_t equation, restarted per sequence).
+//
+// The recurrence is affine in r[t+1], and affine maps compose associatively,
+// so it is scanned in three levels:
+//   lane   : 8 consecutive tokens, serial;
+//   warp   : 32 lanes (a 256-token chunk) by a shuffle scan of the lane maps;
+//   chunks : one thread per draw walks the chunk maps from the end (k_carry).
+// A chunk's tokens then take r_true[t] = r_local[t] + P[t] * carry[chunk],
+// with P[t] the product of m from t to the chunk's last token.
+#include "internal.cuh"
+
+namespace dust {
+
+namespace {
+
+constexpr int kDrawGroup = 32;  // draws staged in shared memory at once
+
+// m[t] for the 256 tokens of a chunk: 0 where t is the last token of its
+// sequence (t + 1 is an offset in seq_offsets[1..n_seq]) or t >= T.
+__device__ float decay_of(int64_t t, int64_t T, const int32_t* __restrict__ so, int64_t n_seq,
+                          float gamma) {
+    if (t >= T - 1) return 0.0f;
+    const int64_t key = t + 1;
+    int64_t lo = 1, hi = n_seq;  // search seq_offsets[1..n_seq]
+    while (lo <= hi) {
+        const int64_t mid = (lo + hi) >> 1;
+        const int64_t v = so[mid];
+        if (v == key) return 0.0f;
+        if (v < key) lo = mid + 1; else hi = mid - 1;
+    }
+    return gamma;
+}
+
+__global__ void __launch_bounds__(256) k_scan_local(const float* __restrict__ delta, int64_t K,
+                                                    int64_t T, const int32_t* __restrict__ so,
+                                                    int64_t n_seq, float gamma, int center,
+                                                    float* __restrict__ r, float* __restrict__ P,
+                                                    float* __restrict__ A, float* __restrict__ B) {
+    __shared__ float s_m[kScanChunk];
+    __shared__ float s_mean[kScanChunk];
+    __shared__ float s_c[kDrawGroup][kScanChunk + 1];
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int64_t chunk = blockIdx.x;
+    const int64_t t0 = chunk * kScanChunk;
+    const int64_t t = t0 + tid;
+
+    s_m[tid] = decay_of(t, T, so, n_seq, gamma);
+    float mean = 0.0f;
+    if (center && K > 1 && t < T) {
+        for (int64_t i = 0; i < K; ++i) mean += delta[i * T + t];
+        mean /= static_cast<float>(K);
+    }
+    s_mean[tid] = mean;
+    __syncthreads();
+
+    // Lane maps of the decay products (draw-independent): P for the lane's 8
+    // tokens, then the suffix over the lanes after it.
+    float mloc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) mloc[j] = s_m[lane * 8 + j];
+    float Bl = 1.0f;
+#pragma unroll
+    for (int j = 7; j >= 0; --j) Bl *= mloc[j];
+    // Inclusive suffix product of Bl over lanes >= lane.
+    float Bsuf = Bl;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float o = __shfl_down_sync(0xffffffffu, Bsuf, off);
+        if (lane + off < 32) Bsuf *= o;
+    }
+    float Bnext = __shfl_down_sync(0xffffffffu, Bsuf, 1);
+    if (lane == 31) Bnext = 1.0f;
+    if (warp == 0) {
+        float p = Bnext;
+        for (int j = 7; j >= 0; --j) {
+            p *= mloc[j];
+            const int64_t tt = t0 + lane * 8 + j;
+            if (tt < T) P[tt] = p;
+        }
+        if (lane == 0) B[chunk] = Bsuf;
+    }
+
+    for (int64_t g0 = 0; g0 < K; g0 += kDrawGroup) {
+        const int gn = static_cast<int>(K - g0 < kDrawGroup ? K - g0 : kDrawGroup);
+        // Load the group's centred reductions c = -(delta - mean).
+        for (int k = 0; k < gn; ++k) {
+            float v = 0.0f;
+            if (t < T) v = -(delta[(g0 + k) * T + t] - s_mean[tid]);
+            s_c[k][tid] = v;
+        }
+        __syncthreads();
+        for (int k = warp; k < gn; k += 8) {
+            float cl[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) cl[j] = s_c[k][lane * 8 + j];
+            float x = 0.0f;
+#pragma unroll
+            for (int j = 7; j >= 0; --j) x = cl[j] + mloc[j] * x;
+            // Suffix composition of the lane maps (x_l, Bl).
+            float As = x, Bs = Bl;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float oA = __shfl_down_sync(0xffffffffu, As, off);
+                const float oB = __shfl_down_sync(0xffffffffu, Bs, off);
+                if (lane + off < 32) {
+                    As = fmaf(Bs, oA, As);
+                    Bs *= oB;
+                }
+            }
+            float carry = __shfl_down_sync(0xffffffffu, As, 1);
+            if (lane == 31) carry = 0.0f;
+            x = carry;
+#pragma unroll
+            for (int j = 7; j >= 0; --j) {
+                x = cl[j] + mloc[j] * x;
+                s_c[k][lane * 8 + j] = x;
+            }
+            if (lane == 0) A[chunk * K + g0 + k] = As;
+        }
+        __syncthreads();
+        // Write r_local token-major: r[t][g0 + k].
+        for (int e = tid; e < gn * kScanChunk; e += blockDim.x) {
+            const int tok = e / gn, k = e - tok * gn;
+            const int64_t tt = t0 + tok;
+            if (tt < T) r[tt * K + g0 + k] = s_c[k][tok];
+        }
+        __syncthreads();
+    }
+}
+
+// carry[j][i] = A[j+1][i] + B[j+1] * carry[j+1][i], carry[last] = 0.
+__global__ void __launch_bounds__(256) k_carry(const float* __restrict__ A,
+                                               const float* __restrict__ B, int64_t K,
+                                               int64_t n_chunks, float* __restrict__ carry) {
+    const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    if (i >= K) return;
+    float c = 0.0f;
+    int64_t j = n_chunks - 1;
+    carry[j * K + i] = 0.0f;
+    // Unrolled by 4 so the loads of the next summaries overlap the chain.
+    for (; j >= 4; j -= 4) {
+        const float a0 = A[j * K + i], a1 = A[(j - 1) * K + i];
+        const float a2 = A[(j - 2) * K + i], a3 = A[(j - 3) * K + i];
+        const float b0 = B[j], b1 = B[j - 1], b2 = B[j - 2], b3 = B[j - 3];
+        c = fmaf(b0, c, a0);
+        carry[(j - 1) * K + i] = c;
+        c = fmaf(b1, c, a1);
+        carry[(j - 2) * K + i] = c;
+        c = fmaf(b2, c, a2);
+        carry[(j - 3) * K + i] = c;
+        c = fmaf(b3, c, a3);
+        carry[(j - 4) * K + i] = c;
+    }
+    for (; j >= 1; --j) {
+        c = fmaf(B[j], c, A[j * K + i]);
+        carry[(j - 1) * K + i] = c;
+    }
+}
+
+__global__ void __launch_bounds__(256) k_fixup(float* __restrict__ r, const float* __restrict__ P,
+                                               const float* __restrict__ carry, int64_t K,
+                                               int64_t T) {
+    const int64_t n = K * T;
+    for (int64_t q = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; q < n;
+         q += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = q / K, i = q - t * K;
+        r[q] = fmaf(P[t], carry[(t / kScanChunk) * K + i], r[q]);
+    }
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+size_t scan_workspace_bytes(int64_t K, int64_t T) {
+    const int64_t nc = (T + kScanChunk - 1) / kScanChunk;
+    return align256(sizeof(float) * K * T) + align256(sizeof(float) * T) +
+           2 * align256(sizeof(float) * nc * K) + align256(sizeof(float) * nc);
+}
+
+ScanBuffers scan_carve(void* ws, int64_t K, int64_t T) {
+    ScanBuffers b;
+    b.n_chunks = (T + kScanChunk - 1) / kScanChunk;
+    char* p = static_cast<char*>(ws);
+    b.r = reinterpret_cast<float*>(p);
+    p += align256(sizeof(float) * K * T);
+    b.P = reinterpret_cast<float*>(p);
+    p += align256(sizeof(float) * T);
+    b.A = reinterpret_cast<float*>(p);
+    p += align256(sizeof(float) * b.n_chunks * K);
+    b.carry = reinterpret_cast<float*>(p);
+    p += align256(sizeof(float) * b.n_chunks * K);
+    b.B = reinterpret_cast<float*>(p);
+    return b;
+}
+
+cudaError_t launch_scan(const float* delta, int64_t K, int64_t T, const int32_t* seq_offsets,
+                        int64_t n_seq, float gamma, bool center, const ScanBuffers& b,
+                        cudaStream_t s) {
+    if (T == 0 || K == 0) return cudaSuccess;
+    {
+    ProfScope ps(kStageScanLocal, s);
+    k_scan_local<<<static_cast<unsigned>(b.n_chunks), 256, 0, s>>>(
+        delta, K, T, seq_offsets, n_seq, gamma, center ? 1 : 0, b.r, b.P, b.A, b.B);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    ProfScope ps(kStageScanCarry, s);
+    k_carry<<<static_cast<unsigned>((K + 255) / 256), 256, 0, s>>>(b.A, b.B, K, b.n_chunks,
+                                                                   b.carry);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scan_fixup(const ScanBuffers& b, int64_t K, int64_t T, cudaStream_t s) {
+    const int64_t n = K * T;
+    if (n == 0) return cudaSuccess;
+    int64_t grid = (n + 255) / 256;
+    if (grid > 152 * 32) grid = 152 * 32;
+    ProfScope ps(kStageScanFixup, s);
+    k_fixup<<<static_cast<unsigned>(grid), 256, 0, s>>>(b.r, b.P, b.carry, K, T);
+    return cudaGetLastError();
+}
+
+}  // namespace dust
