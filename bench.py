@@ -217,9 +217,31 @@ def load_peaks():
                 "fallback": True}
 
 
-def traffic_from_profiles(kernel, lib_stamp):
-    """DRAM bytes per launch from a committed ncu capture, if it was taken on
-    the current build of the kernels (else None)."""
+KERNEL_SOURCES = {
+    "weight": ["k_weight.cu", "noise.cuh", "internal.cuh"],
+    "gemm_tc": ["k_gemm_tc.cu", "tc_common.cuh", "internal.cuh"],
+    "fused": ["k_fused.cu", "noise.cuh", "tc_common.cuh", "internal.cuh"],
+}
+
+
+def kernel_source_hash(kernel):
+    import hashlib
+    files = KERNEL_SOURCES.get(kernel)
+    if not files:
+        return None
+    h = hashlib.sha256()
+    for f in files:
+        p = os.path.join(ROOT, "token_perturbation_estimator_gb300", "csrc", f)
+        if not os.path.exists(p):
+            return None
+        with open(p, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profiles(kernel):
+    """DRAM bytes (read + write) per launch from a committed ncu capture, if
+    the kernel's sources are unchanged since the capture (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
@@ -227,7 +249,7 @@ def traffic_from_profiles(kernel, lib_stamp):
     except (OSError, ValueError):
         return None
     e = d.get(kernel)
-    if not e or e.get("build_stamp") != lib_stamp:
+    if not e or e.get("source_hash") != kernel_source_hash(kernel):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -396,10 +418,7 @@ def run_gb300(args):
     top_ms = top[1]["total_ms"] / top[1]["launches"]
     peaks = load_peaks()
     roof = roofline_for(top[0], top_ms, w, peaks, path)
-    stamp_file = os.path.join(ROOT, "token_perturbation_estimator_gb300", "lib",
-                              "libdust_gb300.so.stamp")
-    stamp = open(stamp_file).read().strip() if os.path.exists(stamp_file) else None
-    roof["traffic"] = traffic_from_profiles(top[0], stamp)
+    roof["traffic"] = traffic_from_profiles(top[0])
     breakdown = {k: {"launches": v["launches"],
                      "ms_per_launch": v["total_ms"] / v["launches"],
                      "share": v["total_ms"] / sum(x["total_ms"] for x in prof.values())}

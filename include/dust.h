@@ -173,6 +173,23 @@ dust_status dust_error_estimate(const float* r, int64_t K, int64_t T, int64_t d_
                                 void* stream);
 
 /*
+ * dust_contract_workspace / dust_contract — the contraction on its own (the
+ * G_W equation): GW[c][j] = scale * sum_t g[t][c] x[t][j].
+ *   g       device [T][d_out]; X device [T][d_in]; both DUST_BF16 (tensor
+ *           cores, fp32 accumulation; needs d_in % 8 == 0, d_out % 8 == 0 and
+ *           16-byte aligned bases, otherwise CUDA cores) or both DUST_F32
+ *           (CUDA cores, fp32).
+ *   flags   DUST_ACCUMULATE, DUST_FORCE_SIMT.
+ *   gW      device f32 [d_out][d_in].
+ *   workspace as for dust_estimate_gW (split-token partials).
+ */
+dust_status dust_contract_workspace(size_t* bytes, int64_t T, int64_t d_in, int64_t d_out,
+                                    dust_dtype dtype, uint32_t flags);
+dust_status dust_contract(const void* g, const void* X, dust_dtype dtype, int64_t T,
+                          int64_t d_in, int64_t d_out, float scale, uint32_t flags, float* gW,
+                          void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * dust_estimate_gW_workspace / dust_estimate_gW — the whole path, delta and X
  * to the weight gradient GW (the three equations above, in one call).
  *   X           device [T][d_in], DUST_BF16 (tensor-core path, fp32

@@ -100,7 +100,7 @@ def test_estimate_gW_small(w, force):
     got = _run(w, X, delta, so, flags).double().cpu().numpy()
     want = oracle.estimate_gW(X, delta, w.d_out, so, w.seed, w.kind, 0, np.float32(w.sigma),
                               np.float32(w.gamma), 1.0, oracle.CENTER)
-    tol = 1e-5 if (w.x_dtype == "f32" or path == dust.PATH_SIMT) else 1e-2
+    tol = 1e-5 if w.x_dtype == "f32" else 1e-2
     assert rel_fro(got, want) <= tol, (path, rel_fro(got, want))
 
 

@@ -53,6 +53,8 @@ def _signatures():
         "dust_credit_scan_workspace": (i32, [PSZ, i64, i64]),
         "dust_credit_scan": (i32, [P, i64, i64, P, i64, f32, u32, P, P, SZ, P]),
         "dust_error_estimate": (i32, [P, i64, i64, i64, u64, i32, i64, f32, u32, P, i32, P]),
+        "dust_contract_workspace": (i32, [PSZ, i64, i64, i64, i32, u32]),
+        "dust_contract": (i32, [P, P, i32, i64, i64, i64, f32, u32, P, P, SZ, P]),
         "dust_estimate_gW_workspace": (i32, [PSZ, i64, i64, i64, i64, i32, u32]),
         "dust_estimate_gW": (i32, [P, i32, i64, i64, P, i64, i64, P, i64, u64, i32, i64, f32,
                                    f32, f32, u32, P, P, SZ, P]),
@@ -183,6 +185,27 @@ def dust_error_estimate(r, d_out, seed, kind, draw_begin, sigma, flags=0, g=None
                                      flags, _ptr(g), _dtype_code(g), _stream(stream)),
            "dust_error_estimate")
     return g
+
+
+def dust_contract(g, X, scale=1.0, flags=0, gW=None, workspace=None, stream=None):
+    """g: [T, d_out], X: [T, d_in], same dtype (bf16 or f32); returns
+    gW f32 [d_out, d_in] = scale * g^T X."""
+    import torch
+    _need_cuda(g, X, gW)
+    T, d_out = g.shape
+    d_in = X.shape[1]
+    dt = _dtype_code(X)
+    if gW is None:
+        gW = torch.empty((d_out, d_in), dtype=torch.float32, device=X.device)
+    n = C.c_size_t(0)
+    _check(lib().dust_contract_workspace(C.byref(n), T, d_in, d_out, dt, flags),
+           "dust_contract_workspace")
+    if workspace is None:
+        workspace = _workspace(n.value, X.device)
+    _check(lib().dust_contract(_ptr(g), _ptr(X), dt, T, d_in, d_out, float(scale), flags,
+                               _ptr(gW), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "dust_contract")
+    return gW
 
 
 def dust_estimate_gW_workspace(T, d_in, d_out, K, x_dtype, flags=CENTER):

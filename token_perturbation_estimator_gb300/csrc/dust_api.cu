@@ -52,12 +52,14 @@ dust_status check_estimate(int64_t T, int64_t d_in, int64_t d_out, int64_t K, du
 int choose_path(int64_t T, int64_t d_in, int64_t d_out, int64_t K, dust_dtype x_dtype,
                 uint32_t flags) {
     (void)T;
-    (void)d_in;
-    (void)d_out;
     (void)K;
-    (void)x_dtype;
-    (void)flags;
-    return DUST_PATH_SIMT;
+    const bool forced_tc = (flags & (DUST_FORCE_UNFUSED | DUST_FORCE_FUSED)) != 0;
+    if (x_dtype != DUST_BF16) return forced_tc ? -DUST_ERR_UNSUPPORTED : DUST_PATH_SIMT;
+    if (flags & DUST_FORCE_SIMT) return DUST_PATH_SIMT;
+    const bool tc_shape = (d_in % 8 == 0) && (d_out % 8 == 0) && d_in > 0 && d_out > 0;
+    if (!tc_shape) return forced_tc ? -DUST_ERR_UNSUPPORTED : DUST_PATH_SIMT;
+    if (flags & DUST_FORCE_FUSED) return -DUST_ERR_UNSUPPORTED;
+    return DUST_PATH_UNFUSED_TC;
 }
 
 struct Layout {
@@ -66,14 +68,23 @@ struct Layout {
     int g_bf16 = 0;
 };
 
+// Workspace: scan buffers, then g [T][d_out] (bf16 when X is bf16, else
+// fp32), then the contraction's split-token partials. Sized for the chosen
+// path and for the CUDA-core fallback taken at run time when X is not
+// 16-byte aligned.
 Layout layout(int64_t T, int64_t d_in, int64_t d_out, int64_t K, dust_dtype x_dtype,
               uint32_t flags) {
     Layout L;
     L.path = choose_path(T, d_in, d_out, K, x_dtype, flags);
     L.scan = a256(scan_workspace_bytes(K, T));
-    L.g_bf16 = 0;
+    L.g_bf16 = (x_dtype == DUST_BF16) ? 1 : 0;
     L.g = a256(static_cast<size_t>(T) * static_cast<size_t>(d_out) * (L.g_bf16 ? 2 : 4));
-    L.gemm = a256(simt_gemm_workspace_bytes(T, d_in, d_out));
+    size_t gemm = simt_gemm_workspace_bytes(T, d_in, d_out);
+    if (L.path == DUST_PATH_UNFUSED_TC) {
+        const size_t tcb = tc_gemm_workspace_bytes(T, d_in, d_out);
+        if (tcb > gemm) gemm = tcb;
+    }
+    L.gemm = a256(gemm);
     L.total = L.scan + L.g + L.gemm;
     if (L.total == 0) L.total = 256;
     return L;
@@ -200,12 +211,51 @@ dust_status dust_error_estimate(const float* r, int64_t K, int64_t T, int64_t d_
                                      g_dtype == DUST_BF16, static_cast<cudaStream_t>(stream)));
 }
 
+dust_status dust_contract_workspace(size_t* bytes, int64_t T, int64_t d_in, int64_t d_out,
+                                    dust_dtype dtype, uint32_t flags) {
+    if (!bytes || T < 0 || d_in < 0 || d_out < 0) return DUST_ERR_INVALID_ARG;
+    if (dtype != DUST_F32 && dtype != DUST_BF16) return DUST_ERR_INVALID_ARG;
+    if (flags & ~(DUST_ACCUMULATE | DUST_FORCE_SIMT)) return DUST_ERR_INVALID_ARG;
+    size_t b = simt_gemm_workspace_bytes(T, d_in, d_out);
+    const size_t tcb = tc_gemm_workspace_bytes(T, d_in, d_out);
+    if (tcb > b) b = tcb;
+    *bytes = a256(b) + 256;
+    return DUST_OK;
+}
+
+dust_status dust_contract(const void* g, const void* X, dust_dtype dtype, int64_t T, int64_t d_in,
+                          int64_t d_out, float scale, uint32_t flags, float* gW, void* workspace,
+                          size_t ws_bytes, void* stream) {
+    size_t need = 0;
+    dust_status st = dust_contract_workspace(&need, T, d_in, d_out, dtype, flags);
+    if (st != DUST_OK) return st;
+    if (!finite(scale)) return DUST_ERR_INVALID_ARG;
+    if (d_in * d_out == 0) return DUST_OK;
+    if (!gW) return DUST_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool acc = (flags & DUST_ACCUMULATE) != 0;
+    if (T == 0) return acc ? DUST_OK : cuda_status(launch_zero(gW, d_out * d_in, s));
+    if (!g || !X) return DUST_ERR_INVALID_ARG;
+    if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
+        return DUST_ERR_WORKSPACE;
+    float* part = static_cast<float*>(workspace);
+    const bool bf16 = dtype == DUST_BF16;
+    cudaError_t e;
+    if (bf16 && !(flags & DUST_FORCE_SIMT) && tc_gemm_supported(g, X, d_in, d_out))
+        e = launch_tc_gemm(g, X, T, d_in, d_out, scale, acc, gW, part, s);
+    else
+        e = launch_simt_gemm(g, bf16, X, bf16, T, d_in, d_out, scale, acc, gW, part, s);
+    return cuda_status(e);
+}
+
 dust_status dust_estimate_gW_workspace(size_t* bytes, int64_t T, int64_t d_in, int64_t d_out,
                                        int64_t K, dust_dtype x_dtype, uint32_t flags) {
     if (!bytes) return DUST_ERR_INVALID_ARG;
     dust_status st = check_estimate(T, d_in, d_out, K, x_dtype, flags);
     if (st != DUST_OK) return st;
-    *bytes = layout(T, d_in, d_out, K, x_dtype, flags).total;
+    const Layout L = layout(T, d_in, d_out, K, x_dtype, flags);
+    if (L.path < 0) return static_cast<dust_status>(-L.path);
+    *bytes = L.total;
     return DUST_OK;
 }
 
@@ -242,6 +292,7 @@ dust_status dust_estimate_gW(const void* X, dust_dtype x_dtype, int64_t T, int64
     const size_t esz = (x_dtype == DUST_BF16) ? 2 : 4;
     if (reinterpret_cast<uintptr_t>(X) % esz) return DUST_ERR_INVALID_ARG;
     const Layout L = layout(T, d_in, d_out, K, x_dtype, flags);
+    if (L.path < 0) return static_cast<dust_status>(-L.path);
     if (!workspace || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255))
         return DUST_ERR_WORKSPACE;
 
@@ -258,8 +309,11 @@ dust_status dust_estimate_gW(const void* X, dust_dtype x_dtype, int64_t T, int64
     e = launch_weight(b, true, K, T, d_out, seed, static_cast<int>(kind), draw_begin, coef, anti,
                       g, L.g_bf16, s);
     if (e != cudaSuccess) return DUST_ERR_CUDA;
-    e = launch_simt_gemm(g, L.g_bf16, X, x_dtype == DUST_BF16, T, d_in, d_out, scale, acc, gW,
-                         part, s);
+    if (L.path == DUST_PATH_UNFUSED_TC && tc_gemm_supported(g, X, d_in, d_out))
+        e = launch_tc_gemm(g, X, T, d_in, d_out, scale, acc, gW, part, s);
+    else
+        e = launch_simt_gemm(g, L.g_bf16, X, x_dtype == DUST_BF16, T, d_in, d_out, scale, acc,
+                             gW, part, s);
     return cuda_status(e);
 }
 

@@ -89,6 +89,18 @@ cudaError_t launch_simt_gemm(const void* g, int g_bf16, const void* X, int x_bf1
                              int64_t d_in, int64_t d_out, float scale, bool accumulate,
                              float* gW, float* partials, cudaStream_t s);
 
+// gW[q] = scale * sum_{s<S} partials[s][q] (+ gW[q] when accumulating), in
+// slice order (deterministic).
+cudaError_t launch_reduce(const float* partials, int64_t S, int64_t n, float scale,
+                          bool accumulate, float* gW, cudaStream_t s);
+
+// Tensor-core contraction (tcgen05, bf16 g and X, fp32 accumulate).
+bool tc_gemm_supported(const void* g, const void* X, int64_t d_in, int64_t d_out);
+size_t tc_gemm_workspace_bytes(int64_t T, int64_t d_in, int64_t d_out);
+cudaError_t launch_tc_gemm(const void* g, const void* X, int64_t T, int64_t d_in, int64_t d_out,
+                           float scale, bool accumulate, float* gW, float* partials,
+                           cudaStream_t s);
+
 // Fill gW with zeros (T == 0) unless accumulating.
 cudaError_t launch_zero(float* p, int64_t n, cudaStream_t s);
 

@@ -129,16 +129,21 @@ cudaError_t run(const void* g, const void* X, int64_t T, int64_t d_in, int64_t d
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const int64_t n = d_out * d_in;
-    int64_t rg = (n + 255) / 256;
-    if (rg > 152 * 16) rg = 152 * 16;
-    ProfScope ps(kStageReduce, s);
-    k_reduce<<<static_cast<unsigned>(rg), 256, 0, s>>>(partials, S_used, n, scale,
-                                                       accumulate ? 1 : 0, gW);
-    return cudaGetLastError();
+    return launch_reduce(partials, S_used, d_out * d_in, scale, accumulate, gW, s);
 }
 
 }  // namespace
+
+cudaError_t launch_reduce(const float* partials, int64_t S, int64_t n, float scale,
+                          bool accumulate, float* gW, cudaStream_t s) {
+    if (n == 0) return cudaSuccess;
+    int64_t rg = (n + 255) / 256;
+    if (rg > 152 * 16) rg = 152 * 16;
+    ProfScope ps(kStageReduce, s);
+    k_reduce<<<static_cast<unsigned>(rg), 256, 0, s>>>(partials, S, n, scale, accumulate ? 1 : 0,
+                                                       gW);
+    return cudaGetLastError();
+}
 
 size_t simt_gemm_workspace_bytes(int64_t T, int64_t d_in, int64_t d_out) {
     const int64_t S = slices_for(T, d_in, d_out);
