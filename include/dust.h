@@ -161,6 +161,30 @@ dust_status dust_credit_scan(const float* delta, int64_t K, int64_t T,
                              void* stream);
 
 /*
+ * dust_credit_scan_noalloc — the same centring + credit scan as
+ * dust_credit_scan, for callers that cannot allocate device memory (for
+ * example a plugin whose host framework's pooling allocator owns all device
+ * memory, or a latency-critical loop where cudaMalloc/cudaFree may
+ * synchronise the device). The paper has no counterpart: this is a memory
+ * management variant of the library, not a step of the method.
+ * Its scratch is a fixed array of dust_credit_scan_noalloc_capacity() bytes
+ * (8 MiB) built into the library as a static device variable, held by every
+ * GPU that loads it until the process exits; it calls no cudaMalloc or
+ * cudaFree. The caller still passes delta, seq_offsets and r (same meaning,
+ * layout and results as dust_credit_scan). A call needing more scratch than
+ * the capacity (about 4 T + 8 K ceil(T/256) bytes) returns DUST_ERR_RANGE.
+ * The first call on a device looks up the array's device address with that
+ * device current; make it before any stream capture. All calls share the
+ * array: calls whose GPU work overlaps (several streams or host threads on
+ * one device) race. Each call writes every scratch word it reads, so no
+ * clearing between calls is needed.
+ */
+size_t dust_credit_scan_noalloc_capacity(void);
+dust_status dust_credit_scan_noalloc(const float* delta, int64_t K, int64_t T,
+                                     const int32_t* seq_offsets, int64_t n_seq, float gamma,
+                                     uint32_t flags, float* r, void* stream);
+
+/*
  * dust_error_estimate — reward-weighted noise on its own (the g_t equation):
  * g[t][c] = -(1/(K sigma)) sum_{i<K} r[t][i] a_t^(draw_begin+i)[c].
  *   r      device f32 [T][K] (the output of dust_credit_scan).

@@ -62,6 +62,8 @@ def _signatures():
         "dust_estimate_gW_host": (i32, [P, P, i32, i64, i64, P, P, i64, i64, P, P, i64, u64,
                                         i32, i64, f32, f32, f32, u32, P, P, P, SZ, P]),
         "dust_last_error": (i32, [P]),
+        "dust_credit_scan_noalloc_capacity": (SZ, []),
+        "dust_credit_scan_noalloc": (i32, [P, i64, i64, P, i64, f32, u32, P, P]),
         "dust_profile_enable": (i32, [i32]),
         "dust_profile_read": (i32, [P, i32]),
     }
@@ -170,6 +172,22 @@ def dust_credit_scan(delta, seq_offsets, gamma, flags=CENTER, r=None, workspace=
     _check(lib().dust_credit_scan(_ptr(delta), K, T, _ptr(seq_offsets), seq_offsets.numel() - 1,
                                   float(gamma), flags, _ptr(r), _ptr(workspace),
                                   workspace.numel(), _stream(stream)), "dust_credit_scan")
+    return r
+
+
+def dust_credit_scan_noalloc(delta, seq_offsets, gamma, flags=CENTER, r=None, stream=None):
+    """As dust_credit_scan, with the library's built-in scratch array instead
+    of a caller workspace (for callers that cannot allocate device memory).
+    r must be passed in by such callers; it is allocated here only for
+    convenience when omitted."""
+    import torch
+    _need_cuda(delta, seq_offsets, r)
+    K, T = delta.shape
+    if r is None:
+        r = torch.empty((T, K), dtype=torch.float32, device=delta.device)
+    _check(lib().dust_credit_scan_noalloc(_ptr(delta), K, T, _ptr(seq_offsets),
+                                          seq_offsets.numel() - 1, float(gamma), flags, _ptr(r),
+                                          _stream(stream)), "dust_credit_scan_noalloc")
     return r
 
 
