@@ -91,15 +91,17 @@ enum {
     DUST_ACCUMULATE = 4u,      /* GW += result instead of GW = result */
     DUST_FORCE_UNFUSED = 8u,   /* estimator: write g to the workspace, then contract */
     DUST_FORCE_FUSED = 16u,    /* estimator: produce g tiles inside the contraction
-                                  (DUST_ERR_UNSUPPORTED where that kernel cannot run) */
+                                  (needs bf16 X, d_in <= 512, d_in % 8 == 0,
+                                  d_out % 8 == 0, K <= 64; else DUST_ERR_UNSUPPORTED) */
     DUST_WORD_STREAM1 = 32u,   /* dust_noise RAW_WORDS: words of stream s = 1 */
     DUST_FORCE_SIMT = 64u      /* estimator: contraction on CUDA cores (fp32 FFMA) */
 };
 
 /* Contraction paths reported by dust_estimate_gW_path. */
 typedef enum {
-    DUST_PATH_FUSED_TC = 1,    /* fused g-producer + tcgen05 MMA, bf16 in, fp32 accumulate */
-    DUST_PATH_UNFUSED_TC = 2,  /* weighting kernel -> g (bf16) -> tcgen05 GEMM */
+    DUST_PATH_FUSED_TC = 1,    /* fused g-producer + tcgen05 MMA, bf16 in, fp32 accumulate
+                                  (g never written to HBM); opt-in via DUST_FORCE_FUSED */
+    DUST_PATH_UNFUSED_TC = 2,  /* weighting kernel -> g (bf16) -> tcgen05 GEMM; default for bf16 */
     DUST_PATH_SIMT = 3         /* weighting kernel -> g (fp32 or bf16) -> FFMA GEMM */
 } dust_path;
 
@@ -204,7 +206,7 @@ dust_status dust_error_estimate(const float* r, int64_t K, int64_t T, int64_t d_
  *           16-byte aligned bases, otherwise CUDA cores) or both DUST_F32
  *           (CUDA cores, fp32).
  *   flags   DUST_ACCUMULATE, DUST_FORCE_SIMT.
- *   gW      device f32 [d_out][d_in].
+ *   gW      device f32 [d_out][d_in], 16-byte aligned.
  *   workspace as for dust_estimate_gW (split-token partials).
  */
 dust_status dust_contract_workspace(size_t* bytes, int64_t T, int64_t d_in, int64_t d_out,
@@ -227,8 +229,8 @@ dust_status dust_contract(const void* g, const void* X, dust_dtype dtype, int64_
  *   sigma       finite, non-zero; gamma finite, |gamma| <= 1; scale finite.
  *   flags       DUST_CENTER, DUST_ANTITHETIC, DUST_ACCUMULATE and at most one
  *               of DUST_FORCE_UNFUSED / DUST_FORCE_FUSED / DUST_FORCE_SIMT.
- *   gW          device f32 [d_out][d_in], W's layout; overwritten, or
- *               accumulated into with DUST_ACCUMULATE.
+ *   gW          device f32 [d_out][d_in], W's layout, 16-byte aligned;
+ *               overwritten, or accumulated into with DUST_ACCUMULATE.
  *   workspace   device, >= dust_estimate_gW_workspace(...) bytes, 256-byte
  *               aligned; contents on entry are ignored.
  * The result is a deterministic function of the inputs (no floating-point

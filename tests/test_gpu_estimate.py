@@ -230,3 +230,55 @@ def test_estimate_gW_full_size_sampled(w):
                              1.0, oracle.CENTER)
     tol = 1e-5 if w.x_dtype == "f32" else 1e-2
     assert rel_fro(got[chan, col], want) <= tol
+
+
+# ------------------------------------------------- fused vs unfused paths --
+
+FUSED_SHAPES = [
+    # T, d_in, d_out, K, kind, gamma
+    (1000, 264, 136, 8, 1, 0.9),    # two MMA halves (256 + 64), channel tail, ragged T
+    (4096, 512, 2048, 8, 1, 0.0),   # the measured up-projection shape, shorter T
+    (777, 40, 256, 5, 0, 0.5),      # one narrow MMA, Rademacher, odd K
+    (2048, 512, 512, 32, 1, 0.9),
+    (300, 128, 8, 3, 0, 0.0),       # a single 8-channel tile
+    (1500, 96, 384, 64, 1, 0.98),   # the largest K of the fused kernel, unaligned carry rows
+]
+
+
+@pytest.mark.parametrize("T,d_in,d_out,K,kind,gamma", FUSED_SHAPES)
+def test_fused_matches_unfused(T, d_in, d_out, K, kind, gamma):
+    """The fused kernel makes the same bf16 g tiles as the weighting kernel
+    (same draw order, same rounding) and contracts them in another order, so
+    the two paths agree to fp32 summation error."""
+    import torch
+    dev = cuda()
+    rng = np.random.default_rng(T + d_in + d_out + K)
+    so = torch.from_numpy(offsets_from_lengths(random_lengths(rng, T, 300))).to(dev)
+    X = torch.from_numpy(rng.standard_normal((T, d_in)).astype(np.float32)).to(torch.bfloat16).to(dev)
+    delta = torch.from_numpy((0.05 * rng.standard_normal((K, T))).astype(np.float32)).to(dev)
+    args = (d_out, so, 11, kind, 4, 1e-3, gamma, 0.5)
+    assert dust.dust_estimate_gW_path(T, d_in, d_out, K, dust.BF16,
+                                      dust.CENTER | dust.FORCE_FUSED) == dust.PATH_FUSED_TC
+    a = dust.dust_estimate_gW(X, delta, *args, dust.CENTER | dust.FORCE_FUSED)
+    b = dust.dust_estimate_gW(X, delta, *args, dust.CENTER | dust.FORCE_UNFUSED)
+    torch.cuda.synchronize()
+    assert dust.dust_last_error() == dust.OK
+    assert rel_fro(a.cpu().numpy(), b.cpu().numpy()) <= 1e-5
+    a2 = dust.dust_estimate_gW(X, delta, *args, dust.CENTER | dust.FORCE_FUSED)
+    assert torch.equal(a, a2)
+    base = torch.randn_like(a)
+    acc = base.clone()
+    dust.dust_estimate_gW(X, delta, *args, dust.CENTER | dust.FORCE_FUSED | dust.ACCUMULATE,
+                          gW=acc)
+    assert torch.allclose(acc, base + a, rtol=1e-6, atol=1e-6 * a.abs().max().item())
+
+
+def test_fused_limits():
+    assert dust.dust_estimate_gW_path(1024, 520, 256, 8, dust.BF16, dust.CENTER) == \
+        dust.PATH_UNFUSED_TC
+    with pytest.raises(dust.DustError):
+        dust.dust_estimate_gW_path(1024, 512, 256, 65, dust.BF16, dust.CENTER | dust.FORCE_FUSED)
+    with pytest.raises(dust.DustError):
+        dust.dust_estimate_gW_path(1024, 520, 256, 8, dust.BF16, dust.CENTER | dust.FORCE_FUSED)
+    with pytest.raises(dust.DustError):
+        dust.dust_estimate_gW_path(1024, 64, 64, 8, dust.F32, dust.CENTER | dust.FORCE_FUSED)

@@ -4,7 +4,7 @@
 #include <cmath>
 #include <cstring>
 
-#include "../../include/dust.h"
+#include "dust.h"
 #include "internal.cuh"
 
 using namespace dust;
@@ -58,7 +58,12 @@ int choose_path(int64_t T, int64_t d_in, int64_t d_out, int64_t K, dust_dtype x_
     if (flags & DUST_FORCE_SIMT) return DUST_PATH_SIMT;
     const bool tc_shape = (d_in % 8 == 0) && (d_out % 8 == 0) && d_in > 0 && d_out > 0;
     if (!tc_shape) return forced_tc ? -DUST_ERR_UNSUPPORTED : DUST_PATH_SIMT;
-    if (flags & DUST_FORCE_FUSED) return -DUST_ERR_UNSUPPORTED;
+    // The fused kernel is opt-in: on GB300 it is limited to one 1024-thread
+    // CTA per SM (its TMEM accumulator spans the SM), too few warps to hide
+    // the producers' latencies, and measures slower than the weighting
+    // kernel followed by the tensor-core GEMM.
+    if (flags & DUST_FORCE_FUSED)
+        return fused_supported(d_in, d_out, K) ? DUST_PATH_FUSED_TC : -DUST_ERR_UNSUPPORTED;
     return DUST_PATH_UNFUSED_TC;
 }
 
@@ -70,14 +75,19 @@ struct Layout {
 
 // Workspace: scan buffers, then g [T][d_out] (bf16 when X is bf16, else
 // fp32), then the contraction's split-token partials. Sized for the chosen
-// path and for the CUDA-core fallback taken at run time when X is not
-// 16-byte aligned.
+// path (the fused path needs no g buffer).
 Layout layout(int64_t T, int64_t d_in, int64_t d_out, int64_t K, dust_dtype x_dtype,
               uint32_t flags) {
     Layout L;
     L.path = choose_path(T, d_in, d_out, K, x_dtype, flags);
     L.scan = a256(scan_workspace_bytes(K, T));
     L.g_bf16 = (x_dtype == DUST_BF16) ? 1 : 0;
+    if (L.path == DUST_PATH_FUSED_TC) {
+        L.g = 0;
+        L.gemm = a256(fused_workspace_bytes(T, d_in, d_out));
+        L.total = L.scan + L.gemm;
+        return L;
+    }
     L.g = a256(static_cast<size_t>(T) * static_cast<size_t>(d_out) * (L.g_bf16 ? 2 : 4));
     size_t gemm = simt_gemm_workspace_bytes(T, d_in, d_out);
     if (L.path == DUST_PATH_UNFUSED_TC) {
@@ -231,7 +241,7 @@ dust_status dust_contract(const void* g, const void* X, dust_dtype dtype, int64_
     if (st != DUST_OK) return st;
     if (!finite(scale)) return DUST_ERR_INVALID_ARG;
     if (d_in * d_out == 0) return DUST_OK;
-    if (!gW) return DUST_ERR_INVALID_ARG;
+    if (!gW || (reinterpret_cast<uintptr_t>(gW) % 16)) return DUST_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool acc = (flags & DUST_ACCUMULATE) != 0;
     if (T == 0) return acc ? DUST_OK : cuda_status(launch_zero(gW, d_out * d_in, s));
@@ -284,13 +294,12 @@ dust_status dust_estimate_gW(const void* X, dust_dtype x_dtype, int64_t T, int64
     if (T > 0 && (n_seq < 1 || n_seq > T)) return DUST_ERR_INVALID_ARG;
     if (n_seq < 0) return DUST_ERR_INVALID_ARG;
     if (d_out * d_in == 0) return DUST_OK;
-    if (!gW) return DUST_ERR_INVALID_ARG;
+    if (!gW || (reinterpret_cast<uintptr_t>(gW) % 16)) return DUST_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool acc = (flags & DUST_ACCUMULATE) != 0;
     if (T == 0) return acc ? DUST_OK : cuda_status(launch_zero(gW, d_out * d_in, s));
     if (!X || !delta || !seq_offsets) return DUST_ERR_INVALID_ARG;
-    const size_t esz = (x_dtype == DUST_BF16) ? 2 : 4;
-    if (reinterpret_cast<uintptr_t>(X) % esz) return DUST_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(X) % 16) return DUST_ERR_INVALID_ARG;
     const Layout L = layout(T, d_in, d_out, K, x_dtype, flags);
     if (L.path < 0) return static_cast<dust_status>(-L.path);
     if (!workspace || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255))
@@ -306,6 +315,11 @@ dust_status dust_estimate_gW(const void* X, dust_dtype x_dtype, int64_t T, int64
     cudaError_t e = launch_scan(delta, K, T, seq_offsets, n_seq, gamma,
                                 (flags & DUST_CENTER) != 0, b, s);
     if (e != cudaSuccess) return DUST_ERR_CUDA;
+    if (L.path == DUST_PATH_FUSED_TC) {
+        float* fpart = reinterpret_cast<float*>(ws + L.scan);
+        return cuda_status(launch_fused(b, X, K, T, d_in, d_out, seed, static_cast<int>(kind),
+                                        draw_begin, coef, anti, scale, acc, gW, fpart, s));
+    }
     e = launch_weight(b, true, K, T, d_out, seed, static_cast<int>(kind), draw_begin, coef, anti,
                       g, L.g_bf16, s);
     if (e != cudaSuccess) return DUST_ERR_CUDA;

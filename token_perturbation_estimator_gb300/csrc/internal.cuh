@@ -101,6 +101,15 @@ cudaError_t launch_tc_gemm(const void* g, const void* X, int64_t T, int64_t d_in
                            float scale, bool accumulate, float* gW, float* partials,
                            cudaStream_t s);
 
+// Fused weighting + tensor-core contraction (d_in <= 512): g tiles are made
+// in shared memory and never written to HBM.
+bool fused_supported(int64_t d_in, int64_t d_out, int64_t K);
+size_t fused_workspace_bytes(int64_t T, int64_t d_in, int64_t d_out);
+cudaError_t launch_fused(const ScanBuffers& b, const void* X, int64_t K, int64_t T, int64_t d_in,
+                         int64_t d_out, uint64_t seed, int kind, int64_t draw_begin, float coef,
+                         bool anti, float scale, bool accumulate, float* gW, float* partials,
+                         cudaStream_t s);
+
 // Fill gW with zeros (T == 0) unless accumulating.
 cudaError_t launch_zero(float* p, int64_t n, cudaStream_t s);
 

@@ -87,9 +87,32 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const TG* __restrict__ g,
 
 __global__ void __launch_bounds__(256) k_reduce(const float* __restrict__ part, int64_t S,
                                                 int64_t n, float scale, int accumulate,
-                                                float* __restrict__ gW) {
-    for (int64_t q = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; q < n;
-         q += (int64_t)gridDim.x * blockDim.x) {
+                                                float* __restrict__ gW, int vec4) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t tid = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    if (vec4) {
+        const int64_t n4 = n >> 2;
+        const float4* p4 = reinterpret_cast<const float4*>(part);
+        float4* g4 = reinterpret_cast<float4*>(gW);
+        for (int64_t q = tid; q < n4; q += stride) {
+            float4 v = p4[q];
+            for (int64_t s = 1; s < S; ++s) {
+                const float4 w = p4[s * n4 + q];
+                v.x += w.x;
+                v.y += w.y;
+                v.z += w.z;
+                v.w += w.w;
+            }
+            float4 o = make_float4(scale * v.x, scale * v.y, scale * v.z, scale * v.w);
+            if (accumulate) {
+                const float4 a = g4[q];
+                o = make_float4(a.x + o.x, a.y + o.y, a.z + o.z, a.w + o.w);
+            }
+            g4[q] = o;
+        }
+        return;
+    }
+    for (int64_t q = tid; q < n; q += stride) {
         float v = 0.0f;
         for (int64_t s = 0; s < S; ++s) v += part[s * n + q];
         gW[q] = accumulate ? gW[q] + scale * v : scale * v;
@@ -140,8 +163,10 @@ cudaError_t launch_reduce(const float* partials, int64_t S, int64_t n, float sca
     int64_t rg = (n + 255) / 256;
     if (rg > 152 * 16) rg = 152 * 16;
     ProfScope ps(kStageReduce, s);
+    const int vec4 = ((n & 3) == 0) && (reinterpret_cast<uintptr_t>(gW) % 16 == 0) &&
+                     (reinterpret_cast<uintptr_t>(partials) % 16 == 0);
     k_reduce<<<static_cast<unsigned>(rg), 256, 0, s>>>(partials, S, n, scale, accumulate ? 1 : 0,
-                                                       gW);
+                                                       gW, vec4);
     return cudaGetLastError();
 }
 

@@ -213,14 +213,16 @@ int64_t tc_slices(int64_t T, int64_t d_in, int64_t d_out) {
 
 }  // namespace
 
-// A bf16 [rows][cols] row-major matrix as a 2-D tensor map with 64 x 64 boxes
-// and the 128-byte swizzle; false if the driver refuses it.
-bool make_tmap_bf16_64x64(CUtensorMap* map, const void* base, int64_t rows, int64_t cols) {
+// A bf16 [rows][cols] row-major matrix as a 2-D tensor map with boxes of 64
+// columns x box_rows rows and the 128-byte swizzle; false if the driver
+// refuses it.
+bool make_tmap_bf16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
+                    uint32_t box_rows) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-    cuuint32_t box[2] = {64, 64};
+    cuuint32_t box[2] = {64, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -243,7 +245,7 @@ cudaError_t launch_tc_gemm(const void* g, const void* X, int64_t T, int64_t d_in
                            float scale, bool accumulate, float* gW, float* partials,
                            cudaStream_t s) {
     CUtensorMap ta, tb;
-    if (!make_tmap_bf16_64x64(&ta, g, T, d_out) || !make_tmap_bf16_64x64(&tb, X, T, d_in))
+    if (!make_tmap_bf16(&ta, g, T, d_out, kBK) || !make_tmap_bf16(&tb, X, T, d_in, kBK))
         return cudaErrorInvalidValue;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;

@@ -16,7 +16,9 @@ namespace dust {
 
 namespace {
 
-constexpr int kDrawGroup = 32;  // draws staged in shared memory at once
+constexpr int kDrawGroup = 32;       // draws staged in shared memory at once
+constexpr int64_t kCoopOffsets = 4096;  // up to this many sequences, scan all offsets
+constexpr size_t kCarrySmem = 96 * 1024;  // chunk summaries staged by k_carry
 
 // m[t] for the 256 tokens of a chunk: 0 where t is the last token of its
 // sequence (t + 1 is an offset in seq_offsets[1..n_seq]) or t >= T.
@@ -49,7 +51,21 @@ __global__ void __launch_bounds__(256) k_scan_local(const float* __restrict__ de
     const int64_t t0 = chunk * kScanChunk;
     const int64_t t = t0 + tid;
 
-    s_m[tid] = decay_of(t, T, so, n_seq, gamma);
+    if (n_seq <= kCoopOffsets) {
+        // Mark the chunk's sequence ends from all offsets at once (independent
+        // loads) rather than by a chain of dependent binary-search loads.
+        __shared__ unsigned char s_end[kScanChunk];
+        s_end[tid] = 0;
+        __syncthreads();
+        for (int64_t q = 1 + tid; q <= n_seq; q += blockDim.x) {
+            const int64_t e = static_cast<int64_t>(so[q]) - 1 - t0;
+            if (e >= 0 && e < kScanChunk) s_end[e] = 1;
+        }
+        __syncthreads();
+        s_m[tid] = (t >= T - 1 || s_end[tid]) ? 0.0f : gamma;
+    } else {
+        s_m[tid] = decay_of(t, T, so, n_seq, gamma);
+    }
     float mean = 0.0f;
     if (center && K > 1 && t < T) {
         for (int64_t i = 0; i < K; ++i) mean += delta[i * T + t];
@@ -134,31 +150,31 @@ __global__ void __launch_bounds__(256) k_scan_local(const float* __restrict__ de
 }
 
 // carry[j][i] = A[j+1][i] + B[j+1] * carry[j+1][i], carry[last] = 0.
+// The summaries are first staged in shared memory by all threads (when they
+// fit), so the serial chain of each draw runs at shared-memory latency.
 __global__ void __launch_bounds__(256) k_carry(const float* __restrict__ A,
                                                const float* __restrict__ B, int64_t K,
-                                               int64_t n_chunks, float* __restrict__ carry) {
-    const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-    if (i >= K) return;
-    float c = 0.0f;
-    int64_t j = n_chunks - 1;
-    carry[j * K + i] = 0.0f;
-    // Unrolled by 4 so the loads of the next summaries overlap the chain.
-    for (; j >= 4; j -= 4) {
-        const float a0 = A[j * K + i], a1 = A[(j - 1) * K + i];
-        const float a2 = A[(j - 2) * K + i], a3 = A[(j - 3) * K + i];
-        const float b0 = B[j], b1 = B[j - 1], b2 = B[j - 2], b3 = B[j - 3];
-        c = fmaf(b0, c, a0);
-        carry[(j - 1) * K + i] = c;
-        c = fmaf(b1, c, a1);
-        carry[(j - 2) * K + i] = c;
-        c = fmaf(b2, c, a2);
-        carry[(j - 3) * K + i] = c;
-        c = fmaf(b3, c, a3);
-        carry[(j - 4) * K + i] = c;
+                                               int64_t n_chunks, float* __restrict__ carry,
+                                               int staged) {
+    extern __shared__ float s_sum[];  // [n_chunks][K] A, then [n_chunks] B
+    const float* sA = A;
+    const float* sB = B;
+    if (staged) {
+        float* dA = s_sum;
+        float* dB = s_sum + n_chunks * K;
+        for (int64_t e = threadIdx.x; e < n_chunks * K; e += blockDim.x) dA[e] = A[e];
+        for (int64_t e = threadIdx.x; e < n_chunks; e += blockDim.x) dB[e] = B[e];
+        __syncthreads();
+        sA = dA;
+        sB = dB;
     }
-    for (; j >= 1; --j) {
-        c = fmaf(B[j], c, A[j * K + i]);
-        carry[(j - 1) * K + i] = c;
+    for (int64_t i = threadIdx.x; i < K; i += blockDim.x) {
+        float c = 0.0f;
+        carry[(n_chunks - 1) * K + i] = 0.0f;
+        for (int64_t j = n_chunks - 1; j >= 1; --j) {
+            c = fmaf(sB[j], c, sA[j * K + i]);
+            carry[(j - 1) * K + i] = c;
+        }
     }
 }
 
@@ -177,10 +193,12 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 }  // namespace
 
+// Every buffer keeps at least 16 bytes of slack after it, so that a copy
+// rounded up to 16 bytes never leaves the workspace.
 size_t scan_workspace_bytes(int64_t K, int64_t T) {
     const int64_t nc = (T + kScanChunk - 1) / kScanChunk;
-    return align256(sizeof(float) * K * T) + align256(sizeof(float) * T) +
-           2 * align256(sizeof(float) * nc * K) + align256(sizeof(float) * nc);
+    return align256(sizeof(float) * K * T + 16) + align256(sizeof(float) * T + 16) +
+           2 * align256(sizeof(float) * nc * K + 16) + align256(sizeof(float) * nc + 16);
 }
 
 ScanBuffers scan_carve(void* ws, int64_t K, int64_t T) {
@@ -188,13 +206,13 @@ ScanBuffers scan_carve(void* ws, int64_t K, int64_t T) {
     b.n_chunks = (T + kScanChunk - 1) / kScanChunk;
     char* p = static_cast<char*>(ws);
     b.r = reinterpret_cast<float*>(p);
-    p += align256(sizeof(float) * K * T);
+    p += align256(sizeof(float) * K * T + 16);
     b.P = reinterpret_cast<float*>(p);
-    p += align256(sizeof(float) * T);
+    p += align256(sizeof(float) * T + 16);
     b.A = reinterpret_cast<float*>(p);
-    p += align256(sizeof(float) * b.n_chunks * K);
+    p += align256(sizeof(float) * b.n_chunks * K + 16);
     b.carry = reinterpret_cast<float*>(p);
-    p += align256(sizeof(float) * b.n_chunks * K);
+    p += align256(sizeof(float) * b.n_chunks * K + 16);
     b.B = reinterpret_cast<float*>(p);
     return b;
 }
@@ -210,9 +228,13 @@ cudaError_t launch_scan(const float* delta, int64_t K, int64_t T, const int32_t*
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    const size_t smem = sizeof(float) * static_cast<size_t>(b.n_chunks * (K + 1));
+    const int staged = smem <= kCarrySmem ? 1 : 0;
+    static cudaError_t attr = cudaFuncSetAttribute(
+        k_carry, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kCarrySmem));
+    if (attr != cudaSuccess) return attr;
     ProfScope ps(kStageScanCarry, s);
-    k_carry<<<static_cast<unsigned>((K + 255) / 256), 256, 0, s>>>(b.A, b.B, K, b.n_chunks,
-                                                                   b.carry);
+    k_carry<<<1, 256, staged ? smem : 0, s>>>(b.A, b.B, K, b.n_chunks, b.carry, staged);
     return cudaGetLastError();
 }
 

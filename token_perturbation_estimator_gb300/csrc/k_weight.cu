@@ -5,8 +5,8 @@
 // from the hash for every (draw, token, channel) and used once; nothing of it
 // is stored.
 //
-// Mapping: one warp per token, 8 channels per lane (4 Box-Muller pairs or 8
-// signs), 8 tokens x 256 channels per CTA. The per-draw keys and the
+// Mapping: one warp per token, kCpt channels per lane (kCpt/2 Box-Muller pairs
+// or kCpt signs), 8 tokens x 32 kCpt channels per CTA. The per-draw keys and the
 // per-token rewards (already multiplied by -1/(K sigma) and, for antithetic
 // draws, by the pair sign) are staged in shared memory 64 draws at a time and
 // read as warp-wide broadcasts. The per-channel counters are pre-folded once
@@ -19,17 +19,22 @@ namespace dust {
 
 namespace {
 
-constexpr int kTok = 8;     // tokens per CTA (one per warp)
-constexpr int kCh = 256;    // channels per CTA (8 per lane)
-constexpr int kGroup = 64;  // draws staged per pass
+#ifndef DUST_WEIGHT_CPT
+#define DUST_WEIGHT_CPT 16
+#endif
+constexpr int kTok = 8;                 // tokens per CTA (one per warp)
+constexpr int kCpt = DUST_WEIGHT_CPT;   // channels per lane (8 or 16)
+constexpr int kCh = 32 * kCpt;          // channels per CTA
+constexpr int kGroup = 64;              // draws staged per pass
+static_assert(kCpt % 8 == 0, "channels per lane must be a multiple of 8");
 
 template <typename OutT>
 __device__ __forceinline__ void store8(OutT* g, int64_t row, int64_t d_out, int64_t c0,
-                                       const float (&acc)[8], bool vec);
+                                       const float* acc, bool vec);
 
 template <>
 __device__ __forceinline__ void store8<float>(float* g, int64_t row, int64_t d_out, int64_t c0,
-                                              const float (&acc)[8], bool vec) {
+                                              const float* acc, bool vec) {
     float* p = g + row * d_out + c0;
     if (vec) {
         reinterpret_cast<float4*>(p)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
@@ -44,7 +49,7 @@ __device__ __forceinline__ void store8<float>(float* g, int64_t row, int64_t d_o
 template <>
 __device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16* g, int64_t row,
                                                       int64_t d_out, int64_t c0,
-                                                      const float (&acc)[8], bool vec) {
+                                                      const float* acc, bool vec) {
     __nv_bfloat16* p = g + row * d_out + c0;
     if (vec) {
         __nv_bfloat162 h[4];
@@ -64,34 +69,34 @@ __global__ void __launch_bounds__(256) k_weight(const float* __restrict__ r,
                                                 const float* __restrict__ carry, int64_t K,
                                                 int64_t T, int64_t d_out, uint32_t skey,
                                                 int64_t draw_begin, float coef, bool anti,
-                                                OutT* __restrict__ g) {
-    __shared__ uint32_t s_k0[kGroup];
-    __shared__ uint32_t s_k1[kGroup];
+                                                OutT* __restrict__ g, bool vec_ok) {
+    __shared__ uint2 s_key[kGroup];  // folded keys of streams 0 and 1
     __shared__ float s_r[kTok][kGroup];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t tb = static_cast<int64_t>(blockIdx.x) * kTok;
     const int64_t t = tb + warp;
-    const int64_t c0 = static_cast<int64_t>(blockIdx.y) * kCh + lane * 8;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.y) * kCh + lane * kCpt;
     const bool active = (t < T) && (c0 < d_out);
 
     // Pre-folded counters: pairs for the Gaussian, single channels for signs.
-    uint32_t nf[8];
+    constexpr int kNf = (KIND == 1) ? kCpt / 2 : kCpt;
+    uint32_t nf[kNf];
     const uint32_t base = static_cast<uint32_t>(t * d_out + c0);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) nf[j] = fold16(base + (KIND == 1 ? 2u * (j & 3) : j));
+    for (int j = 0; j < kNf; ++j) nf[j] = fold16(base + (KIND == 1 ? 2u * j : j));
 
-    float acc[8];
+    float acc[kCpt];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+    for (int j = 0; j < kCpt; ++j) acc[j] = 0.0f;
 
     for (int64_t g0 = 0; g0 < K; g0 += kGroup) {
         const int gn = static_cast<int>(K - g0 < kGroup ? K - g0 : kGroup);
         if (tid < gn) {
             const int64_t i = draw_begin + g0 + tid;
             const int64_t bi = base_draw(i, anti);
-            s_k0[tid] = fold16(draw_key(skey, bi, 0));
-            if (KIND == 1) s_k1[tid] = fold16(draw_key(skey, bi, 1));
+            s_key[tid] = make_uint2(fold16(draw_key(skey, bi, 0)),
+                                    KIND == 1 ? fold16(draw_key(skey, bi, 1)) : 0u);
         }
         for (int e = tid; e < kTok * gn; e += blockDim.x) {
             const int tok = e / gn, k = e - tok * gn;
@@ -111,14 +116,14 @@ __global__ void __launch_bounds__(256) k_weight(const float* __restrict__ r,
 #pragma unroll 2
                 for (int k = 0; k < gn; ++k) {
                     const float rr = s_r[warp][k];
-                    const uint32_t k0 = s_k0[k], k1 = s_k1[k];
+                    const uint2 key = s_key[k];
 #pragma unroll
-                    for (int p = 0; p < 4; ++p) {
-                        const float f0 = unit_ff(k0, nf[p]);
-                        const float f1 = unit_ff(k1, nf[p]);
+                    for (int p = 0; p < kCpt / 2; ++p) {
+                        const float f0 = unit_ff(key.x, nf[p]);
+                        const float f1 = unit_ff(key.y, nf[p]);
                         const float tr = rr * neg_radius(f0);
                         float sn, cs;
-                        __sincosf(6.28318530717958648f * (f1 - 1.5f), &sn, &cs);
+                        __sincosf(centred_angle(f1), &sn, &cs);
                         acc[2 * p] = fmaf(tr, cs, acc[2 * p]);
                         acc[2 * p + 1] = fmaf(tr, sn, acc[2 * p + 1]);
                     }
@@ -127,9 +132,9 @@ __global__ void __launch_bounds__(256) k_weight(const float* __restrict__ r,
 #pragma unroll 2
                 for (int k = 0; k < gn; ++k) {
                     const uint32_t rb = __float_as_uint(s_r[warp][k]);
-                    const uint32_t k0 = s_k0[k];
+                    const uint32_t k0 = s_key[k].x;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
+                    for (int j = 0; j < kCpt; ++j)
                         acc[j] += __uint_as_float(rb ^ sign_ff(k0, nf[j]));
                 }
             }
@@ -137,8 +142,12 @@ __global__ void __launch_bounds__(256) k_weight(const float* __restrict__ r,
         __syncthreads();
     }
     if (active) {
-        const bool vec = ((d_out & 7) == 0) && (c0 + 8 <= d_out);
-        store8<OutT>(g, t, d_out, c0, acc, vec);
+        const bool vec = vec_ok;  // 16-byte aligned rows (host-checked)
+#pragma unroll
+        for (int q = 0; q < kCpt / 8; ++q) {
+            const int64_t cq = c0 + 8 * q;
+            if (cq < d_out) store8<OutT>(g, t, d_out, cq, acc + 8 * q, vec && cq + 8 <= d_out);
+        }
     }
 }
 
@@ -148,15 +157,16 @@ cudaError_t launch_kind(const ScanBuffers& b, int64_t K, int64_t T, int64_t d_ou
                         cudaStream_t s) {
     dim3 grid(static_cast<unsigned>((T + kTok - 1) / kTok),
               static_cast<unsigned>((d_out + kCh - 1) / kCh));
+    const bool vec_ok = (d_out % 8 == 0) && (reinterpret_cast<uintptr_t>(g) % 16 == 0);
     ProfScope ps(kStageWeight, s);
     if (g_bf16)
         k_weight<KIND, FIX, __nv_bfloat16><<<grid, 256, 0, s>>>(
             b.r, b.P, b.carry, K, T, d_out, skey, draw_begin, coef, anti,
-            static_cast<__nv_bfloat16*>(g));
+            static_cast<__nv_bfloat16*>(g), vec_ok);
     else
         k_weight<KIND, FIX, float><<<grid, 256, 0, s>>>(b.r, b.P, b.carry, K, T, d_out, skey,
                                                         draw_begin, coef, anti,
-                                                        static_cast<float*>(g));
+                                                        static_cast<float*>(g), vec_ok);
     return cudaGetLastError();
 }
 

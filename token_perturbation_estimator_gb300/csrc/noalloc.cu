@@ -20,7 +20,7 @@
 #include <cmath>
 #include <mutex>
 
-#include "../../include/dust.h"
+#include "dust.h"
 #include "internal.cuh"
 
 namespace dust {

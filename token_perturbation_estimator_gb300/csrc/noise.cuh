@@ -80,28 +80,34 @@ __device__ __forceinline__ float sqrt_approx(float x) {
 
 // Box-Muller radius with its sign folded in: returns -rho, rho =
 // sqrt(-2 ln u1), from f0 = 1 + v, v = (w0 >> 9) 2^-23, u1 = 1 - v (exact).
-// -2 ln(1 - v) is taken from the hardware log2 where u1 <= 1 - 2^-7 and from
-// the Mercator series 2v + v^2 + (2/3)v^3 + (1/2)v^4 below that, where the
-// hardware log's absolute error would dominate the small result (the series
-// truncation there is below v^4/5 relative).
+// -2 ln(1 - v) is taken from the hardware log2 where u1 <= 1 - 2^-11 and from
+// the first two terms of the Mercator series below that, 2v + v^2 =
+// f0^2 - 1 (one fused multiply-add, a single rounding): there the hardware
+// log2's absolute error (about 2^-22) would dominate the small result, while
+// the series' truncation is below v^2/3 <= 2^-22/3 relative. Above the
+// threshold rho >= 1/32, so a 2^-22 log2 error moves rho by at most
+// 2 ln2 2^-22 / (2/32) ~ 5.3e-6.
 __device__ __forceinline__ float neg_radius(float f0) {
-    const float v = f0 - 1.0f;
     const float u1 = 2.0f - f0;
     const float q_log = -1.38629436111989061f * lg2_approx(u1);  // -2 ln 2 * log2(u1)
-    const float q_ser = v * fmaf(v, fmaf(v, fmaf(v, 0.5f, 0.666666667f), 1.0f), 2.0f);
-    const float q = (v < 0.0078125f) ? q_ser : q_log;
+    const float q_ser = fmaf(f0, f0, -1.0f);
+    const float q = (f0 < 1.00048828125f) ? q_ser : q_log;  // v < 2^-11
     return -sqrt_approx(q);
 }
 
+// Centred Box-Muller angle 2 pi (u2 - 1/2) in [-pi, pi) from f1 = 1 + u2, in
+// one fused multiply-add; cos/sin of the shifted angle are the negatives of
+// cos/sin(2 pi u2), which neg_radius' sign undoes.
+__device__ __forceinline__ float centred_angle(float f1) {
+    return fmaf(f1, 6.28318530717958648f, -9.42477796076937972f);
+}
+
 // Box-Muller pair for channel pair p: a[p] = rho cos(2 pi u2), a[p+1] = rho
-// sin(2 pi u2). The angle is centred, 2 pi (u2 - 1/2) in [-pi, pi), where the
-// hardware sine/cosine are most accurate; cos/sin of the shifted angle are the
-// negatives of the unshifted ones, which neg_radius' sign undoes.
+// sin(2 pi u2), evaluated where the hardware sine/cosine are most accurate.
 __device__ __forceinline__ void gauss_pair(float f0, float f1, float& a_even, float& a_odd) {
     const float nr = neg_radius(f0);
-    const float th = 6.28318530717958648f * (f1 - 1.5f);
     float s, c;
-    __sincosf(th, &s, &c);
+    __sincosf(centred_angle(f1), &s, &c);
     a_even = nr * c;
     a_odd = nr * s;
 }

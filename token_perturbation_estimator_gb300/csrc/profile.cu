@@ -5,7 +5,7 @@
 #include <mutex>
 #include <vector>
 
-#include "../../include/dust.h"
+#include "dust.h"
 #include "internal.cuh"
 
 namespace dust {

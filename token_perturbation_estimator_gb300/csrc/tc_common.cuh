@@ -68,6 +68,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     }
 }
 
+// As mbar_wait, but backs off with __nanosleep between polls: for threads
+// that wait most of the time (a TMA or MMA issuer sharing its sub-partition
+// with compute warps), so that the polling does not take issue slots.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                unsigned int ns = 64) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    while (true) {
+        __nanosleep(ns);
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer() - t0 > kWaitNs) return false;
+    }
+}
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int32_t x,
