@@ -33,7 +33,6 @@ if ROOT not in sys.path:
 
 METRIC = "Dust ĜW token-draws/s at 1 GB300; % tensor-pipe peak (ĝᵀX) and % HBM (noise)"
 UNIT = "token-draws/s"
-WORKLOAD = "mlp_up_512to2048_T16384_K8_gaussian"
 SMI_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -51,6 +50,9 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--flags", type=int, default=None,
                    help="extra dust_estimate_gW flags (e.g. force a path)")
+    p.add_argument("--workload", default="mlp_up",
+                   choices=["mlp_up", "toy", "qkv", "square_r", "square_g", "sweep"],
+                   help="mlp_up is the measured headline; the others are for study")
     return p.parse_args(argv)
 
 
@@ -149,7 +151,9 @@ def make_inputs(w, dev):
     import token_perturbation_estimator_gb300 as dust
     import workloads as wl
 
-    X = torch.from_numpy(wl.make_X(w)).to(dev).to(torch.bfloat16)
+    X = torch.from_numpy(wl.make_X(w)).to(dev)
+    if w.x_dtype == "bf16":
+        X = X.to(torch.bfloat16)
     dplant = torch.from_numpy(wl.make_dplant(w)).to(dev)
     eps = torch.from_numpy(wl.make_eps(w)).to(dev)
     a = torch.empty((1, w.T, w.d_out), dtype=torch.float32, device=dev)
@@ -165,45 +169,78 @@ def make_inputs(w, dev):
     return X, delta.contiguous(), so
 
 
+WORKLOADS = {
+    "mlp_up": "mlp_up_512to2048_T16384_K8_gaussian",
+    "toy": "toy_fp32_64x64_T256_K4_rademacher",
+    "qkv": "qkv_1024to3072_T16384_K16_gaussian_gamma0.9",
+    "square_r": "square_4096_T32768_K64_rademacher",
+    "square_g": "square_4096_T32768_K64_gaussian",
+    "sweep": "sweep_12x4_sites_T65536_K32_gaussian",
+}
+
+
+def workload_sites(name):
+    import workloads as wl
+    if name == "sweep":
+        return wl.sweep_sites()
+    return [{"mlp_up": wl.MLP_UP, "toy": wl.TOY, "qkv": wl.QKV_DECAY, "square_r": wl.SQUARE_R,
+             "square_g": wl.SQUARE_G}[name]]
+
+
+def make_inputs_fast(w, dev, site):
+    """Device-generated inputs for the many-site sweep: X ~ N(0, 1) in bf16
+    from a seeded device generator, loss changes with the planted
+    construction's marginal distribution (values do not change the work)."""
+    import torch
+    import workloads as wl
+    g = torch.Generator(device=dev)
+    g.manual_seed(1000 + site)
+    X = torch.randn((w.T, w.d_in), generator=g, device=dev).to(torch.bfloat16)
+    delta = torch.from_numpy(wl.marginal_delta(w)).to(dev)
+    so = torch.from_numpy(wl.seq_offsets(w)).to(dev)
+    return X, delta, so
+
+
 # ---------------------------------------------------------- roofline -----
 
-def roofline_for(stage, ms_per_launch, w, peaks, path):
-    """Roofline of the dominant kernel family. Algorithmic work per launch:
+def roofline_for(stage, ms_per_step, sites, peaks):
+    """Roofline of the dominant kernel family, from its CUDA-event time per
+    step and the algorithmic work of one step (summed over the step's sites):
       weight / fused (Gaussian): 2 transcendental (XU) ops per element-draw
         (Box-Muller's log, sqrt, sin, cos per channel pair) -> bound "alu"
         against the XU pipe: 16 ops/clk/SM x 152 SMs x 2.07 GHz;
-      weight / fused (Rademacher): 1 hash word per element-draw, 6 integer
-        ALU ops each -> bound "alu" against 64 int ops/clk/SM x 152 x 2.07 GHz;
+      weight / fused (Rademacher): 4 integer-ALU-pipe ops per element-draw (the
+        key xor, fmix32's xor-shift by 13 (shift + xor) and the sign merge into
+        the reward; its two multiplies issue on the FMA pipe) -> bound "alu"
+        against the ALU pipe: 64 ops/clk/SM x 152 SMs x 2.07 GHz;
       gemm_tc: 2 T d_in d_out FLOP -> bound "tensor" (measured bf16 peak);
       gemm_simt: same FLOP on FFMA -> "alu", 256 FLOP/clk/SM x 152 x 2.07 GHz."""
     sm, clk = 152, 2.07e9
-    s = ms_per_launch / 1000.0
+    s = ms_per_step / 1000.0
+    el = float(sum(w.element_draws for w in sites))
+    fl = float(sum(w.gemm_flops for w in sites))
     if stage in ("weight", "fused"):
-        if w.kind == 1:
-            ops = 2.0 * w.element_draws
-            peak = 16 * sm * clk
+        if sites[0].kind == 1:
+            ops, peak = 2.0 * el, 16 * sm * clk
         else:
-            ops = 6.0 * w.element_draws
-            peak = 64 * sm * clk
+            ops, peak = 4.0 * el, 64 * sm * clk
         ach = ops / s
         return {"bound": "alu", "achieved": ach / 1e9, "peak": peak / 1e9, "unit": "Gop/s",
                 "frac": ach / peak, "traffic": None, "kernel": stage,
-                "algorithmic_per_launch": ops,
+                "algorithmic_per_step": ops,
                 "peak_source": "derived: unit counts x 152 SMs x 2.07 GHz max SM clock"}
     if stage == "gemm_tc":
-        fl = float(w.gemm_flops)
         peak = peaks.get("bf16_tflops_sustained", 1694.3) * 1e12
         ach = fl / s
         return {"bound": "tensor", "achieved": ach / 1e12, "peak": peak / 1e12,
                 "unit": "TFLOP/s", "frac": ach / peak, "traffic": None, "kernel": stage,
-                "algorithmic_per_launch": fl,
+                "algorithmic_per_step": fl,
                 "peak_source": "MEASURED_PEAKS.json bf16_tflops_sustained (of measured)"}
-    fl = float(w.gemm_flops)
     peak = 256 * sm * clk
     ach = fl / s
     return {"bound": "alu", "achieved": ach / 1e12, "peak": peak / 1e12, "unit": "TFLOP/s",
             "frac": ach / peak, "traffic": None, "kernel": stage,
-            "algorithmic_per_launch": fl,
+            "algorithmic_per_step": fl,
             "peak_source": "derived: 128 FFMA lanes x 2 FLOP x 152 SMs x 2.07 GHz"}
 
 
@@ -256,36 +293,44 @@ def traffic_from_profiles(kernel):
 
 # ------------------------------------------------------------- cpu leg ----
 
-def cpu_oracle_rate(w, target_s, max_seqs=None):
+def cpu_oracle_rate(sites, target_s):
     """Time the fp64 oracle on a bounded sample of the workload: whole
-    sequences (all channels, all draws), grown until about target_s."""
+    sequences of each site (all channels, all draws), grown until the sample
+    takes about target_s."""
     import numpy as np
     import oracle
     import workloads as wl
 
-    X_all = wl.to_bf16_exact(wl.make_X(w))
-    dp_all = wl.make_dplant(w)
-    eps_all = wl.make_eps(w)
-    max_seqs = max_seqs or w.n_seq
-
-    def run(nseq):
+    def run(w, nseq):
         T = nseq * w.seq_len
         so = (np.arange(nseq + 1) * w.seq_len).astype(np.int32)
-        delta = oracle.planted_delta(dp_all[:T], w.seed, w.kind, 0, w.K, np.float32(w.sigma),
-                                     w.curvature, eps_all[:, :T]).astype(np.float32)
+        rng = np.random.default_rng(7)
+        X = wl.to_bf16_exact(rng.standard_normal((T, w.d_in), dtype=np.float32)) \
+            if w.x_dtype == "bf16" else rng.standard_normal((T, w.d_in), dtype=np.float32)
+        dp = rng.standard_normal((T, w.d_out), dtype=np.float32)
+        eps = (w.eps_std * rng.standard_normal((w.K, T))).astype(np.float32)
+        delta = oracle.planted_delta(dp, w.seed, w.kind, 0, w.K, np.float32(w.sigma),
+                                     w.curvature, eps).astype(np.float32)
         t0 = time.perf_counter()
-        oracle.estimate_gW(X_all[:T], delta, w.d_out, so, w.seed, w.kind, 0,
-                           np.float32(w.sigma), np.float32(w.gamma), 1.0, oracle.CENTER)
+        oracle.estimate_gW(X, delta, w.d_out, so, w.seed, w.kind, 0, np.float32(w.sigma),
+                           np.float32(w.gamma), 1.0, oracle.CENTER)
         return time.perf_counter() - t0, T
 
-    t1, T1 = run(1)
-    nseq = int(max(1, min(max_seqs, round(target_s / max(t1, 1e-3)))))
-    if nseq > 1:
-        t1, T1 = run(nseq)
-    return {"value": w.K * T1 / t1, "unit": UNIT, "cores": oracle.num_threads(),
-            "kind": "oracle",
-            "sample": "%d of %d sequences (%d tokens x %d draws x d_out %d x d_in %d), "
-                      "%.1f s" % (T1 // w.seq_len, w.n_seq, T1, w.K, w.d_out, w.d_in, t1)}
+    kinds = {}
+    for w in sites:  # one representative per distinct shape
+        kinds.setdefault((w.d_in, w.d_out, w.gamma), w)
+    reps = list(kinds.values())
+    t1 = sum(run(w, 1)[0] for w in reps)
+    nseq = int(max(1, min(min(w.n_seq for w in reps), round(target_s / max(t1, 1e-3)))))
+    tot_t, tot_u, desc = 0.0, 0, []
+    for w in reps:
+        t, T = run(w, nseq)
+        tot_t += t
+        tot_u += w.K * T
+        desc.append("%d of %d sequences of %d->%d (%d tokens x %d draws)"
+                    % (nseq, w.n_seq, w.d_in, w.d_out, T, w.K))
+    return {"value": tot_u / tot_t, "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": "; ".join(desc) + "; %.1f s" % tot_t}
 
 
 def run_reference(args):
@@ -322,7 +367,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": WORKLOAD, "sample_tokens_per_step": T,
+        "data": "synthetic", "config": {"workload": WORKLOADS["mlp_up"], "sample_tokens_per_step": T,
                                         "d_in": w.d_in, "d_out": w.d_out, "K": w.K},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": "one %d-token sequence per step, all draws and channels"
@@ -366,19 +411,30 @@ def run_gb300(args):
         if pg is not None:
             pg.barrier()
 
-    w = wl.MLP_UP
-    X, delta, so = make_inputs(w, dev)
+    sites = workload_sites(args.workload)
     flags = dust.CENTER | (args.flags or 0)
-    path = dust.dust_estimate_gW_path(w.T, w.d_in, w.d_out, w.K, dust.BF16, flags)
-    ws_bytes = dust.dust_estimate_gW_workspace(w.T, w.d_in, w.d_out, w.K, dust.BF16, flags)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    gW = torch.empty((w.d_out, w.d_in), dtype=torch.float32, device=dev)
-    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)  # 256 MB > L2
     stream = torch.cuda.current_stream()
+    bundles = []
+    for i, w in enumerate(sites):
+        if len(sites) == 1:
+            X, delta, so = make_inputs(w, dev)
+        else:
+            X, delta, so = make_inputs_fast(w, dev, i)
+        xd = dust.BF16 if X.dtype == torch.bfloat16 else dust.F32
+        ws = torch.empty(dust.dust_estimate_gW_workspace(w.T, w.d_in, w.d_out, w.K, xd, flags),
+                         dtype=torch.uint8, device=dev)
+        gW = torch.empty((w.d_out, w.d_in), dtype=torch.float32, device=dev)
+        bundles.append({"w": w, "X": X, "delta": delta, "so": so, "ws": ws, "gW": gW,
+                        "path": dust.dust_estimate_gW_path(w.T, w.d_in, w.d_out, w.K, xd, flags)})
+    units = sum(w.token_draws for w in sites)
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)  # 256 MB > L2
 
     def step():
-        dust.dust_estimate_gW(X, delta, w.d_out, so, w.seed, w.kind, 0, w.sigma, w.gamma, 1.0,
-                              flags, gW=gW, workspace=ws, stream=stream)
+        for b in bundles:
+            w = b["w"]
+            dust.dust_estimate_gW(b["X"], b["delta"], w.d_out, b["so"], w.seed, w.kind, 0,
+                                  w.sigma, w.gamma, 1.0, flags, gW=b["gW"], workspace=b["ws"],
+                                  stream=stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -402,7 +458,7 @@ def run_gb300(args):
         torch.cuda.synchronize()
     barrier()
     ms_total = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
-    value, ms_per_step = aggregate(w.token_draws, ms_total, args.steps, world, max_over_ranks)
+    value, ms_per_step = aggregate(units, ms_total, args.steps, world, max_over_ranks)
 
     # ---- profiled pass (same steps) for per-kernel times
     dust.dust_profile_enable(True)
@@ -415,26 +471,31 @@ def run_gb300(args):
     dust.dust_profile_enable(False)
     launches_per_step = sum(v["launches"] for v in prof.values()) / args.steps
     top = max(prof.items(), key=lambda kv: kv[1]["total_ms"])
-    top_ms = top[1]["total_ms"] / top[1]["launches"]
     peaks = load_peaks()
-    roof = roofline_for(top[0], top_ms, w, peaks, path)
-    roof["traffic"] = traffic_from_profiles(top[0])
+    roof = roofline_for(top[0], top[1]["total_ms"] / args.steps, sites, peaks)
+    roof["launches_per_step"] = top[1]["launches"] / args.steps
+    roof["traffic"] = traffic_from_profiles(top[0]) if len(sites) == 1 else None
+    tot_ms = sum(x["total_ms"] for x in prof.values())
     breakdown = {k: {"launches": v["launches"],
                      "ms_per_launch": v["total_ms"] / v["launches"],
-                     "share": v["total_ms"] / sum(x["total_ms"] for x in prof.values())}
+                     "share": v["total_ms"] / tot_ms}
                  for k, v in prof.items()}
 
     # ---- end to end through the host-buffer C ABI entry point
-    Xh = X.cpu().pin_memory()
-    dh = delta.cpu().pin_memory()
-    sh = so.cpu().pin_memory()
-    gh = torch.empty((w.d_out, w.d_in), dtype=torch.float32).pin_memory()
-    Xs, ds, ss = torch.empty_like(X), torch.empty_like(delta), torch.empty_like(so)
-    gs = torch.empty_like(gW)
+    hosts = []
+    for b in bundles:
+        hosts.append({"Xh": b["X"].cpu().pin_memory(), "dh": b["delta"].cpu().pin_memory(),
+                      "sh": b["so"].cpu().pin_memory(),
+                      "gh": torch.empty(tuple(b["gW"].shape), dtype=torch.float32).pin_memory(),
+                      "Xs": torch.empty_like(b["X"]), "ds": torch.empty_like(b["delta"]),
+                      "ss": torch.empty_like(b["so"]), "gs": torch.empty_like(b["gW"])})
 
     def e2e_step():
-        dust.dust_estimate_gW_host(Xh, Xs, dh, ds, sh, ss, gh, gs, w.d_out, w.seed, w.kind, 0,
-                                   w.sigma, w.gamma, 1.0, flags, workspace=ws, stream=stream)
+        for b, h in zip(bundles, hosts):
+            w = b["w"]
+            dust.dust_estimate_gW_host(h["Xh"], h["Xs"], h["dh"], h["ds"], h["sh"], h["ss"],
+                                       h["gh"], h["gs"], w.d_out, w.seed, w.kind, 0, w.sigma,
+                                       w.gamma, 1.0, flags, workspace=b["ws"], stream=stream)
         stream.synchronize()
 
     for _ in range(3):
@@ -445,28 +506,36 @@ def run_gb300(args):
     for _ in range(args.e2e_steps):
         e2e_step()
     e2e_s = max_over_ranks(time.perf_counter() - t0)
-    e2e_value = world * w.token_draws * args.e2e_steps / e2e_s
-    h2d = Xh.numel() * Xh.element_size() + dh.numel() * 4 + sh.numel() * 4
-    d2h = gh.numel() * 4
+    e2e_value = world * units * args.e2e_steps / e2e_s
+    h2d = sum(h["Xh"].numel() * h["Xh"].element_size() + h["dh"].numel() * 4 +
+              h["sh"].numel() * 4 for h in hosts)
+    d2h = sum(h["gh"].numel() * 4 for h in hosts)
     # the two results agree (same arguments, deterministic)
-    if not torch.equal(gh, gW.cpu()):
-        raise RuntimeError("host-buffer path disagrees with the device path")
+    for b, h in zip(bundles, hosts):
+        if not torch.equal(h["gh"], b["gW"].cpu()):
+            raise RuntimeError("host-buffer path disagrees with the device path")
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_oracle_rate(w, args.cpu_seconds)
+        cpu = cpu_oracle_rate(sites, args.cpu_seconds)
 
     if rank == 0:
+        w0 = sites[0]
+        cfg = {"workload": WORKLOADS[args.workload], "sites": len(sites),
+               "token_draws_per_step": units,
+               "noise": "gaussian" if w0.kind == 1 else "rademacher",
+               "x_dtype": w0.x_dtype, "paths": sorted({b["path"] for b in bundles}),
+               "parallelism": "replicas" if world > 1 else "single",
+               "l2": "flushed (256 MB write) between timed steps"}
+        if len(sites) == 1:
+            cfg.update({"d_in": w0.d_in, "d_out": w0.d_out, "T": w0.T, "n_seq": w0.n_seq,
+                        "K": w0.K, "sigma": w0.sigma, "gamma": w0.gamma})
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "d_in": w.d_in, "d_out": w.d_out, "T": w.T,
-                       "n_seq": w.n_seq, "K": w.K, "sigma": w.sigma, "gamma": w.gamma,
-                       "noise": "gaussian", "x_dtype": "bf16", "path": path,
-                       "parallelism": "replicas" if world > 1 else "single",
-                       "l2": "flushed (256 MB write) between timed steps"},
+            "dtype": "bf16" if w0.x_dtype == "bf16" else "f32", "data": "synthetic",
+            "config": cfg,
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -474,7 +543,7 @@ def run_gb300(args):
             "gpu_launches": int(round(launches_per_step * args.steps)),
             "clocks": clocks.summary(),
             "breakdown": breakdown,
-            "profiled_ms_per_step": sum(v["total_ms"] for v in prof.values()) / args.steps,
+            "profiled_ms_per_step": tot_ms / args.steps,
         }
         print(json.dumps(line), flush=True)
     if pg is not None:

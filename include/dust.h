@@ -290,6 +290,18 @@ dust_status dust_profile_enable(int32_t on);
 int32_t dust_profile_read(dust_profile_entry* out, int32_t max_entries);
 
 /*
+ * dust_debug_inject_timeout — test hook for the device-side failure path (no
+ * counterpart on the pages). With on != 0, the next tensor-core contraction
+ * launched by this process (dust_contract or the unfused dust_estimate_gW
+ * path) makes its MMA thread wait on an mbarrier that no thread ever arrives
+ * at. The wait gives up after its 1 s limit, the kernel lets its issued TMA
+ * copies land, frees its tensor memory and returns without writing gW, and
+ * dust_last_error then reports DUST_ERR_TIMEOUT; the CUDA context stays
+ * usable. No fault, trap or hang is involved. One-shot; process-global.
+ */
+dust_status dust_debug_inject_timeout(int32_t on);
+
+/*
  * dust_last_error — synchronise `stream`, then return and clear the device
  * status word (DUST_OK, or DUST_ERR_TIMEOUT when a kernel's bounded wait ran
  * out since the last call). DUST_ERR_CUDA if the synchronisation failed.

@@ -282,3 +282,22 @@ def test_fused_limits():
         dust.dust_estimate_gW_path(1024, 520, 256, 8, dust.BF16, dust.CENTER | dust.FORCE_FUSED)
     with pytest.raises(dust.DustError):
         dust.dust_estimate_gW_path(1024, 64, 64, 8, dust.F32, dust.CENTER | dust.FORCE_FUSED)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("site", [0, 1, 2, 3], ids=["qkv", "o", "up", "down"])
+def test_sweep_site_full_size_sampled(site):
+    """One layer of the 12-layer sweep at full size (65,536 tokens, K = 32):
+    QKV 512->1536 (gamma 0.9), O 512->512, up 512->2048, down 2048->512."""
+    w = wl.sweep_sites()[site]
+    X, delta, so = _inputs(w, planted=False)
+    got = _run(w, X, delta, so, dust.CENTER).double().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    rng = np.random.default_rng(11)
+    n = 16
+    chan = rng.integers(0, w.d_out, n)
+    col = rng.integers(0, w.d_in, n)
+    r = oracle.credit(delta, so, np.float32(w.gamma), oracle.CENTER)
+    want = oracle.gW_entries(X, r, w.d_out, chan, col, w.seed, w.kind, 0, np.float32(w.sigma),
+                             1.0, oracle.CENTER)
+    assert rel_fro(got[chan, col], want) <= 1e-2

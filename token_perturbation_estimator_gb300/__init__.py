@@ -64,6 +64,7 @@ def _signatures():
         "dust_last_error": (i32, [P]),
         "dust_credit_scan_noalloc_capacity": (SZ, []),
         "dust_credit_scan_noalloc": (i32, [P, i64, i64, P, i64, f32, u32, P, P]),
+        "dust_debug_inject_timeout": (i32, [i32]),
         "dust_profile_enable": (i32, [i32]),
         "dust_profile_read": (i32, [P, i32]),
     }

@@ -30,6 +30,10 @@ struct ProfScope {
     int slot;
 };
 
+// Test hook: true once after dust_debug_inject_timeout(1); the next
+// tensor-core contraction then makes its bounded wait run out.
+bool take_stall_injection();
+
 // Token chunk of the credit scan (one CTA, 32 lanes x 8 tokens).
 constexpr int kScanChunk = 256;
 

@@ -39,6 +39,7 @@ struct Ctl {
     uint64_t full[kStages];
     uint64_t empty[kStages];
     uint64_t done;
+    uint64_t never;  // no thread ever arrives here (test hook for the bounded waits)
     uint32_t tmem;
     int abort;
     int issued;
@@ -48,7 +49,7 @@ struct Ctl {
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               int64_t d_in, int64_t d_out, int64_t T, int64_t slice, float* __restrict__ out,
-              float scale, int mode, unsigned int* __restrict__ status) {
+              float scale, int mode, unsigned int* __restrict__ status, int stall) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -67,6 +68,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mbar_init(&ctl->empty[i], 1);
         }
         tc::mbar_init(&ctl->done, 1);
+        tc::mbar_init(&ctl->never, 1);
         ctl->abort = 0;
         ctl->issued = 0;
         ctl->consumed = 0;
@@ -108,8 +110,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ctl->issued = it;
     } else if (warp == 1 && lane == 0) {
+        // Test hook: wait on a barrier no one arrives at, so that the bounded
+        // wait runs out and the kernel takes its timeout path.
+        if (stall && !tc::mbar_wait(&ctl->never, 0)) *abort_flag = 1;
         int it = 0;
-        for (; it < n_k; ++it) {
+        for (; it < n_k && !*abort_flag; ++it) {
             const int st = it % kStages;
             const uint32_t ph = (it / kStages) & 1;
             if (!tc::mbar_wait(&ctl->full[st], ph) || *abort_flag) {
@@ -266,7 +271,8 @@ cudaError_t launch_tc_gemm(const void* g, const void* X, int64_t T, int64_t d_in
     {
         ProfScope ps(kStageGemmTc, s);
         k_gemm_tc<<<grid, kThreads, kSmemBytes, s>>>(ta, tb, d_in, d_out, T, slice,
-                                                     S_used > 1 ? partials : gW, scale, mode, st);
+                                                     S_used > 1 ? partials : gW, scale, mode, st,
+                                                     take_stall_injection() ? 1 : 0);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || S_used == 1) return e;

@@ -1,6 +1,7 @@
 // Per-kernel event timing for benchmarks (dust_profile_enable /
 // dust_profile_read). Off by default; when on, each launch is bracketed by
 // two CUDA events on the launching stream.
+#include <atomic>
 #include <cstdio>
 #include <mutex>
 #include <vector>
@@ -55,9 +56,20 @@ ProfScope::~ProfScope() {
     if (slot < static_cast<int>(g_recs.size())) cudaEventRecord(g_recs[slot].b, s);
 }
 
+namespace {
+std::atomic<int> g_inject{0};
+}  // namespace
+
+bool take_stall_injection() { return g_inject.exchange(0) != 0; }
+
 }  // namespace dust
 
 extern "C" {
+
+dust_status dust_debug_inject_timeout(int32_t on) {
+    dust::g_inject.store(on ? 1 : 0);
+    return DUST_OK;
+}
 
 dust_status dust_profile_enable(int32_t on) {
     std::lock_guard<std::mutex> lk(dust::g_mu);
