@@ -68,7 +68,7 @@ int choose_path(int64_t T, int64_t d_in, int64_t d_out, int64_t K, dust_dtype x_
 }
 
 struct Layout {
-    size_t scan = 0, g = 0, gemm = 0, total = 0;
+    size_t sync = kSyncBytes, scan = 0, g = 0, gemm = 0, total = 0;
     int path = DUST_PATH_SIMT;
     int g_bf16 = 0;
 };
@@ -85,7 +85,7 @@ Layout layout(int64_t T, int64_t d_in, int64_t d_out, int64_t K, dust_dtype x_dt
     if (L.path == DUST_PATH_FUSED_TC) {
         L.g = 0;
         L.gemm = a256(fused_workspace_bytes(T, d_in, d_out));
-        L.total = L.scan + L.gemm;
+        L.total = L.sync + L.scan + L.gemm;
         return L;
     }
     L.g = a256(static_cast<size_t>(T) * static_cast<size_t>(d_out) * (L.g_bf16 ? 2 : 4));
@@ -95,8 +95,7 @@ Layout layout(int64_t T, int64_t d_in, int64_t d_out, int64_t K, dust_dtype x_dt
         if (tcb > gemm) gemm = tcb;
     }
     L.gemm = a256(gemm);
-    L.total = L.scan + L.g + L.gemm;
-    if (L.total == 0) L.total = 256;
+    L.total = L.sync + L.scan + L.g + L.gemm;
     return L;
 }
 
@@ -229,7 +228,7 @@ dust_status dust_contract_workspace(size_t* bytes, int64_t T, int64_t d_in, int6
     size_t b = simt_gemm_workspace_bytes(T, d_in, d_out);
     const size_t tcb = tc_gemm_workspace_bytes(T, d_in, d_out);
     if (tcb > b) b = tcb;
-    *bytes = a256(b) + 256;
+    *bytes = kSyncBytes + a256(b) + 256;
     return DUST_OK;
 }
 
@@ -248,10 +247,11 @@ dust_status dust_contract(const void* g, const void* X, dust_dtype dtype, int64_
     if (!g || !X) return DUST_ERR_INVALID_ARG;
     if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
         return DUST_ERR_WORKSPACE;
-    float* part = static_cast<float*>(workspace);
+    float* part = reinterpret_cast<float*>(static_cast<char*>(workspace) + kSyncBytes);
     const bool bf16 = dtype == DUST_BF16;
     cudaError_t e;
-    if (bf16 && !(flags & DUST_FORCE_SIMT) && tc_gemm_supported(g, X, d_in, d_out))
+    const bool tc = bf16 && !(flags & DUST_FORCE_SIMT) && tc_gemm_supported(g, X, d_in, d_out);
+    if (tc)
         e = launch_tc_gemm(g, X, T, d_in, d_out, scale, acc, gW, part, s);
     else
         e = launch_simt_gemm(g, bf16, X, bf16, T, d_in, d_out, scale, acc, gW, part, s);
@@ -306,14 +306,17 @@ dust_status dust_estimate_gW(const void* X, dust_dtype x_dtype, int64_t T, int64
         return DUST_ERR_WORKSPACE;
 
     char* ws = static_cast<char*>(workspace);
+    unsigned int* sync = reinterpret_cast<unsigned int*>(ws);  // [0]: the scan's ticket
+    ws += L.sync;
     ScanBuffers b = scan_carve(ws, K, T);
     void* g = ws + L.scan;
     float* part = reinterpret_cast<float*>(ws + L.scan + L.g);
     const float coef = static_cast<float>(-1.0 / (static_cast<double>(K) * sigma));
     const bool anti = (flags & DUST_ANTITHETIC) != 0;
 
+    if (cudaMemsetAsync(sync, 0, kSyncBytes, s) != cudaSuccess) return DUST_ERR_CUDA;
     cudaError_t e = launch_scan(delta, K, T, seq_offsets, n_seq, gamma,
-                                (flags & DUST_CENTER) != 0, b, s);
+                                (flags & DUST_CENTER) != 0, b, s, sync);
     if (e != cudaSuccess) return DUST_ERR_CUDA;
     if (L.path == DUST_PATH_FUSED_TC) {
         float* fpart = reinterpret_cast<float*>(ws + L.scan);

@@ -75,9 +75,11 @@ cudaError_t launch_jitter(void* y, int y_bf16, int64_t ld_y, int64_t T, int64_t 
 
 // Centring + chunk-local scan + chunk carries. After it, r holds chunk-local
 // values; the true r is r[t][i] + P[t] * carry[t / kScanChunk][i].
+// With `ticket` (a zeroed device word) the carry pass runs in the scan
+// kernel's last CTA when the summaries fit; otherwise as a second kernel.
 cudaError_t launch_scan(const float* delta, int64_t K, int64_t T, const int32_t* seq_offsets,
                         int64_t n_seq, float gamma, bool center, const ScanBuffers& b,
-                        cudaStream_t s);
+                        cudaStream_t s, unsigned int* ticket = nullptr);
 cudaError_t launch_scan_fixup(const ScanBuffers& b, int64_t K, int64_t T, cudaStream_t s);
 
 // g[t][c] = coef * sum_i r[t][i] a_t^(draw_begin+i)[c]; with `fix` the scan
@@ -104,6 +106,10 @@ size_t tc_gemm_workspace_bytes(int64_t T, int64_t d_in, int64_t d_out);
 cudaError_t launch_tc_gemm(const void* g, const void* X, int64_t T, int64_t d_in, int64_t d_out,
                            float scale, bool accumulate, float* gW, float* partials,
                            cudaStream_t s);
+
+// Bytes of per-call synchronisation words (the scan's ticket) at the head of
+// a workspace; zeroed by one cudaMemsetAsync per call.
+constexpr size_t kSyncBytes = 4096;
 
 // Fused weighting + tensor-core contraction (d_in <= 512): g tiles are made
 // in shared memory and never written to HBM.

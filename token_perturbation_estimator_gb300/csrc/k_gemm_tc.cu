@@ -25,15 +25,31 @@ namespace dust {
 
 namespace {
 
-constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 4;
-constexpr int kBoxBytes = 64 * kBK * 2;                 // one 64 x 64 bf16 box: 8 KB
-constexpr int kABytes = (kBM / 64) * kBoxBytes;          // 16 KB
-constexpr int kBBytes = (kBN / 64) * kBoxBytes;          // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;           // 48 KB
+#ifndef DUST_GEMM_MT
+#define DUST_GEMM_MT 1       // 128-row accumulators per CTA (1 or 2)
+#endif
+#ifndef DUST_GEMM_BN
+#define DUST_GEMM_BN 256     // inputs per CTA tile (64..256)
+#endif
+#ifndef DUST_GEMM_BK
+#define DUST_GEMM_BK 64      // tokens per stage
+#endif
+#ifndef DUST_GEMM_STAGES
+#define DUST_GEMM_STAGES 4
+#endif
+constexpr int kMT = DUST_GEMM_MT;
+constexpr int kBM = 128 * kMT, kBN = DUST_GEMM_BN, kBK = DUST_GEMM_BK, kStages = DUST_GEMM_STAGES;
+constexpr int kBoxBytes = 64 * kBK * 2;                 // one 64-wide bf16 box of kBK rows
+constexpr int kABytes = (kBM / 64) * kBoxBytes;
+constexpr int kBBytes = (kBN / 64) * kBoxBytes;
+constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
 constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kIdesc = tc::idesc_bf16_mn(kBM, kBN);
+constexpr uint32_t kTmemCols = (kMT * kBN <= 256) ? 256u : 512u;
+constexpr uint32_t kIdesc = tc::idesc_bf16_mn(128, kBN);
+static_assert(kMT * kBN <= 512, "accumulators must fit the 512 TMEM columns");
+static_assert(kBK % 16 == 0 && kBN % 64 == 0, "tile shape");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
 struct Ctl {
     uint64_t full[kStages];
@@ -126,9 +142,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t b = a + kABytes;
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk) {
-                const uint64_t ad = tc::sdesc_sw128(a + kk * 2048, kBoxBytes, 1024);
                 const uint64_t bd = tc::sdesc_sw128(b + kk * 2048, kBoxBytes, 1024);
-                tc::mma_bf16(tmem, ad, bd, kIdesc, (it | kk) != 0 ? 1u : 0u);
+#pragma unroll
+                for (int mt = 0; mt < kMT; ++mt) {
+                    const uint64_t ad =
+                        tc::sdesc_sw128(a + 2 * mt * kBoxBytes + kk * 2048, kBoxBytes, 1024);
+                    tc::mma_bf16(tmem + mt * kBN, ad, bd, kIdesc, (it | kk) != 0 ? 1u : 0u);
+                }
             }
             tc::mma_commit(&ctl->empty[st]);
         }
@@ -140,40 +160,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) *abort_flag = 1;
         if (ok && !*abort_flag && n_k > 0) {
             const int q = warp & 3;  // TMEM lane quarter this warp may access
-            const int64_t row = m0 + 32 * q + lane;
-            float* dst = nullptr;
-            if (row < d_out) {
-                dst = (mode == 0) ? out + (static_cast<int64_t>(blockIdx.z) * d_out + row) * d_in
-                                  : out + row * d_in;
-            }
 #pragma unroll 1
-            for (int c = 0; c < kBN / 32; ++c) {
-                float v[32];
-                tc::tmem_ld_32x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + c * 32, v);
-                const int64_t j0 = n0 + c * 32;
-                if (!dst || j0 >= d_in) continue;
-                if (j0 + 32 <= d_in) {
+            for (int mt = 0; mt < kMT; ++mt) {
+                const int64_t row = m0 + 128 * mt + 32 * q + lane;
+                float* dst = nullptr;
+                if (row < d_out) {
+                    dst = (mode == 0)
+                              ? out + (static_cast<int64_t>(blockIdx.z) * d_out + row) * d_in
+                              : out + row * d_in;
+                }
+#pragma unroll 1
+                for (int c = 0; c < kBN / 32; ++c) {
+                    float v[32];
+                    tc::tmem_ld_32x32(
+                        tmem + (static_cast<uint32_t>(32 * q) << 16) + mt * kBN + c * 32, v);
+                    const int64_t j0 = n0 + c * 32;
+                    if (!dst || j0 >= d_in) continue;
+                    if (j0 + 32 <= d_in) {
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        float4 w4 = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
-                        float4* p = reinterpret_cast<float4*>(dst + j0 + 4 * u);
-                        if (mode == 0) {
-                            *p = w4;
-                        } else if (mode == 1) {
-                            *p = make_float4(scale * w4.x, scale * w4.y, scale * w4.z, scale * w4.w);
-                        } else {
-                            float4 o = *p;
-                            *p = make_float4(o.x + scale * w4.x, o.y + scale * w4.y,
-                                             o.z + scale * w4.z, o.w + scale * w4.w);
+                        for (int u = 0; u < 8; ++u) {
+                            float4 w4 = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2],
+                                                    v[4 * u + 3]);
+                            float4* p = reinterpret_cast<float4*>(dst + j0 + 4 * u);
+                            if (mode == 0) {
+                                *p = w4;
+                            } else if (mode == 1) {
+                                *p = make_float4(scale * w4.x, scale * w4.y, scale * w4.z,
+                                                 scale * w4.w);
+                            } else {
+                                float4 o = *p;
+                                *p = make_float4(o.x + scale * w4.x, o.y + scale * w4.y,
+                                                 o.z + scale * w4.z, o.w + scale * w4.w);
+                            }
                         }
-                    }
-                } else {
+                    } else {
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) {
-                        if (j0 + u >= d_in) continue;
-                        if (mode == 0) dst[j0 + u] = v[u];
-                        else if (mode == 1) dst[j0 + u] = scale * v[u];
-                        else dst[j0 + u] += scale * v[u];
+                        for (int u = 0; u < 32; ++u) {
+                            if (j0 + u >= d_in) continue;
+                            if (mode == 0) dst[j0 + u] = v[u];
+                            else if (mode == 1) dst[j0 + u] = scale * v[u];
+                            else dst[j0 + u] += scale * v[u];
+                        }
                     }
                 }
             }
@@ -244,6 +271,10 @@ bool tc_gemm_supported(const void* g, const void* X, int64_t d_in, int64_t d_out
 size_t tc_gemm_workspace_bytes(int64_t T, int64_t d_in, int64_t d_out) {
     const int64_t S = tc_slices(T, d_in, d_out);
     return S > 1 ? sizeof(float) * static_cast<size_t>(S * d_out * d_in) : 0;
+}
+
+int64_t tc_gemm_tiles(int64_t d_in, int64_t d_out) {
+    return ((d_out + kBM - 1) / kBM) * ((d_in + kBN - 1) / kBN);
 }
 
 cudaError_t launch_tc_gemm(const void* g, const void* X, int64_t T, int64_t d_in, int64_t d_out,

@@ -40,7 +40,9 @@ __global__ void __launch_bounds__(256) k_scan_local(const float* __restrict__ de
                                                     int64_t T, const int32_t* __restrict__ so,
                                                     int64_t n_seq, float gamma, int center,
                                                     float* __restrict__ r, float* __restrict__ P,
-                                                    float* __restrict__ A, float* __restrict__ B) {
+                                                    float* __restrict__ A, float* __restrict__ B,
+                                                    float* __restrict__ carry,
+                                                    unsigned int* __restrict__ ticket) {
     __shared__ float s_m[kScanChunk];
     __shared__ float s_mean[kScanChunk];
     __shared__ float s_c[kDrawGroup][kScanChunk + 1];
@@ -147,6 +149,30 @@ __global__ void __launch_bounds__(256) k_scan_local(const float* __restrict__ de
         }
         __syncthreads();
     }
+    if (!ticket) return;
+    // The last CTA to finish runs the carry pass over all chunk summaries
+    // (the host picks this form only when they fit in s_c).
+    __shared__ unsigned int s_last;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = (atomicAdd(ticket, 1u) == gridDim.x - 1) ? 1u : 0u;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const int64_t nc = gridDim.x;
+    float* sA = &s_c[0][0];
+    float* sB = sA + nc * K;
+    for (int64_t e = tid; e < nc * K; e += blockDim.x) sA[e] = __ldcg(A + e);
+    for (int64_t e = tid; e < nc; e += blockDim.x) sB[e] = __ldcg(B + e);
+    __syncthreads();
+    for (int64_t i = tid; i < K; i += blockDim.x) {
+        float c = 0.0f;
+        carry[(nc - 1) * K + i] = 0.0f;
+        for (int64_t j = nc - 1; j >= 1; --j) {
+            c = fmaf(sB[j], c, sA[j * K + i]);
+            carry[(j - 1) * K + i] = c;
+        }
+    }
 }
 
 // carry[j][i] = A[j+1][i] + B[j+1] * carry[j+1][i], carry[last] = 0.
@@ -219,15 +245,20 @@ ScanBuffers scan_carve(void* ws, int64_t K, int64_t T) {
 
 cudaError_t launch_scan(const float* delta, int64_t K, int64_t T, const int32_t* seq_offsets,
                         int64_t n_seq, float gamma, bool center, const ScanBuffers& b,
-                        cudaStream_t s) {
+                        cudaStream_t s, unsigned int* ticket) {
     if (T == 0 || K == 0) return cudaSuccess;
+    // Carry pass inside the scan kernel's last CTA when the chunk summaries
+    // fit in its shared staging buffer and a zeroed ticket word is provided.
+    const bool merged =
+        ticket && b.n_chunks * (K + 1) <= static_cast<int64_t>(kDrawGroup) * (kScanChunk + 1);
     {
     ProfScope ps(kStageScanLocal, s);
     k_scan_local<<<static_cast<unsigned>(b.n_chunks), 256, 0, s>>>(
-        delta, K, T, seq_offsets, n_seq, gamma, center ? 1 : 0, b.r, b.P, b.A, b.B);
+        delta, K, T, seq_offsets, n_seq, gamma, center ? 1 : 0, b.r, b.P, b.A, b.B, b.carry,
+        merged ? ticket : nullptr);
     }
     cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess || merged) return e;
     const size_t smem = sizeof(float) * static_cast<size_t>(b.n_chunks * (K + 1));
     const int staged = smem <= kCarrySmem ? 1 : 0;
     static cudaError_t attr = cudaFuncSetAttribute(
