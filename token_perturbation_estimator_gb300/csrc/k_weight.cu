@@ -22,6 +22,14 @@ namespace {
 #ifndef DUST_WEIGHT_CPT
 #define DUST_WEIGHT_CPT 16
 #endif
+#ifndef DUST_WEIGHT_MINB
+#define DUST_WEIGHT_MINB 6       // resident CTAs per SM the register allocation must allow
+#endif
+#ifndef DUST_WEIGHT_UNROLL
+#define DUST_WEIGHT_UNROLL 2
+#endif
+constexpr int kMinBlocks = DUST_WEIGHT_MINB;
+constexpr int kUnrollW = DUST_WEIGHT_UNROLL;
 constexpr int kTok = 8;                 // tokens per CTA (one per warp)
 constexpr int kCpt = DUST_WEIGHT_CPT;   // channels per lane (8 or 16)
 constexpr int kCh = 32 * kCpt;          // channels per CTA
@@ -64,7 +72,7 @@ __device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16* g, int64_t 
 }
 
 template <int KIND, bool FIX, typename OutT>
-__global__ void __launch_bounds__(256) k_weight(const float* __restrict__ r,
+__global__ void __launch_bounds__(256, kMinBlocks) k_weight(const float* __restrict__ r,
                                                 const float* __restrict__ P,
                                                 const float* __restrict__ carry, int64_t K,
                                                 int64_t T, int64_t d_out, uint32_t skey,
@@ -113,7 +121,7 @@ __global__ void __launch_bounds__(256) k_weight(const float* __restrict__ r,
         __syncthreads();
         if (active) {
             if (KIND == 1) {
-#pragma unroll 2
+#pragma unroll kUnrollW
                 for (int k = 0; k < gn; ++k) {
                     const float rr = s_r[warp][k];
                     const uint2 key = s_key[k];
