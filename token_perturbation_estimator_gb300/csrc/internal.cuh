@@ -34,6 +34,46 @@ struct ProfScope {
 // tensor-core contraction then makes its bounded wait run out.
 bool take_stall_injection();
 
+// ---- Programmatic dependent launch. The estimator's kernels are launched so
+// that the next kernel on the stream may be scheduled while the previous one
+// drains (its prologue then overlaps the tail). Each such kernel calls
+// pdl_wait() before its first global memory access: griddepcontrol.wait
+// returns once every prerequisite grid has completed and its writes are
+// visible (at once when there is none), so stream order holds for all data.
+// pdl_trigger(), called right after the wait, lets the next kernel be
+// scheduled once every CTA of this one is past its own wait.
+#ifndef DUST_PDL
+#define DUST_PDL 1
+#endif
+
+__device__ __forceinline__ void pdl_wait() {
+#if DUST_PDL
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+}
+
+__device__ __forceinline__ void pdl_trigger() {
+#if DUST_PDL
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = DUST_PDL ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Token chunk of the credit scan (one CTA, 32 lanes x 8 tokens).
 constexpr int kScanChunk = 256;
 

@@ -166,6 +166,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tc_fence_after();
     const uint32_t tmem = ctl->tmem;
     volatile int* abort_flag = &ctl->abort;
+    pdl_wait();
+    pdl_trigger();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -456,14 +458,14 @@ cudaError_t launch_fused(const ScanBuffers& b, const void* X, int64_t K, int64_t
     fa.out = (S_used > 1) ? partials : gW;
     fa.status = st;
     dim3 grid(static_cast<unsigned>((d_out + kBM - 1) / kBM), static_cast<unsigned>(S_used));
+    cudaError_t e;
     {
         ProfScope ps(kStageFused, s);
         if (kind == 1)
-            k_fused<1><<<grid, kThreads, kSmemBytes, s>>>(tx, fa);
+            e = launch_pdl(k_fused<1>, grid, dim3(kThreads), kSmemBytes, s, tx, fa);
         else
-            k_fused<0><<<grid, kThreads, kSmemBytes, s>>>(tx, fa);
+            e = launch_pdl(k_fused<0>, grid, dim3(kThreads), kSmemBytes, s, tx, fa);
     }
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || S_used == 1) return e;
     return launch_reduce(partials, S_used, d_out * d_in, scale, accumulate, gW, s);
 }

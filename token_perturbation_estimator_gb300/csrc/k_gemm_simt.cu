@@ -20,6 +20,8 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const TG* __restrict__ g,
                                                    int64_t d_in, int64_t d_out, int64_t slice,
                                                    float* __restrict__ out, float scale,
                                                    int mode) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float sg[kBK][kBM];
     __shared__ float sx[kBK][kBN];
     const int tid = threadIdx.x;
@@ -88,6 +90,8 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const TG* __restrict__ g,
 __global__ void __launch_bounds__(256) k_reduce(const float* __restrict__ part, int64_t S,
                                                 int64_t n, float scale, int accumulate,
                                                 float* __restrict__ gW, int vec4) {
+    pdl_wait();
+    pdl_trigger();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int64_t tid = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
     if (vec4) {
@@ -139,18 +143,16 @@ cudaError_t run(const void* g, const void* X, int64_t T, int64_t d_in, int64_t d
               static_cast<unsigned>((d_out + kBM - 1) / kBM), static_cast<unsigned>(S_used));
     if (S_used == 1) {
         ProfScope ps(kStageGemmSimt, s);
-        k_gemm_simt<TG, TX><<<grid, 256, 0, s>>>(static_cast<const TG*>(g),
-                                                 static_cast<const TX*>(X), T, d_in, d_out,
-                                                 slice, gW, scale, accumulate ? 2 : 1);
-        return cudaGetLastError();
+        return launch_pdl(k_gemm_simt<TG, TX>, grid, dim3(256), 0, s,
+                          static_cast<const TG*>(g), static_cast<const TX*>(X), T, d_in, d_out,
+                          slice, gW, scale, accumulate ? 2 : 1);
     }
+    cudaError_t e;
     {
         ProfScope ps(kStageGemmSimt, s);
-        k_gemm_simt<TG, TX><<<grid, 256, 0, s>>>(static_cast<const TG*>(g),
-                                                 static_cast<const TX*>(X), T, d_in, d_out,
-                                                 slice, partials, scale, 0);
+        e = launch_pdl(k_gemm_simt<TG, TX>, grid, dim3(256), 0, s, static_cast<const TG*>(g),
+                       static_cast<const TX*>(X), T, d_in, d_out, slice, partials, scale, 0);
     }
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_reduce(partials, S_used, d_out * d_in, scale, accumulate, gW, s);
 }
@@ -165,9 +167,8 @@ cudaError_t launch_reduce(const float* partials, int64_t S, int64_t n, float sca
     ProfScope ps(kStageReduce, s);
     const int vec4 = ((n & 3) == 0) && (reinterpret_cast<uintptr_t>(gW) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(partials) % 16 == 0);
-    k_reduce<<<static_cast<unsigned>(rg), 256, 0, s>>>(partials, S, n, scale, accumulate ? 1 : 0,
-                                                       gW, vec4);
-    return cudaGetLastError();
+    return launch_pdl(k_reduce, dim3(static_cast<unsigned>(rg)), dim3(256), 0, s, partials, S, n,
+                      scale, accumulate ? 1 : 0, gW, vec4);
 }
 
 size_t simt_gemm_workspace_bytes(int64_t T, int64_t d_in, int64_t d_out) {

@@ -99,6 +99,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tc_fence_after();
     const uint32_t tmem = ctl->tmem;
     volatile int* abort_flag = &ctl->abort;
+    pdl_wait();  // g and X come from the kernels before this one
+    pdl_trigger();
 
     if (warp == 0 && lane == 0) {
         tc::prefetch_tmap(&tmA);
@@ -298,14 +300,14 @@ cudaError_t launch_tc_gemm(const void* g, const void* X, int64_t T, int64_t d_in
     const int64_t S_used = (T + slice - 1) / slice;
     dim3 grid(static_cast<unsigned>((d_in + kBN - 1) / kBN),
               static_cast<unsigned>((d_out + kBM - 1) / kBM), static_cast<unsigned>(S_used));
+    cudaError_t e;
     const int mode = (S_used > 1) ? 0 : (accumulate ? 2 : 1);
     {
         ProfScope ps(kStageGemmTc, s);
-        k_gemm_tc<<<grid, kThreads, kSmemBytes, s>>>(ta, tb, d_in, d_out, T, slice,
-                                                     S_used > 1 ? partials : gW, scale, mode, st,
-                                                     take_stall_injection() ? 1 : 0);
+        e = launch_pdl(k_gemm_tc, grid, dim3(kThreads), kSmemBytes, s, ta, tb, d_in, d_out, T,
+                       slice, S_used > 1 ? partials : gW, scale, mode, st,
+                       take_stall_injection() ? 1 : 0);
     }
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || S_used == 1) return e;
     return launch_reduce(partials, S_used, d_out * d_in, scale, accumulate, gW, s);
 }

@@ -43,8 +43,9 @@ __global__ void __launch_bounds__(256) k_scan_local(const float* __restrict__ de
                                                     float* __restrict__ A, float* __restrict__ B,
                                                     float* __restrict__ carry,
                                                     unsigned int* __restrict__ ticket) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float s_m[kScanChunk];
-    __shared__ float s_mean[kScanChunk];
     __shared__ float s_c[kDrawGroup][kScanChunk + 1];
 
     const int tid = threadIdx.x;
@@ -68,12 +69,21 @@ __global__ void __launch_bounds__(256) k_scan_local(const float* __restrict__ de
     } else {
         s_m[tid] = decay_of(t, T, so, n_seq, gamma);
     }
+    // Loads are issued in batches of independent registers before they are
+    // used, so a thread waits for one memory latency per batch rather than one
+    // per draw (the sum itself stays in draw order).
     float mean = 0.0f;
     if (center && K > 1 && t < T) {
-        for (int64_t i = 0; i < K; ++i) mean += delta[i * T + t];
+        for (int64_t i0 = 0; i0 < K; i0 += 8) {
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = (i0 + j < K) ? delta[(i0 + j) * T + t] : 0.0f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (i0 + j < K) mean += v[j];
+        }
         mean /= static_cast<float>(K);
     }
-    s_mean[tid] = mean;
     __syncthreads();
 
     // Lane maps of the decay products (draw-independent): P for the lane's 8
@@ -105,11 +115,16 @@ __global__ void __launch_bounds__(256) k_scan_local(const float* __restrict__ de
 
     for (int64_t g0 = 0; g0 < K; g0 += kDrawGroup) {
         const int gn = static_cast<int>(K - g0 < kDrawGroup ? K - g0 : kDrawGroup);
-        // Load the group's centred reductions c = -(delta - mean).
-        for (int k = 0; k < gn; ++k) {
-            float v = 0.0f;
-            if (t < T) v = -(delta[(g0 + k) * T + t] - s_mean[tid]);
-            s_c[k][tid] = v;
+        // Load the group's centred reductions c = -(delta - mean), all loads
+        // of the group in flight at once.
+        {
+            float v[kDrawGroup];
+#pragma unroll
+            for (int k = 0; k < kDrawGroup; ++k)
+                v[k] = (k < gn && t < T) ? delta[(g0 + k) * T + t] : 0.0f;
+#pragma unroll
+            for (int k = 0; k < kDrawGroup; ++k)
+                if (k < gn) s_c[k][tid] = (t < T) ? -(v[k] - mean) : 0.0f;
         }
         __syncthreads();
         for (int k = warp; k < gn; k += 8) {
@@ -182,6 +197,8 @@ __global__ void __launch_bounds__(256) k_carry(const float* __restrict__ A,
                                                const float* __restrict__ B, int64_t K,
                                                int64_t n_chunks, float* __restrict__ carry,
                                                int staged) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ float s_sum[];  // [n_chunks][K] A, then [n_chunks] B
     const float* sA = A;
     const float* sB = B;
@@ -207,6 +224,8 @@ __global__ void __launch_bounds__(256) k_carry(const float* __restrict__ A,
 __global__ void __launch_bounds__(256) k_fixup(float* __restrict__ r, const float* __restrict__ P,
                                                const float* __restrict__ carry, int64_t K,
                                                int64_t T) {
+    pdl_wait();
+    pdl_trigger();
     const int64_t n = K * T;
     for (int64_t q = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; q < n;
          q += (int64_t)gridDim.x * blockDim.x) {
@@ -251,13 +270,13 @@ cudaError_t launch_scan(const float* delta, int64_t K, int64_t T, const int32_t*
     // fit in its shared staging buffer and a zeroed ticket word is provided.
     const bool merged =
         ticket && b.n_chunks * (K + 1) <= static_cast<int64_t>(kDrawGroup) * (kScanChunk + 1);
+    cudaError_t e;
     {
     ProfScope ps(kStageScanLocal, s);
-    k_scan_local<<<static_cast<unsigned>(b.n_chunks), 256, 0, s>>>(
-        delta, K, T, seq_offsets, n_seq, gamma, center ? 1 : 0, b.r, b.P, b.A, b.B, b.carry,
-        merged ? ticket : nullptr);
+    e = launch_pdl(k_scan_local, dim3(static_cast<unsigned>(b.n_chunks)), dim3(256), 0, s, delta,
+                   K, T, seq_offsets, n_seq, gamma, center ? 1 : 0, b.r, b.P, b.A, b.B, b.carry,
+                   merged ? ticket : nullptr);
     }
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || merged) return e;
     const size_t smem = sizeof(float) * static_cast<size_t>(b.n_chunks * (K + 1));
     const int staged = smem <= kCarrySmem ? 1 : 0;
@@ -265,8 +284,8 @@ cudaError_t launch_scan(const float* delta, int64_t K, int64_t T, const int32_t*
         k_carry, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kCarrySmem));
     if (attr != cudaSuccess) return attr;
     ProfScope ps(kStageScanCarry, s);
-    k_carry<<<1, 256, staged ? smem : 0, s>>>(b.A, b.B, K, b.n_chunks, b.carry, staged);
-    return cudaGetLastError();
+    return launch_pdl(k_carry, dim3(1), dim3(256), staged ? smem : 0, s, b.A, b.B, K, b.n_chunks,
+                      b.carry, staged);
 }
 
 cudaError_t launch_scan_fixup(const ScanBuffers& b, int64_t K, int64_t T, cudaStream_t s) {
@@ -275,8 +294,8 @@ cudaError_t launch_scan_fixup(const ScanBuffers& b, int64_t K, int64_t T, cudaSt
     int64_t grid = (n + 255) / 256;
     if (grid > 152 * 32) grid = 152 * 32;
     ProfScope ps(kStageScanFixup, s);
-    k_fixup<<<static_cast<unsigned>(grid), 256, 0, s>>>(b.r, b.P, b.carry, K, T);
-    return cudaGetLastError();
+    return launch_pdl(k_fixup, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, b.r, b.P,
+                      b.carry, K, T);
 }
 
 }  // namespace dust

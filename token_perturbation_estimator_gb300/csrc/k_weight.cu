@@ -80,6 +80,8 @@ __global__ void __launch_bounds__(256, kMinBlocks) k_weight(const float* __restr
                                                 OutT* __restrict__ g, bool vec_ok) {
     __shared__ uint2 s_key[kGroup];  // folded keys of streams 0 and 1
     __shared__ float s_r[kTok][kGroup];
+    pdl_wait();
+    pdl_trigger();
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t tb = static_cast<int64_t>(blockIdx.x) * kTok;
@@ -168,14 +170,11 @@ cudaError_t launch_kind(const ScanBuffers& b, int64_t K, int64_t T, int64_t d_ou
     const bool vec_ok = (d_out % 8 == 0) && (reinterpret_cast<uintptr_t>(g) % 16 == 0);
     ProfScope ps(kStageWeight, s);
     if (g_bf16)
-        k_weight<KIND, FIX, __nv_bfloat16><<<grid, 256, 0, s>>>(
-            b.r, b.P, b.carry, K, T, d_out, skey, draw_begin, coef, anti,
-            static_cast<__nv_bfloat16*>(g), vec_ok);
-    else
-        k_weight<KIND, FIX, float><<<grid, 256, 0, s>>>(b.r, b.P, b.carry, K, T, d_out, skey,
-                                                        draw_begin, coef, anti,
-                                                        static_cast<float*>(g), vec_ok);
-    return cudaGetLastError();
+        return launch_pdl(k_weight<KIND, FIX, __nv_bfloat16>, grid, dim3(256), 0, s, b.r, b.P,
+                          b.carry, K, T, d_out, skey, draw_begin, coef, anti,
+                          static_cast<__nv_bfloat16*>(g), vec_ok);
+    return launch_pdl(k_weight<KIND, FIX, float>, grid, dim3(256), 0, s, b.r, b.P, b.carry, K, T,
+                      d_out, skey, draw_begin, coef, anti, static_cast<float*>(g), vec_ok);
 }
 
 }  // namespace
