@@ -104,6 +104,27 @@ def test_estimate_gW_small(w, force):
     assert rel_fro(got, want) <= tol, (path, rel_fro(got, want))
 
 
+@pytest.mark.parametrize("T,K,max_len", [(70000, 2, 9000), (900, 260, 300)])
+def test_estimate_gW_long_token_set_and_many_draws(T, K, max_len):
+    """Many scan chunks (70,000 tokens) and many draws (260, past one
+    weighting draw group): the chunk carries the weighting kernel folds in
+    and the draw grouping both reach the oracle's estimate."""
+    import torch
+    dev = cuda()
+    rng = np.random.default_rng(T + K)
+    so = offsets_from_lengths(random_lengths(rng, T, max_len))
+    d_in, d_out = 16, 24
+    X = bf16_round(rng.standard_normal((T, d_in))).astype(np.float32)
+    delta = (0.05 * rng.standard_normal((K, T))).astype(np.float32)
+    got = dust.dust_estimate_gW(torch.from_numpy(X).to(dev).to(torch.bfloat16),
+                                torch.from_numpy(delta).to(dev), d_out,
+                                torch.from_numpy(so).to(dev), 13, 1, 0, 1e-3, 0.95, 1.0,
+                                dust.CENTER).double().cpu().numpy()
+    want = oracle.estimate_gW(X, delta, d_out, so, 13, 1, 0, np.float32(1e-3),
+                              np.float32(0.95), 1.0, oracle.CENTER)
+    assert rel_fro(got, want) <= 1e-2
+
+
 def test_estimate_matches_brute_force_tiny():
     import torch
     dev = cuda()

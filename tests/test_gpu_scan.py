@@ -22,6 +22,13 @@ CASES = [
     (64, 2048, 2048, 1.0, True),     # undiscounted reward-to-go
     (100, 1000, 37, 0.98, True),
     (3, 20000, 20000, 0.999, False),  # one long sequence across many chunks
+    (5, 65536, 65536, 0.999, False),  # one sequence over 256 chunks
+    (2, 40000, 2, 0.9, True),         # > 4096 sequences: per-token offset search
+    (256, 600, 100, 0.9, True),       # many draws: several draw groups per chunk
+    (257, 600, 100, 0.9, True),       # a one-draw last group
+    (4, 70000, 5000, 0.99, True),
+    (2, 65537, 65537, 1.0, False),    # one undiscounted sequence, a 1-token last chunk
+    (8, 300000, 300000, 0.9999, False),  # too many chunk summaries to merge: separate carry kernel
 ]
 
 
@@ -39,7 +46,12 @@ def test_credit_scan_parity(K, T, max_len, gamma, center):
     got = r.cpu().numpy().T  # [K, T]
     want = oracle.credit(delta, so, np.float32(gamma), flags)
     assert got.shape == want.shape
-    assert rel_fro(got, want) <= 1e-5
+    # fp32 rounding of a first-order recurrence accumulates over its effective
+    # horizon h (the sequence, or 1/(1 - gamma) tokens when shorter): taken as
+    # a random walk of about 8 roundings of 2^-24 per token, bounded below by
+    # the 1e-5 of short horizons.
+    h = max_len if gamma >= 1.0 else min(max_len, 1.0 / (1.0 - gamma))
+    assert rel_fro(got, want) <= max(1e-5, 8 * 2.0 ** -24 * np.sqrt(h))
     scale = np.abs(want).max()
     assert np.max(np.abs(got - want)) <= 1e-5 * scale * max(1.0, np.sqrt(max_len) / 8)
 

@@ -100,12 +100,20 @@ __global__ void __launch_bounds__(256) k_reduce(const float* __restrict__ part, 
         float4* g4 = reinterpret_cast<float4*>(gW);
         for (int64_t q = tid; q < n4; q += stride) {
             float4 v = p4[q];
-            for (int64_t s = 1; s < S; ++s) {
-                const float4 w = p4[s * n4 + q];
-                v.x += w.x;
-                v.y += w.y;
-                v.z += w.z;
-                v.w += w.w;
+            // Up to 8 slices' loads in flight at once; the sum stays in slice order.
+            for (int64_t s0 = 1; s0 < S; s0 += 8) {
+                float4 w[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (s0 + j < S) w[j] = p4[(s0 + j) * n4 + q];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (s0 + j >= S) break;
+                    v.x += w[j].x;
+                    v.y += w[j].y;
+                    v.z += w[j].z;
+                    v.w += w[j].w;
+                }
             }
             float4 o = make_float4(scale * v.x, scale * v.y, scale * v.z, scale * v.w);
             if (accumulate) {

@@ -37,6 +37,10 @@ namespace {
 #ifndef DUST_GEMM_STAGES
 #define DUST_GEMM_STAGES 4
 #endif
+#ifndef DUST_GEMM_CLUSTER_REDUCE
+#define DUST_GEMM_CLUSTER_REDUCE 1  // reduce the token slices in a cluster (else partials)
+#endif
+constexpr bool kClusterReduce = DUST_GEMM_CLUSTER_REDUCE != 0;
 constexpr int kMT = DUST_GEMM_MT;
 constexpr int kBM = 128 * kMT, kBN = DUST_GEMM_BN, kBK = DUST_GEMM_BK, kStages = DUST_GEMM_STAGES;
 constexpr int kBoxBytes = 64 * kBK * 2;                 // one 64-wide bf16 box of kBK rows
@@ -61,6 +65,91 @@ struct Ctl {
     int issued;
     int consumed;
 };
+
+// Cluster reduction of the token slices (modes 3 and 4). The S CTAs of one
+// output tile (one per token slice) form a cluster of S along z. After every
+// CTA's main loop, CTA z sends row block d (kBM / S rows of its fp32
+// accumulator) into slot z of CTA d's shared memory; CTA d then sums its rows
+// over the slots in slice order and writes scale * sum (+ GW when
+// accumulating) to GW. The stage buffers, idle after the main loop, hold the
+// slots. Every thread of every CTA passes both cluster barriers, also after a
+// timeout, so no CTA of the cluster waits on one that left.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t d;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(saddr), "r"(rank));
+    return d;
+}
+
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
+                 "f"(c), "f"(d)
+                 : "memory");
+}
+
+constexpr int kRowPad = kBN + 4;  // floats per slot row (16-byte pad: conflict-free stores)
+static_assert(128 * kRowPad * 4 <= kStages * kStageBytes, "slots fit in the stage buffers");
+
+__device__ void cluster_reduce(unsigned char* smem, uint32_t tmem, bool ok, int64_t m0,
+                               int64_t n0, int64_t d_in, int64_t d_out, float* __restrict__ gW,
+                               float scale, bool accumulate) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = static_cast<int>(gridDim.z);
+    const int R = 128 / S;  // rows summed by each CTA of the cluster
+    const uint32_t me = cluster_rank();
+    float* slots = reinterpret_cast<float*>(smem);  // [S][R][kRowPad]
+    cluster_sync_all();  // every CTA's main loop is over: its stage buffers are free
+    if (warp >= 2 && ok) {
+        const int q = warp & 3;
+        const int row = 32 * q + lane;
+        const uint32_t dst = static_cast<uint32_t>(row / R);
+        const uint32_t local = tc::smem_u32(slots + (static_cast<int>(me) * R + row % R) * kRowPad);
+        const uint32_t remote = map_to_rank(local, dst);
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+            float v[32];
+            tc::tmem_ld_32x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + c * 32, v);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                st_cluster_v4(remote + 4u * (c * 32 + 4 * u), v[4 * u], v[4 * u + 1],
+                              v[4 * u + 2], v[4 * u + 3]);
+        }
+    }
+    cluster_sync_all();  // every slot row has landed
+    const int n4 = kBN / 4;
+    for (int e = threadIdx.x; e < R * n4; e += blockDim.x) {
+        const int rr = e / n4, c4 = e - rr * n4;
+        const int64_t row = m0 + static_cast<int64_t>(me) * R + rr;
+        const int64_t col = n0 + 4 * c4;
+        if (row >= d_out || col >= d_in) continue;
+        const float4* src = reinterpret_cast<const float4*>(slots + rr * kRowPad) + c4;
+        float4 v = src[0];
+        for (int z = 1; z < S; ++z) {
+            const float4 w = src[z * R * (kRowPad / 4)];
+            v.x += w.x;
+            v.y += w.y;
+            v.z += w.z;
+            v.w += w.w;
+        }
+        float4 o = make_float4(scale * v.x, scale * v.y, scale * v.z, scale * v.w);
+        float4* p = reinterpret_cast<float4*>(gW + row * d_in + col);  // d_in % 8 == 0
+        if (accumulate) {
+            const float4 a = *p;
+            o = make_float4(a.x + o.x, a.y + o.y, a.z + o.z, a.w + o.w);
+        }
+        *p = o;
+    }
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -160,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool ok = tc::mbar_wait(&ctl->done, 0);
         tc::tc_fence_after();
         if (!ok) *abort_flag = 1;
-        if (ok && !*abort_flag && n_k > 0) {
+        if (ok && !*abort_flag && n_k > 0 && mode < 3) {
             const int q = warp & 3;  // TMEM lane quarter this warp may access
 #pragma unroll 1
             for (int mt = 0; mt < kMT; ++mt) {
@@ -214,6 +303,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int it = ctl->consumed; it < ctl->issued; ++it)
             tc::mbar_wait(&ctl->full[it % kStages], (it / kStages) & 1);
         atomicExch(status, 5u /* DUST_ERR_TIMEOUT */);
+    }
+    if (mode >= 3) {
+        __syncthreads();
+        cluster_reduce(smem, tmem, !*abort_flag && n_k > 0, m0, n0, d_in, d_out, out, scale,
+                       mode == 4);
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -301,12 +395,36 @@ cudaError_t launch_tc_gemm(const void* g, const void* X, int64_t T, int64_t d_in
     dim3 grid(static_cast<unsigned>((d_in + kBN - 1) / kBN),
               static_cast<unsigned>((d_out + kBM - 1) / kBM), static_cast<unsigned>(S_used));
     cudaError_t e;
+    const int stall = take_stall_injection() ? 1 : 0;
+    if (kClusterReduce && kMT == 1 && (S_used == 2 || S_used == 4 || S_used == 8)) {
+        // The slices of a tile reduce through distributed shared memory.
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = static_cast<unsigned>(S_used);
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = DUST_PDL ? 1 : 0;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        {
+            ProfScope ps(kStageGemmTc, s);
+            e = cudaLaunchKernelEx(&cfg, k_gemm_tc, ta, tb, d_in, d_out, T, slice, gW, scale,
+                                   accumulate ? 4 : 3, st, stall);
+        }
+        if (e == cudaSuccess) return e;
+        (void)cudaGetLastError();  // clusters refused: fall back to partials + reduction
+    }
     const int mode = (S_used > 1) ? 0 : (accumulate ? 2 : 1);
     {
         ProfScope ps(kStageGemmTc, s);
         e = launch_pdl(k_gemm_tc, grid, dim3(kThreads), kSmemBytes, s, ta, tb, d_in, d_out, T,
-                       slice, S_used > 1 ? partials : gW, scale, mode, st,
-                       take_stall_injection() ? 1 : 0);
+                       slice, S_used > 1 ? partials : gW, scale, mode, st, stall);
     }
     if (e != cudaSuccess || S_used == 1) return e;
     return launch_reduce(partials, S_used, d_out * d_in, scale, accumulate, gW, s);
