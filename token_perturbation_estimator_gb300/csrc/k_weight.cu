@@ -22,13 +22,19 @@ namespace {
 #ifndef DUST_WEIGHT_CPT
 #define DUST_WEIGHT_CPT 16
 #endif
-#ifndef DUST_WEIGHT_MINB
-#define DUST_WEIGHT_MINB 6       // resident CTAs per SM the register allocation must allow
+// Resident CTAs per SM that the register allocation must allow, per noise
+// kind (Gaussian: 40 registers; Rademacher: 64).
+#ifndef DUST_WEIGHT_MINB_G
+#define DUST_WEIGHT_MINB_G 6
+#endif
+#ifndef DUST_WEIGHT_MINB_R
+#define DUST_WEIGHT_MINB_R 4
 #endif
 #ifndef DUST_WEIGHT_UNROLL
 #define DUST_WEIGHT_UNROLL 2
 #endif
-constexpr int kMinBlocks = DUST_WEIGHT_MINB;
+constexpr int kMinBlocksG = DUST_WEIGHT_MINB_G;
+constexpr int kMinBlocksR = DUST_WEIGHT_MINB_R;
 constexpr int kUnrollW = DUST_WEIGHT_UNROLL;
 constexpr int kTok = 8;                 // tokens per CTA (one per warp)
 constexpr int kCpt = DUST_WEIGHT_CPT;   // channels per lane (8 or 16)
@@ -72,7 +78,7 @@ __device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16* g, int64_t 
 }
 
 template <int KIND, bool FIX, typename OutT>
-__global__ void __launch_bounds__(256, kMinBlocks) k_weight(const float* __restrict__ r,
+__global__ void __launch_bounds__(256, KIND == 1 ? kMinBlocksG : kMinBlocksR) k_weight(const float* __restrict__ r,
                                                 const float* __restrict__ P,
                                                 const float* __restrict__ carry, int64_t K,
                                                 int64_t T, int64_t d_out, uint32_t skey,
