@@ -253,12 +253,18 @@ int32_t dust_estimate_gW_path(int64_t T, int64_t d_in, int64_t d_out, int64_t K,
 
 /*
  * dust_estimate_gW_host — the same computation from HOST buffers: copies
- * X_host -> X_dev, delta_host -> delta_dev and seq_offsets_host -> seq_dev on
- * `stream`, runs dust_estimate_gW, and copies gW_dev -> gW_host. With
- * DUST_ACCUMULATE, gW_host is first copied to gW_dev. Host buffers should be
- * page-locked (else the copies are synchronous) and must stay valid until
- * the stream has completed; the caller synchronises before reading gW_host.
- * Device staging buffers are caller-owned with the sizes of the host ones.
+ * X_host -> X_dev, delta_host -> delta_dev and seq_offsets_host -> seq_dev,
+ * runs dust_estimate_gW, and copies gW_dev -> gW_host. With DUST_ACCUMULATE,
+ * gW_host is first copied to gW_dev. X, the large input, is copied on an
+ * internal copy stream of the current device (created on first use, never
+ * destroyed) that starts after earlier work on `stream`; the scan and the
+ * weighting run on `stream` meanwhile, and `stream` waits for the copy
+ * before the contraction (on error paths too), so everything this call
+ * does is complete once `stream` is. Concurrent calls on one device share
+ * the copy stream. Host buffers should be page-locked (else the copies are
+ * synchronous) and must stay valid until the stream has completed; the
+ * caller synchronises before reading gW_host. Device staging buffers are
+ * caller-owned with the sizes of the host ones.
  */
 dust_status dust_estimate_gW_host(const void* X_host, void* X_dev, dust_dtype x_dtype,
                                   int64_t T, int64_t d_in, const float* delta_host,

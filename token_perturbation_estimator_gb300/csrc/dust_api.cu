@@ -1,8 +1,10 @@
 // C ABI (include/dust.h): argument validation, workspace layout and dispatch.
-// Everything is enqueued on the caller's stream; nothing here allocates
+// Everything is enqueued on the caller's stream (dust_estimate_gW_host also
+// copies X on an internal stream and joins back); nothing here allocates
 // device memory or synchronises, except dust_last_error.
 #include <cmath>
 #include <cstring>
+#include <mutex>
 
 #include "dust.h"
 #include "internal.cuh"
@@ -276,12 +278,19 @@ int32_t dust_estimate_gW_path(int64_t T, int64_t d_in, int64_t d_out, int64_t K,
     return choose_path(T, d_in, d_out, K, x_dtype, flags);
 }
 
-dust_status dust_estimate_gW(const void* X, dust_dtype x_dtype, int64_t T, int64_t d_in,
-                             const float* delta, int64_t K, int64_t d_out,
-                             const int32_t* seq_offsets, int64_t n_seq, uint64_t seed,
-                             dust_noise_kind kind, int64_t draw_begin, float sigma, float gamma,
-                             float scale, uint32_t flags, float* gW, void* workspace,
-                             size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The whole estimator on `stream`. When x_ready is given, X is still being
+// copied on another stream: the stream waits for that event just before the
+// first kernel that reads X (the contraction), so the scan and the weighting
+// overlap the copy.
+dust_status estimate(const void* X, dust_dtype x_dtype, int64_t T, int64_t d_in,
+                     const float* delta, int64_t K, int64_t d_out, const int32_t* seq_offsets,
+                     int64_t n_seq, uint64_t seed, dust_noise_kind kind, int64_t draw_begin,
+                     float sigma, float gamma, float scale, uint32_t flags, float* gW,
+                     void* workspace, size_t ws_bytes, void* stream, cudaEvent_t x_ready) {
     dust_status st = check_estimate(T, d_in, d_out, K, x_dtype, flags);
     if (st != DUST_OK) return st;
     if (kind != DUST_NOISE_RADEMACHER && kind != DUST_NOISE_GAUSSIAN) return DUST_ERR_INVALID_ARG;
@@ -320,18 +329,53 @@ dust_status dust_estimate_gW(const void* X, dust_dtype x_dtype, int64_t T, int64
     if (e != cudaSuccess) return DUST_ERR_CUDA;
     if (L.path == DUST_PATH_FUSED_TC) {
         float* fpart = reinterpret_cast<float*>(ws + L.scan);
+        if (x_ready && cudaStreamWaitEvent(s, x_ready, 0) != cudaSuccess) return DUST_ERR_CUDA;
         return cuda_status(launch_fused(b, X, K, T, d_in, d_out, seed, static_cast<int>(kind),
                                         draw_begin, coef, anti, scale, acc, gW, fpart, s));
     }
     e = launch_weight(b, true, K, T, d_out, seed, static_cast<int>(kind), draw_begin, coef, anti,
                       g, L.g_bf16, s);
     if (e != cudaSuccess) return DUST_ERR_CUDA;
+    if (x_ready && cudaStreamWaitEvent(s, x_ready, 0) != cudaSuccess) return DUST_ERR_CUDA;
     if (L.path == DUST_PATH_UNFUSED_TC && tc_gemm_supported(g, X, d_in, d_out))
         e = launch_tc_gemm(g, X, T, d_in, d_out, scale, acc, gW, part, s);
     else
         e = launch_simt_gemm(g, L.g_bf16, X, x_dtype == DUST_BF16, T, d_in, d_out, scale, acc,
                              gW, part, s);
     return cuda_status(e);
+}
+
+// A copy stream and two events per device for dust_estimate_gW_host, created
+// on first use and kept for the life of the process. The mutex covers one
+// call's whole enqueue sequence, so the events are re-recorded only after
+// every wait on them has been enqueued.
+struct CopyLane {
+    std::mutex mu;
+    bool ready = false;
+    cudaError_t err = cudaSuccess;
+    cudaStream_t copy = nullptr;
+    cudaEvent_t fork = nullptr, x_done = nullptr;
+};
+constexpr int kMaxDevices = 64;
+CopyLane g_lanes[kMaxDevices];
+
+#ifndef DUST_HOST_DIRECT_GW
+#define DUST_HOST_DIRECT_GW 1
+#endif
+
+}  // namespace
+
+extern "C" {
+
+dust_status dust_estimate_gW(const void* X, dust_dtype x_dtype, int64_t T, int64_t d_in,
+                             const float* delta, int64_t K, int64_t d_out,
+                             const int32_t* seq_offsets, int64_t n_seq, uint64_t seed,
+                             dust_noise_kind kind, int64_t draw_begin, float sigma, float gamma,
+                             float scale, uint32_t flags, float* gW, void* workspace,
+                             size_t ws_bytes, void* stream) {
+    return estimate(X, x_dtype, T, d_in, delta, K, d_out, seq_offsets, n_seq, seed, kind,
+                    draw_begin, sigma, gamma, scale, flags, gW, workspace, ws_bytes, stream,
+                    nullptr);
 }
 
 dust_status dust_estimate_gW_host(const void* X_host, void* X_dev, dust_dtype x_dtype, int64_t T,
@@ -352,23 +396,75 @@ dust_status dust_estimate_gW_host(const void* X_host, void* X_dev, dust_dtype x_
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t esz = (x_dtype == DUST_BF16) ? 2 : 4;
     const size_t gw_bytes = sizeof(float) * static_cast<size_t>(d_out * d_in);
+    const size_t x_bytes = esz * static_cast<size_t>(T * d_in);
+    // The small inputs first, on `stream`: the scan needs them at once.
     if (T > 0) {
-        if (cudaMemcpyAsync(X_dev, X_host, esz * static_cast<size_t>(T * d_in),
-                            cudaMemcpyHostToDevice, s) != cudaSuccess ||
-            cudaMemcpyAsync(delta_dev, delta_host, sizeof(float) * static_cast<size_t>(K * T),
+        if (cudaMemcpyAsync(delta_dev, delta_host, sizeof(float) * static_cast<size_t>(K * T),
                             cudaMemcpyHostToDevice, s) != cudaSuccess ||
             cudaMemcpyAsync(seq_dev, seq_offsets_host, sizeof(int32_t) * (n_seq + 1),
                             cudaMemcpyHostToDevice, s) != cudaSuccess)
             return DUST_ERR_CUDA;
     }
-    if ((flags & DUST_ACCUMULATE) && gw_bytes &&
+    // A page-locked, device-mapped gW_host is written (and, accumulating, read)
+    // by the kernels in place, over the host link, instead of through gW_dev
+    // and a copy back.
+    float* gw_target = gW_dev;
+    bool direct = false;
+#if DUST_HOST_DIRECT_GW
+    if (gw_bytes) {
+        cudaPointerAttributes pa;
+        if (cudaPointerGetAttributes(&pa, gW_host) == cudaSuccess &&
+            pa.type == cudaMemoryTypeHost && pa.devicePointer &&
+            reinterpret_cast<uintptr_t>(pa.devicePointer) % 16 == 0) {
+            gw_target = static_cast<float*>(pa.devicePointer);
+            direct = true;
+        }
+        (void)cudaGetLastError();
+    }
+#endif
+    if ((flags & DUST_ACCUMULATE) && gw_bytes && !direct &&
         cudaMemcpyAsync(gW_dev, gW_host, gw_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
         return DUST_ERR_CUDA;
-    st = dust_estimate_gW(X_dev, x_dtype, T, d_in, delta_dev, K, d_out, seq_dev, n_seq, seed,
-                          kind, draw_begin, sigma, gamma, scale, flags, gW_dev, workspace,
-                          ws_bytes, stream);
+    // X, the large input, then goes over a second copy stream while delta is
+    // scanned and weighted; `stream` waits for it before the contraction and,
+    // in every case, before this call's work on `stream` ends. The copy starts
+    // after everything enqueued on `stream` so far: earlier work that may
+    // still read X_dev, and the small copies above (host-to-device copies
+    // share an engine, so an earlier X copy would hold the scan's inputs up).
+    CopyLane* lane = nullptr;
+    std::unique_lock<std::mutex> lock;
+    if (x_bytes > 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+            return DUST_ERR_CUDA;
+        lane = &g_lanes[dev];
+        lock = std::unique_lock<std::mutex>(lane->mu);
+        if (!lane->ready) {
+            lane->err = cudaStreamCreateWithFlags(&lane->copy, cudaStreamNonBlocking);
+            if (lane->err == cudaSuccess)
+                lane->err = cudaEventCreateWithFlags(&lane->fork, cudaEventDisableTiming);
+            if (lane->err == cudaSuccess)
+                lane->err = cudaEventCreateWithFlags(&lane->x_done, cudaEventDisableTiming);
+
+            lane->ready = true;
+        }
+        if (lane->err != cudaSuccess) return DUST_ERR_CUDA;
+        if (cudaEventRecord(lane->fork, s) != cudaSuccess ||
+            cudaStreamWaitEvent(lane->copy, lane->fork, 0) != cudaSuccess ||
+            cudaMemcpyAsync(X_dev, X_host, x_bytes, cudaMemcpyHostToDevice, lane->copy) !=
+                cudaSuccess ||
+            cudaEventRecord(lane->x_done, lane->copy) != cudaSuccess)
+            return DUST_ERR_CUDA;
+    }
+    auto join = [&]() {
+        return !lane || cudaStreamWaitEvent(s, lane->x_done, 0) == cudaSuccess;
+    };
+    st = estimate(X_dev, x_dtype, T, d_in, delta_dev, K, d_out, seq_dev, n_seq, seed, kind,
+                  draw_begin, sigma, gamma, scale, flags, gw_target, workspace, ws_bytes, stream,
+                  lane ? lane->x_done : nullptr);
+    if (!join()) return DUST_ERR_CUDA;
     if (st != DUST_OK) return st;
-    if (gw_bytes &&
+    if (gw_bytes && !direct &&
         cudaMemcpyAsync(gW_host, gW_dev, gw_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return DUST_ERR_CUDA;
     return DUST_OK;
