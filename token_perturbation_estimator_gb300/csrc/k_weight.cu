@@ -106,11 +106,21 @@ __global__ void __launch_bounds__(256, KIND == 1 ? kMinBlocksG : kMinBlocksR) k_
 #pragma unroll
     for (int j = 0; j < kCpt; ++j) acc[j] = 0.0f;
 
-    for (int64_t g0 = 0; g0 < K; g0 += kGroup) {
-        const int gn = static_cast<int>(K - g0 < kGroup ? K - g0 : kGroup);
+    // With antithetic pairs, draws 2b and 2b + 1 carry +a and -a of base draw
+    // b, so each base draw's noise is evaluated once, weighted by the
+    // difference of the pair's rewards: the loop runs over Kb = K / 2 base
+    // draws (draw_begin is even).
+    auto reward = [&](int64_t tt, int64_t i) {
+        float v = r[tt * K + i];
+        if (FIX) v = fmaf(P[tt], carry[(tt / kScanChunk) * K + i], v);
+        return v;
+    };
+    const int64_t Kb = anti ? K / 2 : K;
+    const int64_t b_begin = anti ? draw_begin / 2 : draw_begin;
+    for (int64_t g0 = 0; g0 < Kb; g0 += kGroup) {
+        const int gn = static_cast<int>(Kb - g0 < kGroup ? Kb - g0 : kGroup);
         if (tid < gn) {
-            const int64_t i = draw_begin + g0 + tid;
-            const int64_t bi = base_draw(i, anti);
+            const int64_t bi = b_begin + g0 + tid;
             s_key[tid] = make_uint2(fold16(draw_key(skey, bi, 0)),
                                     KIND == 1 ? fold16(draw_key(skey, bi, 1)) : 0u);
         }
@@ -119,10 +129,12 @@ __global__ void __launch_bounds__(256, KIND == 1 ? kMinBlocksG : kMinBlocksR) k_
             const int64_t tt = tb + tok;
             float v = 0.0f;
             if (tt < T) {
-                v = r[tt * K + g0 + k];
-                if (FIX) v = fmaf(P[tt], carry[(tt / kScanChunk) * K + g0 + k], v);
-                v *= coef;
-                if (anti && ((draw_begin + g0 + k) & 1)) v = -v;
+                if (anti) {
+                    const int64_t i = 2 * (g0 + k);
+                    v = (reward(tt, i) - reward(tt, i + 1)) * coef;
+                } else {
+                    v = reward(tt, g0 + k) * coef;
+                }
             }
             s_r[tok][k] = v;
         }
