@@ -7,9 +7,9 @@
 //
 // Mapping: one warp per token, kCpt channels per lane (kCpt/2 Box-Muller pairs
 // or kCpt signs), 8 tokens x 32 kCpt channels per CTA. The per-draw keys and the
-// per-token rewards (already multiplied by -1/(K sigma) and, for antithetic
-// draws, by the pair sign) are staged in shared memory 64 draws at a time and
-// read as warp-wide broadcasts. The per-channel counters are pre-folded once
+// per-token rewards (already multiplied by -1/(K sigma); for antithetic pairs,
+// the pair's reward difference, one per base draw) are staged in shared
+// memory 64 draws at a time and read as warp-wide broadcasts. The per-channel counters are pre-folded once
 // per thread, so each element-draw costs the hash tail plus one FMA
 // (Rademacher: the sign bit is xor-ed into the reward's sign bit).
 #include "internal.cuh"
@@ -77,13 +77,11 @@ __device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16* g, int64_t 
     }
 }
 
-template <int KIND, bool FIX, typename OutT>
-__global__ void __launch_bounds__(256, KIND == 1 ? kMinBlocksG : kMinBlocksR) k_weight(const float* __restrict__ r,
-                                                const float* __restrict__ P,
-                                                const float* __restrict__ carry, int64_t K,
-                                                int64_t T, int64_t d_out, uint32_t skey,
-                                                int64_t draw_begin, float coef, bool anti,
-                                                OutT* __restrict__ g, bool vec_ok) {
+template <int KIND, bool FIX, bool ANTI, typename OutT>
+__global__ void __launch_bounds__(256, KIND == 1 ? kMinBlocksG : kMinBlocksR)
+    k_weight(const float* __restrict__ r, const float* __restrict__ P,
+             const float* __restrict__ carry, int64_t K, int64_t T, int64_t d_out, uint32_t skey,
+             int64_t draw_begin, float coef, OutT* __restrict__ g, bool vec_ok) {
     __shared__ uint2 s_key[kGroup];  // folded keys of streams 0 and 1
     __shared__ float s_r[kTok][kGroup];
     pdl_wait();
@@ -115,8 +113,8 @@ __global__ void __launch_bounds__(256, KIND == 1 ? kMinBlocksG : kMinBlocksR) k_
         if (FIX) v = fmaf(P[tt], carry[(tt / kScanChunk) * K + i], v);
         return v;
     };
-    const int64_t Kb = anti ? K / 2 : K;
-    const int64_t b_begin = anti ? draw_begin / 2 : draw_begin;
+    const int64_t Kb = ANTI ? K / 2 : K;
+    const int64_t b_begin = ANTI ? draw_begin / 2 : draw_begin;
     for (int64_t g0 = 0; g0 < Kb; g0 += kGroup) {
         const int gn = static_cast<int>(Kb - g0 < kGroup ? Kb - g0 : kGroup);
         if (tid < gn) {
@@ -129,7 +127,7 @@ __global__ void __launch_bounds__(256, KIND == 1 ? kMinBlocksG : kMinBlocksR) k_
             const int64_t tt = tb + tok;
             float v = 0.0f;
             if (tt < T) {
-                if (anti) {
+                if (ANTI) {
                     const int64_t i = 2 * (g0 + k);
                     v = (reward(tt, i) - reward(tt, i + 1)) * coef;
                 } else {
@@ -187,12 +185,17 @@ cudaError_t launch_kind(const ScanBuffers& b, int64_t K, int64_t T, int64_t d_ou
               static_cast<unsigned>((d_out + kCh - 1) / kCh));
     const bool vec_ok = (d_out % 8 == 0) && (reinterpret_cast<uintptr_t>(g) % 16 == 0);
     ProfScope ps(kStageWeight, s);
+    auto go = [&](auto kernel, auto* out) {
+        return launch_pdl(kernel, grid, dim3(256), 0, s, b.r, b.P, b.carry, K, T, d_out, skey,
+                          draw_begin, coef, out, vec_ok);
+    };
+    auto* gb = static_cast<__nv_bfloat16*>(g);
+    auto* gf = static_cast<float*>(g);
     if (g_bf16)
-        return launch_pdl(k_weight<KIND, FIX, __nv_bfloat16>, grid, dim3(256), 0, s, b.r, b.P,
-                          b.carry, K, T, d_out, skey, draw_begin, coef, anti,
-                          static_cast<__nv_bfloat16*>(g), vec_ok);
-    return launch_pdl(k_weight<KIND, FIX, float>, grid, dim3(256), 0, s, b.r, b.P, b.carry, K, T,
-                      d_out, skey, draw_begin, coef, anti, static_cast<float*>(g), vec_ok);
+        return anti ? go(k_weight<KIND, FIX, true, __nv_bfloat16>, gb)
+                    : go(k_weight<KIND, FIX, false, __nv_bfloat16>, gb);
+    return anti ? go(k_weight<KIND, FIX, true, float>, gf)
+                : go(k_weight<KIND, FIX, false, float>, gf);
 }
 
 }  // namespace
