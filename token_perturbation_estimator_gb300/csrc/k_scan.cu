@@ -7,8 +7,7 @@
 // so it is scanned in three levels:
 //   lane   : 8 consecutive tokens, serial;
 //   warp   : 32 lanes (a 256-token chunk) by a shuffle scan of the lane maps;
-//   chunks : one warp per draw scans the chunk maps from the end (in the last
-//            CTA to finish, or in k_carry when the summaries are too many).
+//   chunks : one thread per draw walks the chunk maps from the end (k_carry).
 // A chunk's tokens then take r_true[t] = r_local[t] + P[t] * carry[chunk],
 // with P[t] the product of m from t to the chunk's last token.
 #include "internal.cuh"
@@ -35,49 +34,6 @@ __device__ float decay_of(int64_t t, int64_t T, const int32_t* __restrict__ so, 
         if (v < key) lo = mid + 1; else hi = mid - 1;
     }
     return gamma;
-}
-
-// carry[j-1][i] = A[j][i] + B[j] * carry[j][i] for j = nc-1 .. 1, carry[nc-1]
-// = 0: for each draw, a reverse scan of the chunk maps x -> A[j] + B[j] x. One
-// warp per draw: each lane composes a block of consecutive chunks, a warp
-// suffix scan hands every lane the value entering its block from above, and
-// the lane walks its block again to write the carries. sA, sB may be shared
-// or global memory.
-__device__ void carry_pass(const float* sA, const float* sB, int64_t nc, int64_t K,
-                           float* __restrict__ carry) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nwarps = blockDim.x >> 5;
-    const int64_t n = nc - 1;                 // maps j = 1 .. nc-1
-    const int64_t per = (n + 31) / 32;        // chunks per lane
-    const int64_t j_hi = nc - 1 - lane * per; // this lane's block: j_hi down to j_lo
-    const int64_t j_lo = j_hi - per + 1 > 1 ? j_hi - per + 1 : 1;
-    for (int64_t i = warp; i < K; i += nwarps) {
-        float a = 0.0f, b = 1.0f;  // the block's composed map
-        for (int64_t j = j_lo; j <= j_hi; ++j) {
-            a = fmaf(b, sA[j * K + i], a);
-            b *= sB[j];
-        }
-        // suffix over the lanes before this one (they hold the higher chunks)
-        float as = a, bs = b;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float oa = __shfl_up_sync(0xffffffffu, as, off);
-            const float ob = __shfl_up_sync(0xffffffffu, bs, off);
-            if (lane >= off) {
-                as = fmaf(bs, oa, as);
-                bs *= ob;
-            }
-        }
-        float x = __shfl_up_sync(0xffffffffu, as, 1);
-        if (lane == 0) {
-            x = 0.0f;
-            carry[(nc - 1) * K + i] = 0.0f;
-        }
-        for (int64_t j = j_hi; j >= j_lo; --j) {
-            x = fmaf(sB[j], x, sA[j * K + i]);
-            carry[(j - 1) * K + i] = x;
-        }
-    }
 }
 
 __global__ void __launch_bounds__(256) k_scan_local(const float* __restrict__ delta, int64_t K,
@@ -224,12 +180,19 @@ __global__ void __launch_bounds__(256) k_scan_local(const float* __restrict__ de
     for (int64_t e = tid; e < nc * K; e += blockDim.x) sA[e] = __ldcg(A + e);
     for (int64_t e = tid; e < nc; e += blockDim.x) sB[e] = __ldcg(B + e);
     __syncthreads();
-    carry_pass(sA, sB, nc, K, carry);
+    for (int64_t i = tid; i < K; i += blockDim.x) {
+        float c = 0.0f;
+        carry[(nc - 1) * K + i] = 0.0f;
+        for (int64_t j = nc - 1; j >= 1; --j) {
+            c = fmaf(sB[j], c, sA[j * K + i]);
+            carry[(j - 1) * K + i] = c;
+        }
+    }
 }
 
 // carry[j][i] = A[j+1][i] + B[j+1] * carry[j+1][i], carry[last] = 0.
 // The summaries are first staged in shared memory by all threads (when they
-// fit), then carry_pass scans them.
+// fit), so the serial chain of each draw runs at shared-memory latency.
 __global__ void __launch_bounds__(256) k_carry(const float* __restrict__ A,
                                                const float* __restrict__ B, int64_t K,
                                                int64_t n_chunks, float* __restrict__ carry,
@@ -248,7 +211,14 @@ __global__ void __launch_bounds__(256) k_carry(const float* __restrict__ A,
         sA = dA;
         sB = dB;
     }
-    carry_pass(sA, sB, n_chunks, K, carry);
+    for (int64_t i = threadIdx.x; i < K; i += blockDim.x) {
+        float c = 0.0f;
+        carry[(n_chunks - 1) * K + i] = 0.0f;
+        for (int64_t j = n_chunks - 1; j >= 1; --j) {
+            c = fmaf(sB[j], c, sA[j * K + i]);
+            carry[(j - 1) * K + i] = c;
+        }
+    }
 }
 
 __global__ void __launch_bounds__(256) k_fixup(float* __restrict__ r, const float* __restrict__ P,
