@@ -203,7 +203,7 @@ def make_inputs_fast(w, dev, site):
 
 # ---------------------------------------------------------- roofline -----
 
-def roofline_for(stage, ms_per_step, sites, peaks):
+def roofline_for(stage, ms_per_step, sites, peaks, antithetic=False):
     """Roofline of the dominant kernel family, from its CUDA-event time per
     step and the algorithmic work of one step (summed over the step's sites):
       weight / fused (Gaussian): 2 transcendental (XU) ops per element-draw
@@ -214,10 +214,14 @@ def roofline_for(stage, ms_per_step, sites, peaks):
         the reward; its two multiplies issue on the FMA pipe) -> bound "alu"
         against the ALU pipe: 64 ops/clk/SM x 152 SMs x 2.07 GHz;
       gemm_tc: 2 T d_in d_out FLOP -> bound "tensor" (measured bf16 peak);
-      gemm_simt: same FLOP on FFMA -> "alu", 256 FLOP/clk/SM x 152 x 2.07 GHz."""
+      gemm_simt: same FLOP on FFMA -> "alu", 256 FLOP/clk/SM x 152 x 2.07 GHz.
+    With antithetic pairs the weighting kernel evaluates each base draw's
+    noise once (K / 2 noise draws per token); the fused kernel still K."""
     sm, clk = 152, 2.07e9
     s = ms_per_step / 1000.0
     el = float(sum(w.element_draws for w in sites))
+    if antithetic and stage == "weight":
+        el /= 2.0
     fl = float(sum(w.gemm_flops for w in sites))
     if stage in ("weight", "fused"):
         if sites[0].kind == 1:
@@ -472,7 +476,8 @@ def run_gb300(args):
     launches_per_step = sum(v["launches"] for v in prof.values()) / args.steps
     top = max(prof.items(), key=lambda kv: kv[1]["total_ms"])
     peaks = load_peaks()
-    roof = roofline_for(top[0], top[1]["total_ms"] / args.steps, sites, peaks)
+    anti = bool(flags & dust.ANTITHETIC)
+    roof = roofline_for(top[0], top[1]["total_ms"] / args.steps, sites, peaks, anti)
     roof["launches_per_step"] = top[1]["launches"] / args.steps
     roof["traffic"] = traffic_from_profiles(top[0]) if len(sites) == 1 else None
     tot_ms = sum(x["total_ms"] for x in prof.values())
