@@ -19,11 +19,13 @@ SHAPES = [
     (128, 8, 8),           # smallest tensor-core shape
     (16384, 512, 512),
     (77, 520, 264),
-    # token-slice counts of the tensor-core kernel: 2, 4 and 8 reduce inside a
-    # thread-block cluster, 3 through fp32 partials and a reduction kernel
+    # token-slice counts of the tensor-core kernel: up to 8 reduce inside a
+    # thread-block cluster (uneven row blocks when 128 is not a multiple),
+    # more through fp32 partials and a reduction kernel
     (8192, 512, 4096),     # 2 slices
     (4096, 512, 1152),     # 8 slices
-    (2048, 512, 3072),     # 3 slices
+    (2048, 512, 2560),     # 3 slices: row blocks of 43, 43, 42
+    (16384, 256, 256),     # 64 slices: partials
 ]
 
 

@@ -13,12 +13,17 @@ from helpers import cuda, rel_fro
 pytestmark = pytest.mark.gpu
 
 
-def test_bounded_wait_timeout_is_reported_and_context_survives():
+@pytest.mark.parametrize("T,d_in,d_out", [
+    (128, 128, 256),    # one slice: direct write
+    (2048, 128, 256),   # 8 slices reduced inside a cluster: every CTA times out together
+    (4096, 256, 128),   # 16 slices: partials and the reduction kernel
+])
+def test_bounded_wait_timeout_is_reported_and_context_survives(T, d_in, d_out):
     import torch
     dev = cuda()
     gen = torch.Generator().manual_seed(3)
-    g = torch.randn((512, 256), generator=gen).to(torch.bfloat16).to(dev)
-    X = torch.randn((512, 128), generator=gen).to(torch.bfloat16).to(dev)
+    g = torch.randn((T, d_out), generator=gen).to(torch.bfloat16).to(dev)
+    X = torch.randn((T, d_in), generator=gen).to(torch.bfloat16).to(dev)
     want = g.double().cpu().numpy().T @ X.double().cpu().numpy()
     assert dust.dust_last_error() == dust.OK
     dust.lib().dust_debug_inject_timeout(1)

@@ -67,9 +67,10 @@ struct Ctl {
 };
 
 // Cluster reduction of the token slices (modes 3 and 4). The S CTAs of one
-// output tile (one per token slice) form a cluster of S along z. After every
-// CTA's main loop, CTA z sends row block d (kBM / S rows of its fp32
-// accumulator) into slot z of CTA d's shared memory; CTA d then sums its rows
+// output tile (one per token slice, 2 <= S <= 8) form a cluster of S along z.
+// After every CTA's main loop, CTA z sends row block d (ceil(128 / S) rows of
+// its fp32 accumulator, fewer in the last block) into slot z of CTA d's
+// shared memory; CTA d then sums its rows
 // over the slots in slice order and writes scale * sum (+ GW when
 // accumulating) to GW. The stage buffers, idle after the main loop, hold the
 // slots. Every thread of every CTA passes both cluster barriers, also after a
@@ -98,15 +99,18 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, f
 }
 
 constexpr int kRowPad = kBN + 4;  // floats per slot row (16-byte pad: conflict-free stores)
-static_assert(128 * kRowPad * 4 <= kStages * kStageBytes, "slots fit in the stage buffers");
+constexpr int kMaxClusterSlices = 8;  // portable cluster size
+// S slots of ceil(128 / S) rows each; the most rows over S = 2..8 is 133 (S = 7).
+static_assert(133 * kRowPad * 4 <= kStages * kStageBytes, "slots fit in the stage buffers");
 
 __device__ void cluster_reduce(unsigned char* smem, uint32_t tmem, bool ok, int64_t m0,
                                int64_t n0, int64_t d_in, int64_t d_out, float* __restrict__ gW,
                                float scale, bool accumulate) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = static_cast<int>(gridDim.z);
-    const int R = 128 / S;  // rows summed by each CTA of the cluster
+    const int R = (128 + S - 1) / S;  // rows summed by each CTA (the last may have fewer)
     const uint32_t me = cluster_rank();
+    const int R_me = (128 - static_cast<int>(me) * R < R) ? 128 - static_cast<int>(me) * R : R;
     float* slots = reinterpret_cast<float*>(smem);  // [S][R][kRowPad]
     cluster_sync_all();  // every CTA's main loop is over: its stage buffers are free
     if (warp >= 2 && ok) {
@@ -127,7 +131,7 @@ __device__ void cluster_reduce(unsigned char* smem, uint32_t tmem, bool ok, int6
     }
     cluster_sync_all();  // every slot row has landed
     const int n4 = kBN / 4;
-    for (int e = threadIdx.x; e < R * n4; e += blockDim.x) {
+    for (int e = threadIdx.x; e < R_me * n4; e += blockDim.x) {
         const int rr = e / n4, c4 = e - rr * n4;
         const int64_t row = m0 + static_cast<int64_t>(me) * R + rr;
         const int64_t col = n0 + 4 * c4;
@@ -331,6 +335,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+// Token slices per output tile: enough CTAs to give every SM one tile slice
+// (S = 152 / tiles), each slice at least 4 k-steps. More slices than that
+// measured slower even where they would fill the GPU better (qkv 1024 x 3072,
+// 96 tiles: 3 slices in 2 waves 131 us against 102 us for 1 slice): the
+// CTAs then share one tile feed.
 int64_t tc_slices(int64_t T, int64_t d_in, int64_t d_out) {
     const int64_t tiles = ((d_out + kBM - 1) / kBM) * ((d_in + kBN - 1) / kBN);
     int64_t S = 152 / tiles;
@@ -373,6 +382,41 @@ int64_t tc_gemm_tiles(int64_t d_in, int64_t d_out) {
     return ((d_out + kBM - 1) / kBM) * ((d_in + kBN - 1) / kBN);
 }
 
+namespace {
+
+// True when all `tiles` clusters of S CTAs can be resident at once. Clusters
+// must fit inside one GPC, so a cluster size that does not divide the GPCs'
+// SM counts leaves SMs unused and can push a few clusters into a second
+// wave; the fp32 partials then win (measured on the 48-site sweep: 6-CTA
+// clusters 5.1 ms of contraction against 4.3 ms with partials).
+bool cluster_fits(int S, int64_t tiles) {
+    static int max_active[kMaxClusterSlices + 1] = {};
+    static std::once_flag once[kMaxClusterSlices + 1];
+    std::call_once(once[S], [S] {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1, 1, static_cast<unsigned>(S));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = static_cast<unsigned>(S);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes) != cudaSuccess ||
+            cudaOccupancyMaxActiveClusters(&n, k_gemm_tc, &cfg) != cudaSuccess)
+            n = 0;
+        (void)cudaGetLastError();
+        max_active[S] = n;
+    });
+    return tiles <= max_active[S];
+}
+
+}  // namespace
+
 cudaError_t launch_tc_gemm(const void* g, const void* X, int64_t T, int64_t d_in, int64_t d_out,
                            float scale, bool accumulate, float* gW, float* partials,
                            cudaStream_t s) {
@@ -396,7 +440,8 @@ cudaError_t launch_tc_gemm(const void* g, const void* X, int64_t T, int64_t d_in
               static_cast<unsigned>((d_out + kBM - 1) / kBM), static_cast<unsigned>(S_used));
     cudaError_t e;
     const int stall = take_stall_injection() ? 1 : 0;
-    if (kClusterReduce && kMT == 1 && (S_used == 2 || S_used == 4 || S_used == 8)) {
+    if (kClusterReduce && kMT == 1 && S_used >= 2 && S_used <= kMaxClusterSlices &&
+        cluster_fits(static_cast<int>(S_used), static_cast<int64_t>(grid.x) * grid.y)) {
         // The slices of a tile reduce through distributed shared memory.
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = grid;
