@@ -235,6 +235,12 @@ dust_status dust_contract(const void* g, const void* X, dust_dtype dtype, int64_
  *               aligned; contents on entry are ignored.
  * The result is a deterministic function of the inputs (no floating-point
  * atomics): two calls with the same arguments give bit-identical gW.
+ * Graph replay: from the second call with identical arguments (every pointer
+ * and scalar) on the current device, the call's launches are captured once
+ * into a CUDA graph and later calls launch that graph on `stream`; it reads
+ * and writes the same buffers, so it sees their current contents. Up to 16
+ * argument sets are kept per device (least recently used dropped). Bypassed
+ * while dust_profile_enable(1) is on.
  */
 dust_status dust_estimate_gW_workspace(size_t* bytes, int64_t T, int64_t d_in,
                                        int64_t d_out, int64_t K, dust_dtype x_dtype,

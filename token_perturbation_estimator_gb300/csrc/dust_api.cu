@@ -363,6 +363,47 @@ CopyLane g_lanes[kMaxDevices];
 #define DUST_HOST_DIRECT_GW 1
 #endif
 
+// Every argument of an estimator call, zero-padded: the key of its graph.
+struct CallArgs {
+    int32_t entry;  // 0: dust_estimate_gW, 1: dust_estimate_gW_host
+    int32_t x_dtype, kind;
+    uint32_t flags;
+    int64_t T, d_in, K, d_out, n_seq, draw_begin;
+    uint64_t seed;
+    float sigma, gamma, scale, pad;
+    const void *X, *X_host;
+    const float *delta, *delta_host;
+    const int32_t *seq, *seq_host;
+    float *gW, *gW_host;
+    void* workspace;
+    size_t ws_bytes;
+};
+
+dust_status estimate_host(const void* X_host, void* X_dev, dust_dtype x_dtype, int64_t T,
+                          int64_t d_in, const float* delta_host, float* delta_dev, int64_t K,
+                          int64_t d_out, const int32_t* seq_offsets_host, int32_t* seq_dev,
+                          int64_t n_seq, uint64_t seed, dust_noise_kind kind,
+                          int64_t draw_begin, float sigma, float gamma, float scale,
+                          uint32_t flags, float* gW_host, float* gW_dev, void* workspace,
+                          size_t ws_bytes, void* stream);
+
+dust_status enqueue_device(const void* ctx, cudaStream_t s) {
+    const CallArgs& a = *static_cast<const CallArgs*>(ctx);
+    return estimate(a.X, static_cast<dust_dtype>(a.x_dtype), a.T, a.d_in, a.delta, a.K,
+                    a.d_out, a.seq, a.n_seq, a.seed, static_cast<dust_noise_kind>(a.kind),
+                    a.draw_begin, a.sigma, a.gamma, a.scale, a.flags, a.gW, a.workspace,
+                    a.ws_bytes, s, nullptr);
+}
+
+dust_status enqueue_host(const void* ctx, cudaStream_t s) {
+    const CallArgs& a = *static_cast<const CallArgs*>(ctx);
+    return estimate_host(a.X_host, const_cast<void*>(a.X), static_cast<dust_dtype>(a.x_dtype),
+                         a.T, a.d_in, a.delta_host, const_cast<float*>(a.delta), a.K, a.d_out,
+                         a.seq_host, const_cast<int32_t*>(a.seq), a.n_seq, a.seed,
+                         static_cast<dust_noise_kind>(a.kind), a.draw_begin, a.sigma, a.gamma,
+                         a.scale, a.flags, a.gW_host, a.gW, a.workspace, a.ws_bytes, s);
+}
+
 }  // namespace
 
 extern "C" {
@@ -373,9 +414,29 @@ dust_status dust_estimate_gW(const void* X, dust_dtype x_dtype, int64_t T, int64
                              dust_noise_kind kind, int64_t draw_begin, float sigma, float gamma,
                              float scale, uint32_t flags, float* gW, void* workspace,
                              size_t ws_bytes, void* stream) {
-    return estimate(X, x_dtype, T, d_in, delta, K, d_out, seq_offsets, n_seq, seed, kind,
-                    draw_begin, sigma, gamma, scale, flags, gW, workspace, ws_bytes, stream,
-                    nullptr);
+    CallArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.entry = 0;
+    a.x_dtype = x_dtype;
+    a.kind = kind;
+    a.flags = flags;
+    a.T = T;
+    a.d_in = d_in;
+    a.K = K;
+    a.d_out = d_out;
+    a.n_seq = n_seq;
+    a.draw_begin = draw_begin;
+    a.seed = seed;
+    a.sigma = sigma;
+    a.gamma = gamma;
+    a.scale = scale;
+    a.X = X;
+    a.delta = delta;
+    a.seq = seq_offsets;
+    a.gW = gW;
+    a.workspace = workspace;
+    a.ws_bytes = ws_bytes;
+    return graph_call(&a, sizeof(a), static_cast<cudaStream_t>(stream), enqueue_device, &a);
 }
 
 dust_status dust_estimate_gW_host(const void* X_host, void* X_dev, dust_dtype x_dtype, int64_t T,
@@ -386,6 +447,49 @@ dust_status dust_estimate_gW_host(const void* X_host, void* X_dev, dust_dtype x_
                                   float gamma, float scale, uint32_t flags, float* gW_host,
                                   float* gW_dev, void* workspace, size_t ws_bytes,
                                   void* stream) {
+    CallArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.entry = 1;
+    a.x_dtype = x_dtype;
+    a.kind = kind;
+    a.flags = flags;
+    a.T = T;
+    a.d_in = d_in;
+    a.K = K;
+    a.d_out = d_out;
+    a.n_seq = n_seq;
+    a.draw_begin = draw_begin;
+    a.seed = seed;
+    a.sigma = sigma;
+    a.gamma = gamma;
+    a.scale = scale;
+    a.X = X_dev;
+    a.X_host = X_host;
+    a.delta = delta_dev;
+    a.delta_host = delta_host;
+    a.seq = seq_dev;
+    a.seq_host = seq_offsets_host;
+    a.gW = gW_dev;
+    a.gW_host = gW_host;
+    a.workspace = workspace;
+    a.ws_bytes = ws_bytes;
+    // Direct launches: replayed as a graph this path measured 6 us slower per
+    // call (229 against 223 us on the 512 x 2048 layer), the copy branch and
+    // the kernels overlapping less well than when issued one by one.
+    return enqueue_host(&a, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
+
+namespace {
+
+dust_status estimate_host(const void* X_host, void* X_dev, dust_dtype x_dtype, int64_t T,
+                          int64_t d_in, const float* delta_host, float* delta_dev, int64_t K,
+                          int64_t d_out, const int32_t* seq_offsets_host, int32_t* seq_dev,
+                          int64_t n_seq, uint64_t seed, dust_noise_kind kind,
+                          int64_t draw_begin, float sigma, float gamma, float scale,
+                          uint32_t flags, float* gW_host, float* gW_dev, void* workspace,
+                          size_t ws_bytes, void* stream) {
     dust_status st = check_estimate(T, d_in, d_out, K, x_dtype, flags);
     if (st != DUST_OK) return st;
     if (n_seq < 0 || (T > 0 && n_seq < 1)) return DUST_ERR_INVALID_ARG;
@@ -469,6 +573,10 @@ dust_status dust_estimate_gW_host(const void* X_host, void* X_dev, dust_dtype x_
         return DUST_ERR_CUDA;
     return DUST_OK;
 }
+
+}  // namespace
+
+extern "C" {
 
 dust_status dust_last_error(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)

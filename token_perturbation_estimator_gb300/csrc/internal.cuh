@@ -5,6 +5,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include "dust.h"
+
 namespace dust {
 
 // Device address of the status word that kernels with bounded waits set when
@@ -33,6 +35,19 @@ struct ProfScope {
 // Test hook: true once after dust_debug_inject_timeout(1); the next
 // tensor-core contraction then makes its bounded wait run out.
 bool take_stall_injection();
+bool stall_injection_pending();
+// True while dust_profile_enable(1) is in effect.
+bool profiling_on();
+
+// Runs `enqueue` on `stream`, or replays it as a CUDA graph: the second call
+// with byte-identical `key` (every argument of the call, pointers included)
+// captures what `enqueue` issues into a graph on an internal stream, and
+// later calls with that key launch the graph on `stream`. Graphs read and
+// write the same addresses, so they see the current contents of every
+// buffer. Bypassed while profiling or a test stall is pending; a call that
+// cannot be captured falls back to direct launches for that key.
+dust_status graph_call(const void* key, size_t key_len, cudaStream_t stream,
+                       dust_status (*enqueue)(const void* ctx, cudaStream_t s), const void* ctx);
 
 // ---- Programmatic dependent launch. The estimator's kernels are launched so
 // that the next kernel on the stream may be scheduled while the previous one
@@ -77,21 +92,6 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // Token chunk of the credit scan (one CTA, 32 lanes x 8 tokens).
 constexpr int kScanChunk = 256;
 
-// Everything one estimator call needs, resolved on the host.
-struct EstimateArgs {
-    const void* X;
-    int x_bf16;
-    int64_t T, d_in, d_out, K;
-    const float* delta;
-    const int32_t* seq_offsets;
-    int64_t n_seq;
-    uint64_t seed;
-    int kind;
-    int64_t draw_begin;
-    float sigma, gamma, scale;
-    uint32_t flags;
-    float* gW;
-};
 
 // Workspace of the credit scan. All pointers are device memory.
 struct ScanBuffers {

@@ -62,6 +62,13 @@ std::atomic<int> g_inject{0};
 
 bool take_stall_injection() { return g_inject.exchange(0) != 0; }
 
+bool stall_injection_pending() { return g_inject.load() != 0; }
+
+bool profiling_on() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    return g_on;
+}
+
 }  // namespace dust
 
 extern "C" {
