@@ -21,6 +21,7 @@ from . import build as _build
 
 RADEMACHER = 0
 GAUSSIAN = 1
+RADEMACHER_PACKED = 3  # 32 signs per hash word
 CENTER = 1
 ANTITHETIC = 2
 

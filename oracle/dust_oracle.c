@@ -40,7 +40,7 @@
 
 #define OR_EXPORT __attribute__((visibility("default")))
 
-enum { OR_RADEMACHER = 0, OR_GAUSSIAN = 1 };
+enum { OR_RADEMACHER = 0, OR_GAUSSIAN = 1, OR_RADEMACHER_PACKED = 3 };
 enum { OR_CENTER = 1, OR_ANTITHETIC = 2 };
 
 static const double OR_PI = 3.14159265358979323846264338327950288;
@@ -104,6 +104,12 @@ static double or_noise_value(int kind, uint64_t seed, int64_t i, int64_t t,
     if (kind == OR_RADEMACHER) {
         uint32_t w = or_word(seed, i, t, c, d_out, 0);
         return sign * ((w >> 31) ? -1.0 : 1.0);
+    }
+    if (kind == OR_RADEMACHER_PACKED) {
+        /* 32 signs per word: channel c takes bit c mod 32 of the word of its
+         * group's first channel 32 floor(c / 32); bit 0 gives +1. */
+        uint32_t w = or_word(seed, i, t, c & ~(int64_t)31, d_out, 0);
+        return sign * (((w >> (c & 31)) & 1u) ? -1.0 : 1.0);
     }
     int64_t p = c & ~(int64_t)1;
     uint32_t w0 = or_word(seed, i, t, p, d_out, 0);

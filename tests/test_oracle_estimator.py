@@ -86,7 +86,7 @@ def test_scan_one_token_sequences(orc):
 
 # ------------------------------------------------------- brute-force sums --
 
-@pytest.mark.parametrize("kind", [0, 1])
+@pytest.mark.parametrize("kind", [0, 1, 3])
 @pytest.mark.parametrize("flags", [0, 1, 3])
 def test_pipeline_equals_brute_force(orc, kind, flags):
     rng = np.random.default_rng(5)
@@ -130,7 +130,7 @@ def _planted(orc, rng, T, d_out, K, sigma, kind, seed, curv=0.0, flags=0, common
     return dp, delta
 
 
-@pytest.mark.parametrize("kind", [0, 1])
+@pytest.mark.parametrize("kind", [0, 1, 3])
 @pytest.mark.parametrize("center", [False, True])
 def test_unbiased_recovers_planted_error(orc, kind, center):
     """Linear loss delta = sigma <dplant, a>: E[g_t] = dplant_t without

@@ -95,3 +95,57 @@ def test_different_seeds_are_uncorrelated(orc):
     a = orc.noise(seed=100, kind=1, draw_begin=0, n_draws=1, T=1000, d_out=200).ravel()
     b = orc.noise(seed=101, kind=1, draw_begin=0, n_draws=1, T=1000, d_out=200).ravel()
     assert abs(np.mean(a * b)) <= 5.0 / np.sqrt(a.size)
+
+
+# ------------------------------------------------- packed Rademacher signs --
+# Thirty-two signs per hash word (a noise kind of this project, motivated by
+# "RandOpt Speedrun", "What was slow, and the fix": the hash is the cost, so
+# spend every bit of it): channel c takes bit c mod 32 of the stream-0 word at
+# the counter of its group's first channel 32 floor(c / 32); bit 0 gives +1.
+
+def test_packed_sign_is_bit_of_group_word(orc):
+    T, d_out = 40, 77  # three groups, the last one 13 channels wide
+    w = orc.words(seed=6, draw_begin=1, n_draws=3, T=T, d_out=d_out, stream=0)
+    a = orc.noise(seed=6, kind=orc.RADEMACHER_PACKED, draw_begin=1, n_draws=3, T=T,
+                  d_out=d_out)
+    c = np.arange(d_out)
+    word = w[..., (c // 32) * 32]
+    bit = (word >> (c % 32).astype(np.uint32)) & np.uint32(1)
+    assert np.array_equal(a, np.where(bit == 1, -1.0, 1.0))
+
+
+def test_packed_top_bit_channel_equals_per_channel_sign(orc):
+    """Channel 32q + 31 reads the top bit of the word at counter 32q, which is
+    exactly the per-channel Rademacher sign of channel 32q."""
+    a = orc.noise(seed=8, kind=orc.RADEMACHER_PACKED, draw_begin=0, n_draws=2, T=50,
+                  d_out=96)
+    r = orc.noise(seed=8, kind=orc.RADEMACHER, draw_begin=0, n_draws=2, T=50, d_out=96)
+    for q in range(3):
+        assert np.array_equal(a[..., 32 * q + 31], r[..., 32 * q])
+
+
+def test_packed_signs_balance_and_independence(orc):
+    a = orc.noise(seed=12, kind=orc.RADEMACHER_PACKED, draw_begin=0, n_draws=4, T=2048,
+                  d_out=1024)
+    assert set(np.unique(a).tolist()) == {-1.0, 1.0}
+    assert abs(a.mean()) <= 4.0 / np.sqrt(a.size)
+    # neighbouring bits of one word, the same bit of neighbouring words,
+    # neighbouring tokens and draws
+    pairs = ((a[..., 1:], a[..., :-1]), (a[..., 32:], a[..., :-32]),
+             (a[:, 1:, :], a[:, :-1, :]), (a[1:], a[:-1]))
+    for x, y in pairs:
+        assert abs(np.mean(x * y)) <= 4.0 / np.sqrt(x.size)
+    # every bit position is balanced on its own
+    for b in range(32):
+        col = a[..., b::32]
+        assert abs(col.mean()) <= 5.0 / np.sqrt(col.size)
+
+
+def test_packed_antithetic_and_draw_split(orc):
+    f = orc.ANTITHETIC
+    k = orc.RADEMACHER_PACKED
+    a = orc.noise(seed=9, kind=k, draw_begin=0, n_draws=6, T=32, d_out=70, flags=f)
+    assert np.array_equal(a[1::2], -a[0::2])
+    full = orc.noise(seed=77, kind=k, draw_begin=0, n_draws=7, T=20, d_out=40)
+    part = orc.noise(seed=77, kind=k, draw_begin=3, n_draws=3, T=20, d_out=40)
+    assert np.array_equal(full[3:6], part)
