@@ -51,7 +51,8 @@ def parse_args(argv=None):
     p.add_argument("--flags", type=int, default=None,
                    help="extra dust_estimate_gW flags (e.g. force a path)")
     p.add_argument("--workload", default="mlp_up",
-                   choices=["mlp_up", "toy", "qkv", "square_r", "square_g", "sweep"],
+                   choices=["mlp_up", "toy", "qkv", "square_r", "square_g", "square_rp",
+                            "sweep"],
                    help="mlp_up is the measured headline; the others are for study")
     return p.parse_args(argv)
 
@@ -175,6 +176,7 @@ WORKLOADS = {
     "qkv": "qkv_1024to3072_T16384_K16_gaussian_gamma0.9",
     "square_r": "square_4096_T32768_K64_rademacher",
     "square_g": "square_4096_T32768_K64_gaussian",
+    "square_rp": "square_4096_T32768_K64_rademacher_packed",
     "sweep": "sweep_12x4_sites_T65536_K32_gaussian",
 }
 
@@ -184,7 +186,7 @@ def workload_sites(name):
     if name == "sweep":
         return wl.sweep_sites()
     return [{"mlp_up": wl.MLP_UP, "toy": wl.TOY, "qkv": wl.QKV_DECAY, "square_r": wl.SQUARE_R,
-             "square_g": wl.SQUARE_G}[name]]
+             "square_g": wl.SQUARE_G, "square_rp": wl.SQUARE_RP}[name]]
 
 
 def make_inputs_fast(w, dev, site):
@@ -213,6 +215,13 @@ def roofline_for(stage, ms_per_step, sites, peaks, antithetic=False):
         key xor, fmix32's xor-shift by 13 (shift + xor) and the sign merge into
         the reward; its two multiplies issue on the FMA pipe) -> bound "alu"
         against the ALU pipe: 64 ops/clk/SM x 152 SMs x 2.07 GHz;
+      weight (packed signs): bound by instruction issue (ncu: issue slots 92 %
+        busy, ALU 65 %, FMA 56 %): per element-draw 3 issued instructions (the
+        shift that brings the channel's bit to the sign position, the masked
+        xor into the reward, the add) plus the word's ~8 (key xor, two
+        multiplies, two xor-shifts) shared by 32 channels -> 3.25 lane
+        instructions per element-draw against 4 warp instructions per clock per
+        SM: 128 lanes x 152 SMs x 2.07 GHz;
       gemm_tc: 2 T d_in d_out FLOP -> bound "tensor" (measured bf16 peak);
       gemm_simt: same FLOP on FFMA -> "alu", 256 FLOP/clk/SM x 152 x 2.07 GHz.
     With antithetic pairs the weighting kernel evaluates each base draw's
@@ -226,6 +235,8 @@ def roofline_for(stage, ms_per_step, sites, peaks, antithetic=False):
     if stage in ("weight", "fused"):
         if sites[0].kind == 1:
             ops, peak = 2.0 * el, 16 * sm * clk
+        elif sites[0].kind == 3:
+            ops, peak = 3.25 * el, 128 * sm * clk
         else:
             ops, peak = 4.0 * el, 64 * sm * clk
         ach = ops / s
@@ -528,7 +539,7 @@ def run_gb300(args):
         w0 = sites[0]
         cfg = {"workload": WORKLOADS[args.workload], "sites": len(sites),
                "token_draws_per_step": units,
-               "noise": "gaussian" if w0.kind == 1 else "rademacher",
+               "noise": {0: "rademacher", 1: "gaussian", 3: "rademacher_packed"}[w0.kind],
                "x_dtype": w0.x_dtype, "paths": sorted({b["path"] for b in bundles}),
                "parallelism": "replicas" if world > 1 else "single",
                "l2": "flushed (256 MB write) between timed steps"}

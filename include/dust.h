@@ -27,6 +27,9 @@
  *   draw_key    fmix32(seed_key ^ (2*i + s) * 0x9E3779B9)    (mod 2^32)
  *   word        fmix32(draw_key(i, s) ^ (t * d_out + c))      (mod 2^32)
  *   Rademacher  a = +1 if word(i,t,c,0) < 2^31, else -1
+ *   Packed      (DUST_NOISE_RADEMACHER_PACKED) 32 signs per word: channel c
+ *               takes bit c mod 32 of word(i, t, 32 floor(c/32), 0); bit 0
+ *               gives +1, bit 1 gives -1
  *   Gaussian    pair p = c & ~1, w0 = word(i,t,p,0), w1 = word(i,t,p,1),
  *               u1 = 1 - (w0 >> 9) 2^-23, u2 = (w1 >> 9) 2^-23,
  *               rho = sqrt(-2 ln u1); even c: rho cos(2 pi u2),
@@ -74,7 +77,8 @@ typedef enum {
 typedef enum {
     DUST_NOISE_RADEMACHER = 0,
     DUST_NOISE_GAUSSIAN = 1,
-    DUST_NOISE_RAW_WORDS = 2   /* dust_noise only: the uint32 hash words */
+    DUST_NOISE_RAW_WORDS = 2,  /* dust_noise only: the uint32 hash words */
+    DUST_NOISE_RADEMACHER_PACKED = 3  /* +-1 signs, 32 per hash word */
 } dust_noise_kind;
 
 typedef enum {
@@ -92,7 +96,8 @@ enum {
     DUST_FORCE_UNFUSED = 8u,   /* estimator: write g to the workspace, then contract */
     DUST_FORCE_FUSED = 16u,    /* estimator: produce g tiles inside the contraction
                                   (needs bf16 X, d_in <= 512, d_in % 8 == 0,
-                                  d_out % 8 == 0, K <= 64; else DUST_ERR_UNSUPPORTED) */
+                                  d_out % 8 == 0, K <= 64, not the packed noise;
+                                  else DUST_ERR_UNSUPPORTED) */
     DUST_WORD_STREAM1 = 32u,   /* dust_noise RAW_WORDS: words of stream s = 1 */
     DUST_FORCE_SIMT = 64u      /* estimator: contraction on CUDA cores (fp32 FFMA) */
 };
@@ -137,7 +142,8 @@ dust_status dust_noise(void* out, dust_dtype out_dtype, uint64_t seed,
  * Depth", section "Kernel Recipes").
  *   y      device, T rows of d_out values with row stride ld_y >= d_out
  *          (elements); DUST_F32 or DUST_BF16 (bf16 rounded to nearest even).
- *   kind   DUST_NOISE_RADEMACHER or DUST_NOISE_GAUSSIAN; draw >= 0.
+ *   kind   DUST_NOISE_RADEMACHER, DUST_NOISE_GAUSSIAN or
+ *          DUST_NOISE_RADEMACHER_PACKED; draw >= 0.
  */
 dust_status dust_jitter_apply(void* y, dust_dtype y_dtype, int64_t ld_y, int64_t T,
                               int64_t d_out, uint64_t seed, dust_noise_kind kind,
@@ -224,7 +230,8 @@ dust_status dust_contract(const void* g, const void* X, dust_dtype dtype, int64_
  *               d_in % 8 == 0 and d_out % 8 == 0 (otherwise the CUDA-core
  *               contraction runs).
  *   delta       device f32 [K][T]; seq_offsets as for dust_credit_scan.
- *   kind        DUST_NOISE_RADEMACHER or DUST_NOISE_GAUSSIAN.
+ *   kind        DUST_NOISE_RADEMACHER, DUST_NOISE_GAUSSIAN or
+ *               DUST_NOISE_RADEMACHER_PACKED.
  *   draw_begin  absolute index of the first draw (>= 0).
  *   sigma       finite, non-zero; gamma finite, |gamma| <= 1; scale finite.
  *   flags       DUST_CENTER, DUST_ANTITHETIC, DUST_ACCUMULATE and at most one

@@ -108,3 +108,24 @@ def test_scan_and_weighting_reject_bad_arguments(L):
     assert L.dust_error_estimate(fake, 4, 8, 8, 0, dust.GAUSSIAN, 0, 0.0, 0, fake, dust.F32, NULL) == dust.ERR_INVALID_ARG
     assert L.dust_error_estimate(fake, 3, 8, 8, 0, dust.GAUSSIAN, 0, 1.0, dust.ANTITHETIC, fake, dust.F32, NULL) == dust.ERR_INVALID_ARG
     assert L.dust_error_estimate(fake, 4, 8, 8, 0, dust.GAUSSIAN, 0, 1.0, 0, fake, dust.U32, NULL) == dust.ERR_INVALID_ARG
+
+
+def test_packed_signs_accepted_where_values_are(L):
+    """DUST_NOISE_RADEMACHER_PACKED is a value kind like the other two: it is
+    refused as a word stream and as a U32 output, and unknown kinds (4) are
+    refused everywhere."""
+    fake = C.c_void_p(1 << 20)
+    P = dust.RADEMACHER_PACKED
+    assert L.dust_noise(fake, dust.U32, 0, P, 0, 1, 4, 4, 0, NULL) == dust.ERR_INVALID_ARG
+    assert L.dust_noise(fake, dust.F32, 0, P, 0, 1, 4, 4, dust.WORD_STREAM1, NULL) == \
+        dust.ERR_INVALID_ARG
+    assert L.dust_noise(NULL, dust.F32, 0, P, 0, 0, 4, 4, 0, NULL) == dust.OK
+    assert L.dust_noise(fake, dust.F32, 0, 4, 0, 1, 4, 4, 0, NULL) == dust.ERR_INVALID_ARG
+    assert L.dust_jitter_apply(fake, dust.F32, 4, 0, 4, 0, P, 0, 1.0, 0, NULL) == dust.OK
+    assert L.dust_jitter_apply(fake, dust.F32, 4, 4, 4, 0, 4, 0, 1.0, 0, NULL) == \
+        dust.ERR_INVALID_ARG
+    assert L.dust_jitter_apply(fake, dust.F32, 4, 4, 4, 0, dust.RAW_WORDS, 0, 1.0, 0, NULL) == \
+        dust.ERR_INVALID_ARG
+    assert L.dust_error_estimate(fake, 4, 0, 8, 0, P, 0, 1.0, 0, fake, dust.F32, NULL) == dust.OK
+    assert L.dust_error_estimate(fake, 4, 8, 8, 0, 4, 0, 1.0, 0, fake, dust.F32, NULL) == \
+        dust.ERR_INVALID_ARG

@@ -28,6 +28,11 @@ W_CASES = [
     (65, 31, 513, 1, 123, 0),
     (16, 200, 2048, 1, 0, 0),
     (130, 17, 64, 0, 2, dust.ANTITHETIC),
+    # packed signs: one 32-sign word per lane, 1024 channels per CTA
+    (8, 100, 77, 3, 0, 0),            # a 13-channel last word
+    (65, 33, 1000, 3, 5, 0),          # two draw groups, a ragged CTA
+    (16, 64, 2048, 3, 2, dust.ANTITHETIC),
+    (3, 5, 31, 3, 1, 0),              # narrower than one word
 ]
 
 
@@ -81,6 +86,7 @@ SMALL = [
     wl.QKV_DECAY.scaled(n_seq=2, seq_len=300, d_in=64, d_out=192),
     wl.SQUARE_R.scaled(n_seq=4, seq_len=64, d_in=128, d_out=128, K=16),
     wl.SQUARE_G.scaled(n_seq=4, seq_len=64, d_in=120, d_out=40, K=16),
+    wl.SQUARE_RP.scaled(n_seq=4, seq_len=64, d_in=128, d_out=200, K=16),
 ]
 
 FORCE = [0, dust.FORCE_SIMT, dust.FORCE_UNFUSED, dust.FORCE_FUSED]
@@ -96,6 +102,11 @@ def test_estimate_gW_small(w, force):
         path = dust.dust_estimate_gW_path(w.T, w.d_in, w.d_out, w.K, xd, flags)
     except dust.DustError as e:
         assert e.status == dust.ERR_UNSUPPORTED
+        return
+    if w.kind == dust.RADEMACHER_PACKED and force == dust.FORCE_FUSED:
+        with pytest.raises(dust.DustError) as e:  # the fused kernel has no packed signs
+            _run(w, X, delta, so, flags)
+        assert e.value.status == dust.ERR_UNSUPPORTED
         return
     got = _run(w, X, delta, so, flags).double().cpu().numpy()
     want = oracle.estimate_gW(X, delta, w.d_out, so, w.seed, w.kind, 0, np.float32(w.sigma),
@@ -303,6 +314,20 @@ def test_fused_limits():
         dust.dust_estimate_gW_path(1024, 520, 256, 8, dust.BF16, dust.CENTER | dust.FORCE_FUSED)
     with pytest.raises(dust.DustError):
         dust.dust_estimate_gW_path(1024, 64, 64, 8, dust.F32, dust.CENTER | dust.FORCE_FUSED)
+
+
+def test_fused_rejects_packed_signs():
+    """The fused kernel evaluates only Gaussian and per-channel signs: packed
+    signs with DUST_FORCE_FUSED are refused before anything is enqueued."""
+    import torch
+    dev = cuda()
+    X = torch.zeros((256, 64), dtype=torch.bfloat16, device=dev)
+    delta = torch.zeros((4, 256), dtype=torch.float32, device=dev)
+    so = torch.tensor([0, 256], dtype=torch.int32, device=dev)
+    with pytest.raises(dust.DustError) as e:
+        dust.dust_estimate_gW(X, delta, 64, so, 0, dust.RADEMACHER_PACKED, 0, 1e-3, 0.0, 1.0,
+                              dust.CENTER | dust.FORCE_FUSED)
+    assert e.value.status == dust.ERR_UNSUPPORTED
 
 
 @pytest.mark.slow

@@ -34,12 +34,13 @@ def test_raw_words_bit_exact(draw_begin, n_draws, T, d_out, stream):
 
 @pytest.mark.parametrize("draw_begin,n_draws,T,d_out", SHAPES)
 @pytest.mark.parametrize("flags", [0, dust.ANTITHETIC])
-def test_rademacher_bit_exact(draw_begin, n_draws, T, d_out, flags):
+@pytest.mark.parametrize("kind", [dust.RADEMACHER, dust.RADEMACHER_PACKED])
+def test_rademacher_bit_exact(draw_begin, n_draws, T, d_out, flags, kind):
     import torch
     dev = cuda()
     out = torch.empty((n_draws, T, d_out), dtype=torch.float32, device=dev)
-    dust.dust_noise(out, 42, dust.RADEMACHER, draw_begin, n_draws, T, d_out, flags)
-    want = oracle.noise(42, oracle.RADEMACHER, draw_begin, n_draws, T, d_out, flags)
+    dust.dust_noise(out, 42, kind, draw_begin, n_draws, T, d_out, flags)
+    want = oracle.noise(42, kind, draw_begin, n_draws, T, d_out, flags)
     assert np.array_equal(out.cpu().numpy().astype(np.float64), want)
 
 
@@ -59,7 +60,7 @@ def test_gaussian_within_bound(draw_begin, n_draws, T, d_out, flags):
 def test_bf16_output_is_rounded_fp32():
     import torch
     dev = cuda()
-    for kind in (dust.RADEMACHER, dust.GAUSSIAN):
+    for kind in (dust.RADEMACHER, dust.GAUSSIAN, dust.RADEMACHER_PACKED):
         a = torch.empty((2, 100, 77), dtype=torch.float32, device=dev)
         b = torch.empty((2, 100, 77), dtype=torch.bfloat16, device=dev)
         dust.dust_noise(a, 3, kind, 5, 2, 100, 77)
@@ -86,7 +87,7 @@ def test_counter_limit_two_pow_32():
         dust.dust_noise(torch.empty(1, device=dev), 99, dust.RADEMACHER, 0, 1, T + 1, d_out)
 
 
-@pytest.mark.parametrize("kind", [0, 1])
+@pytest.mark.parametrize("kind", [0, 1, 3])
 @pytest.mark.parametrize("flags", [0, dust.ANTITHETIC])
 def test_jitter_f32(kind, flags):
     import torch

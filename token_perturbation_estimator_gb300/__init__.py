@@ -23,7 +23,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "dust.h")
 # dust_status
 OK, ERR_INVALID_ARG, ERR_RANGE, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE = range(7)
 # dust_noise_kind
-RADEMACHER, GAUSSIAN, RAW_WORDS = 0, 1, 2
+RADEMACHER, GAUSSIAN, RAW_WORDS, RADEMACHER_PACKED = 0, 1, 2, 3
 # dust_dtype
 F32, BF16, U32 = 0, 1, 2
 # flags

@@ -34,6 +34,12 @@ dust_status counter_ok(int64_t T, int64_t d_out) {
 
 dust_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DUST_OK : DUST_ERR_CUDA; }
 
+// Noise kinds that give jitter values (all but the raw words).
+bool value_kind(int kind) {
+    return kind == DUST_NOISE_RADEMACHER || kind == DUST_NOISE_GAUSSIAN ||
+           kind == DUST_NOISE_RADEMACHER_PACKED;
+}
+
 // Shape/flag validation shared by the estimator entry points.
 dust_status check_estimate(int64_t T, int64_t d_in, int64_t d_out, int64_t K, dust_dtype x_dtype,
                            uint32_t flags) {
@@ -132,7 +138,7 @@ dust_status dust_noise(void* out, dust_dtype out_dtype, uint64_t seed, dust_nois
     if (kind == DUST_NOISE_RAW_WORDS) {
         if (out_dtype != DUST_U32) return DUST_ERR_INVALID_ARG;
         out_kind = 2;
-    } else if (kind == DUST_NOISE_RADEMACHER || kind == DUST_NOISE_GAUSSIAN) {
+    } else if (value_kind(kind)) {
         if (out_dtype == DUST_F32) out_kind = 0;
         else if (out_dtype == DUST_BF16) out_kind = 1;
         else return DUST_ERR_INVALID_ARG;
@@ -155,7 +161,7 @@ dust_status dust_jitter_apply(void* y, dust_dtype y_dtype, int64_t ld_y, int64_t
     if (st != DUST_OK) return st;
     if (ld_y < d_out || draw < 0) return DUST_ERR_INVALID_ARG;
     if (draw >= (int64_t(1) << 31)) return DUST_ERR_RANGE;
-    if (kind != DUST_NOISE_RADEMACHER && kind != DUST_NOISE_GAUSSIAN) return DUST_ERR_INVALID_ARG;
+    if (!value_kind(kind)) return DUST_ERR_INVALID_ARG;
     if (y_dtype != DUST_F32 && y_dtype != DUST_BF16) return DUST_ERR_INVALID_ARG;
     if (flags & ~DUST_ANTITHETIC) return DUST_ERR_INVALID_ARG;
     if (!finite(sigma)) return DUST_ERR_INVALID_ARG;
@@ -206,7 +212,7 @@ dust_status dust_error_estimate(const float* r, int64_t K, int64_t T, int64_t d_
     if (K > DUST_MAX_DRAWS) return DUST_ERR_RANGE;
     dust_status st = counter_ok(T, d_out);
     if (st != DUST_OK) return st;
-    if (kind != DUST_NOISE_RADEMACHER && kind != DUST_NOISE_GAUSSIAN) return DUST_ERR_INVALID_ARG;
+    if (!value_kind(kind)) return DUST_ERR_INVALID_ARG;
     if (g_dtype != DUST_F32 && g_dtype != DUST_BF16) return DUST_ERR_INVALID_ARG;
     if (flags & ~(DUST_CENTER | DUST_ANTITHETIC)) return DUST_ERR_INVALID_ARG;
     if ((flags & DUST_ANTITHETIC) && ((K & 1) || (draw_begin & 1))) return DUST_ERR_INVALID_ARG;
@@ -293,7 +299,7 @@ dust_status estimate(const void* X, dust_dtype x_dtype, int64_t T, int64_t d_in,
                      void* workspace, size_t ws_bytes, void* stream, cudaEvent_t x_ready) {
     dust_status st = check_estimate(T, d_in, d_out, K, x_dtype, flags);
     if (st != DUST_OK) return st;
-    if (kind != DUST_NOISE_RADEMACHER && kind != DUST_NOISE_GAUSSIAN) return DUST_ERR_INVALID_ARG;
+    if (!value_kind(kind)) return DUST_ERR_INVALID_ARG;
     if (draw_begin < 0) return DUST_ERR_INVALID_ARG;
     if (draw_begin > (int64_t(1) << 31) - K) return DUST_ERR_RANGE;
     if ((flags & DUST_ANTITHETIC) && (draw_begin & 1)) return DUST_ERR_INVALID_ARG;
@@ -311,6 +317,9 @@ dust_status estimate(const void* X, dust_dtype x_dtype, int64_t T, int64_t d_in,
     if (reinterpret_cast<uintptr_t>(X) % 16) return DUST_ERR_INVALID_ARG;
     const Layout L = layout(T, d_in, d_out, K, x_dtype, flags);
     if (L.path < 0) return static_cast<dust_status>(-L.path);
+    // The fused kernel evaluates Gaussian or per-channel Rademacher noise only.
+    if (L.path == DUST_PATH_FUSED_TC && kind == DUST_NOISE_RADEMACHER_PACKED)
+        return DUST_ERR_UNSUPPORTED;
     if (!workspace || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255))
         return DUST_ERR_WORKSPACE;
 

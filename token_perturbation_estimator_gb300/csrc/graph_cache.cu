@@ -2,8 +2,9 @@
 //
 // One estimator call issues a memset and three to five kernels; on the host
 // that is about 20 microseconds, and small layers are launch-bound (64 x 64,
-// 256 tokens: 35.8 -> 32.6 us per synchronised call with graphs). A call whose every argument matches an earlier one is captured once
-// into a graph and afterwards launched with a single cudaGraphLaunch. The
+// 256 tokens: 35.8 -> 32.6 us per synchronised call with graphs). A call
+// whose every argument matches an earlier one is captured once into a graph
+// and afterwards launched with a single cudaGraphLaunch. The
 // graph holds the same pointers and scalars, so it reads the buffers' current
 // contents and is exactly the work the direct launches would do.
 #include <cstddef>

@@ -37,6 +37,14 @@ __global__ void __launch_bounds__(256) k_noise(void* __restrict__ out, uint32_t 
         if (kind == 0) {
             v0 = noise_value(0, skey, i, n0, n0, false, anti);
             if (has_odd) v1 = noise_value(0, skey, i, n0 + 1, n0, true, anti);
+        } else if (kind == 3) {
+            // p is even, so p and p + 1 share their 32-channel group's word
+            const int64_t bi = anti ? (i >> 1) : i;
+            const uint32_t sg = (anti && (i & 1)) ? 0x80000000u : 0u;
+            const int j = static_cast<int>(p & 31);
+            const uint32_t w = word_ff(fold16(draw_key(skey, bi, 0)), fold16(n0 - j));
+            v0 = __uint_as_float(0x3F800000u | (packed_sign_bit(w, j) ^ sg));
+            v1 = __uint_as_float(0x3F800000u | (packed_sign_bit(w, j + 1) ^ sg));
         } else {
             float sgn = 1.0f;
             int64_t bi = i;
@@ -88,6 +96,11 @@ __global__ void __launch_bounds__(256) k_jitter(void* __restrict__ y, int64_t ld
         if (kind == 0) {
             a0 = __uint_as_float(0x3F800000u | sign_ff(kf0, fold16(n0)));
             a1 = __uint_as_float(0x3F800000u | sign_ff(kf0, fold16(n0 + 1)));
+        } else if (kind == 3) {
+            const int j = static_cast<int>(p & 31);
+            const uint32_t w = word_ff(kf0, fold16(n0 - j));
+            a0 = __uint_as_float(0x3F800000u | packed_sign_bit(w, j));
+            a1 = __uint_as_float(0x3F800000u | packed_sign_bit(w, j + 1));
         } else {
             const uint32_t nf = fold16(n0);
             gauss_pair(unit_ff(kf0, nf), unit_ff(kf1, nf), a0, a1);

@@ -6,7 +6,8 @@
 // is stored.
 //
 // Mapping: one warp per token, kCpt channels per lane (kCpt/2 Box-Muller pairs
-// or kCpt signs), 8 tokens x 32 kCpt channels per CTA. The per-draw keys and the
+// or kCpt signs; packed signs: the 32 channels of one hash word), 8 tokens x
+// 32 lanes' channels per CTA. The per-draw keys and the
 // per-token rewards (already multiplied by -1/(K sigma); for antithetic pairs,
 // the pair's reward difference, one per base draw) are staged in shared
 // memory 64 draws at a time and read as warp-wide broadcasts. The per-channel counters are pre-folded once
@@ -38,7 +39,8 @@ constexpr int kMinBlocksR = DUST_WEIGHT_MINB_R;
 constexpr int kUnrollW = DUST_WEIGHT_UNROLL;
 constexpr int kTok = 8;                 // tokens per CTA (one per warp)
 constexpr int kCpt = DUST_WEIGHT_CPT;   // channels per lane (8 or 16)
-constexpr int kCh = 32 * kCpt;          // channels per CTA
+// Channels per lane for a noise kind: one 32-sign word for packed signs.
+constexpr int cpt_of(int kind) { return kind == 3 ? 32 : kCpt; }
 constexpr int kGroup = 64;              // draws staged per pass
 static_assert(kCpt % 8 == 0, "channels per lane must be a multiple of 8");
 
@@ -87,22 +89,25 @@ __global__ void __launch_bounds__(256, KIND == 1 ? kMinBlocksG : kMinBlocksR)
     pdl_wait();
     pdl_trigger();
 
+    // Channels per lane: one 32-sign word for the packed signs, else kCpt.
+    constexpr int cpt = cpt_of(KIND);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t tb = static_cast<int64_t>(blockIdx.x) * kTok;
     const int64_t t = tb + warp;
-    const int64_t c0 = static_cast<int64_t>(blockIdx.y) * kCh + lane * kCpt;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.y) * (32 * cpt) + lane * cpt;
     const bool active = (t < T) && (c0 < d_out);
 
-    // Pre-folded counters: pairs for the Gaussian, single channels for signs.
-    constexpr int kNf = (KIND == 1) ? kCpt / 2 : kCpt;
+    // Pre-folded counters: pairs for the Gaussian, single channels for signs,
+    // the group's first channel for packed signs.
+    constexpr int kNf = (KIND == 1) ? cpt / 2 : (KIND == 3 ? 1 : cpt);
     uint32_t nf[kNf];
     const uint32_t base = static_cast<uint32_t>(t * d_out + c0);
 #pragma unroll
     for (int j = 0; j < kNf; ++j) nf[j] = fold16(base + (KIND == 1 ? 2u * j : j));
 
-    float acc[kCpt];
+    float acc[cpt];
 #pragma unroll
-    for (int j = 0; j < kCpt; ++j) acc[j] = 0.0f;
+    for (int j = 0; j < cpt; ++j) acc[j] = 0.0f;
 
     // With antithetic pairs, draws 2b and 2b + 1 carry +a and -a of base draw
     // b, so each base draw's noise is evaluated once, weighted by the
@@ -144,7 +149,7 @@ __global__ void __launch_bounds__(256, KIND == 1 ? kMinBlocksG : kMinBlocksR)
                     const float rr = s_r[warp][k];
                     const uint2 key = s_key[k];
 #pragma unroll
-                    for (int p = 0; p < kCpt / 2; ++p) {
+                    for (int p = 0; p < cpt / 2; ++p) {
                         const float f0 = unit_ff(key.x, nf[p]);
                         const float f1 = unit_ff(key.y, nf[p]);
                         const float tr = rr * neg_radius(f0);
@@ -154,13 +159,22 @@ __global__ void __launch_bounds__(256, KIND == 1 ? kMinBlocksG : kMinBlocksR)
                         acc[2 * p + 1] = fmaf(tr, sn, acc[2 * p + 1]);
                     }
                 }
+            } else if (KIND == 3) {
+#pragma unroll 2
+                for (int k = 0; k < gn; ++k) {
+                    const uint32_t rb = __float_as_uint(s_r[warp][k]);
+                    const uint32_t w = word_ff(s_key[k].x, nf[0]);
+#pragma unroll
+                    for (int j = 0; j < cpt; ++j)
+                        acc[j] += __uint_as_float(rb ^ packed_sign_bit(w, j));
+                }
             } else {
 #pragma unroll 2
                 for (int k = 0; k < gn; ++k) {
                     const uint32_t rb = __float_as_uint(s_r[warp][k]);
                     const uint32_t k0 = s_key[k].x;
 #pragma unroll
-                    for (int j = 0; j < kCpt; ++j)
+                    for (int j = 0; j < cpt; ++j)
                         acc[j] += __uint_as_float(rb ^ sign_ff(k0, nf[j]));
                 }
             }
@@ -170,7 +184,7 @@ __global__ void __launch_bounds__(256, KIND == 1 ? kMinBlocksG : kMinBlocksR)
     if (active) {
         const bool vec = vec_ok;  // 16-byte aligned rows (host-checked)
 #pragma unroll
-        for (int q = 0; q < kCpt / 8; ++q) {
+        for (int q = 0; q < cpt / 8; ++q) {
             const int64_t cq = c0 + 8 * q;
             if (cq < d_out) store8<OutT>(g, t, d_out, cq, acc + 8 * q, vec && cq + 8 <= d_out);
         }
@@ -181,8 +195,9 @@ template <int KIND, bool FIX>
 cudaError_t launch_kind(const ScanBuffers& b, int64_t K, int64_t T, int64_t d_out, uint32_t skey,
                         int64_t draw_begin, float coef, bool anti, void* g, int g_bf16,
                         cudaStream_t s) {
+    constexpr int ch = 32 * cpt_of(KIND);  // channels per CTA
     dim3 grid(static_cast<unsigned>((T + kTok - 1) / kTok),
-              static_cast<unsigned>((d_out + kCh - 1) / kCh));
+              static_cast<unsigned>((d_out + ch - 1) / ch));
     const bool vec_ok = (d_out % 8 == 0) && (reinterpret_cast<uintptr_t>(g) % 16 == 0);
     ProfScope ps(kStageWeight, s);
     auto go = [&](auto kernel, auto* out) {
@@ -208,6 +223,9 @@ cudaError_t launch_weight(const ScanBuffers& b, bool fix, int64_t K, int64_t T, 
     if (kind == 1)
         return fix ? launch_kind<1, true>(b, K, T, d_out, skey, draw_begin, coef, anti, g, g_bf16, s)
                    : launch_kind<1, false>(b, K, T, d_out, skey, draw_begin, coef, anti, g, g_bf16, s);
+    if (kind == 3)
+        return fix ? launch_kind<3, true>(b, K, T, d_out, skey, draw_begin, coef, anti, g, g_bf16, s)
+                   : launch_kind<3, false>(b, K, T, d_out, skey, draw_begin, coef, anti, g, g_bf16, s);
     return fix ? launch_kind<0, true>(b, K, T, d_out, skey, draw_begin, coef, anti, g, g_bf16, s)
                : launch_kind<0, false>(b, K, T, d_out, skey, draw_begin, coef, anti, g, g_bf16, s);
 }

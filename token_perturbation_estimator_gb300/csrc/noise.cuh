@@ -112,6 +112,13 @@ __device__ __forceinline__ void gauss_pair(float f0, float f1, float& a_even, fl
     a_odd = nr * s;
 }
 
+// Packed Rademacher: 32 signs per word. Bit j of the word at the counter of a
+// 32-channel group's first channel is channel (first + j)'s sign, as the
+// float sign bit (0: +1).
+__device__ __forceinline__ uint32_t packed_sign_bit(uint32_t w, int j) {
+    return (w << (31 - j)) & 0x80000000u;
+}
+
 // Scalar reference path on the device: value of a_t^(i)[c] (absolute draw i).
 // Used by the materialising kernels (noise, jitter) where speed is secondary.
 __device__ __forceinline__ float noise_value(int kind, uint32_t skey, int64_t i, uint32_t n,

@@ -19,6 +19,7 @@ import numpy as np
 
 RADEMACHER = 0
 GAUSSIAN = 1
+RADEMACHER_PACKED = 3  # 32 signs per hash word
 
 SEED_EST, SEED_X, SEED_PLANT, SEED_EPS = 0, 1, 2, 3
 
@@ -82,6 +83,9 @@ SQUARE_R = Workload("square_4096_T32768_K64_rademacher", 4096, 4096, 32, 1024, 6
                     RADEMACHER, "bf16", 1.0, x_channel_scale=True)
 SQUARE_G = Workload("square_4096_T32768_K64_gaussian", 4096, 4096, 32, 1024, 64, 5e-4, 0.0,
                     GAUSSIAN, "bf16", 1.0, x_channel_scale=True)
+# The square layer with packed signs (32 per hash word): same shapes and draws.
+SQUARE_RP = Workload("square_4096_T32768_K64_rademacher_packed", 4096, 4096, 32, 1024, 64,
+                     5e-4, 0.0, RADEMACHER_PACKED, "bf16", 1.0, x_channel_scale=True)
 
 
 def sweep_sites():
@@ -96,7 +100,7 @@ def sweep_sites():
     return sites
 
 
-CONFIGS = {w.name: w for w in (TOY, MLP_UP, QKV_DECAY, SQUARE_R, SQUARE_G)}
+CONFIGS = {w.name: w for w in (TOY, MLP_UP, QKV_DECAY, SQUARE_R, SQUARE_G, SQUARE_RP)}
 
 
 def seq_offsets(w: Workload) -> np.ndarray:
