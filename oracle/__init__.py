@@ -57,6 +57,7 @@ def lib():
             "dust_oracle_bruteforce_gW": (None, [P, i64, i64, P, i64, i64, P, i64, u64, i32,
                                                  i64, f64, f64, f64, u32, P]),
             "dust_oracle_jitter": (None, [P, i64, i64, i64, u64, i32, i64, f64, u32]),
+            "dust_oracle_local_score": (None, [P, P, i64, i64, i64, P]),
             "dust_oracle_planted_delta": (None, [P, P, P, i64, i64, i64, u64, i32, i64, f64,
                                                  f64, u32]),
         }
@@ -216,6 +217,18 @@ def jitter(y, seed, kind, draw, sigma, flags=0):
     T, d_out = y.shape
     lib().dust_oracle_jitter(_p(y), d_out, T, d_out, seed, kind, draw, float(sigma), flags)
     return y
+
+
+def local_score(g, delta_o):
+    """delta[k][s] = <g[s], delta_o[k][s]>: the loss change whose reduction is
+    the page's local score c_s = -<g_s, delta_o_s>."""
+    g = _f64(g)
+    delta_o = _f64(delta_o)
+    K, T, d = delta_o.shape
+    assert g.shape == (T, d)
+    out = np.empty((K, T), dtype=np.float64)
+    lib().dust_oracle_local_score(_p(g), _p(delta_o), K, T, d, _p(out))
+    return out
 
 
 def planted_delta(dplant, seed, kind, draw_begin, n_draws, sigma, curv=1.0, eps=None,

@@ -362,6 +362,25 @@ OR_EXPORT void dust_oracle_jitter(double* y, int64_t ld_y, int64_t T, int64_t d_
             y[t * ld_y + c] += sigma * or_noise_value(kind, seed, draw, t, c, d_out, flags);
 }
 
+/* Local scores of blocks whose output does not reach the loss directly
+ * ("Dust: every token is a member of the population", section "What the
+ * released code actually does", step 4): the score of a jittered draw at
+ * token s is c_s = -<g_s, delta_o_s>, the estimated output error g_s against
+ * the change delta_o_s of the block's output under that draw. Returned as the
+ * first-order loss change delta[k][s] = <g_s, delta_o[k][s]>, the quantity
+ * the scan consumes (its reduction -delta is the page's c_s).
+ *   g [T][d], delta_o [K][T][d], delta [K][T]. */
+OR_EXPORT void dust_oracle_local_score(const double* g, const double* delta_o, int64_t K,
+                                       int64_t T, int64_t d, double* delta) {
+#pragma omp parallel for schedule(static)
+    for (int64_t q = 0; q < K * T; ++q) {
+        const int64_t t = q % T;
+        double acc = 0.0;
+        for (int64_t j = 0; j < d; ++j) acc += g[t * d + j] * delta_o[q * d + j];
+        delta[q] = acc;
+    }
+}
+
 /* Loss changes of a planted per-token quadratic loss, the workload of the
  * configurations this project measures:
  *   delta[k][t] = sigma <dplant_t, a_t^(draw_begin+k)>
