@@ -150,6 +150,26 @@ dust_status dust_jitter_apply(void* y, dust_dtype y_dtype, int64_t ld_y, int64_t
                               int64_t draw, float sigma, uint32_t flags, void* stream);
 
 /*
+ * dust_local_score — loss changes of draws scored locally: for blocks whose
+ * output does not reach the loss (attention internals), each jittered draw k
+ * is scored at token s against the block output's estimated error ("Dust:
+ * every token is a member of the population", "What the released code
+ * actually does", step 4: c_s = -<g_s, delta_o_s>). Returned as the loss
+ * change delta[k][s] = <g_s, delta_o[k][s]>, the input dust_credit_scan and
+ * dust_estimate_gW take (their reduction -delta is the page's c_s; keys and
+ * values then use gamma 0.98 over later tokens, queries gamma 0).
+ *   g        device [T][d], the block output's estimated error, DUST_F32 or
+ *            DUST_BF16.
+ *   delta_o  device [K][T][d], the change of the block output under each
+ *            draw, DUST_F32 or DUST_BF16.
+ *   delta    device f32 [K][T], written.
+ * Sums run in fp32 in a fixed order (deterministic).
+ */
+dust_status dust_local_score(const void* g, dust_dtype g_dtype, const void* delta_o,
+                             dust_dtype o_dtype, int64_t K, int64_t T, int64_t d,
+                             float* delta, void* stream);
+
+/*
  * dust_credit_scan_workspace / dust_credit_scan — centring and the reverse
  * credit scan on their own (the r_t equation; centring as described above).
  *   delta       device f32 [K][T] loss changes.

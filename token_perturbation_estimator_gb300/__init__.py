@@ -64,6 +64,7 @@ def _signatures():
         "dust_last_error": (i32, [P]),
         "dust_credit_scan_noalloc_capacity": (SZ, []),
         "dust_credit_scan_noalloc": (i32, [P, i64, i64, P, i64, f32, u32, P, P]),
+        "dust_local_score": (i32, [P, i32, P, i32, i64, i64, i64, P, P]),
         "dust_debug_inject_timeout": (i32, [i32]),
         "dust_profile_enable": (i32, [i32]),
         "dust_profile_read": (i32, [P, i32]),
@@ -146,6 +147,21 @@ def dust_jitter_apply(y, seed, kind, draw, sigma, flags=0, stream=None):
                                    draw, float(sigma), flags, _stream(stream)),
            "dust_jitter_apply")
     return y
+
+
+def dust_local_score(g, delta_o, out=None, stream=None):
+    """g: CUDA [T, d] (f32 or bf16); delta_o: CUDA [K, T, d]; returns the loss
+    changes delta f32 [K, T] = <g[t], delta_o[k, t]>."""
+    import torch
+    _need_cuda(g, delta_o, out)
+    K, T, d = delta_o.shape
+    if tuple(g.shape) != (T, d):
+        raise ValueError("g must be [T, d] matching delta_o [K, T, d]")
+    if out is None:
+        out = torch.empty((K, T), dtype=torch.float32, device=delta_o.device)
+    _check(lib().dust_local_score(_ptr(g), _dtype_code(g), _ptr(delta_o), _dtype_code(delta_o),
+                                  K, T, d, _ptr(out), _stream(stream)), "dust_local_score")
+    return out
 
 
 def dust_credit_scan_workspace(K, T):

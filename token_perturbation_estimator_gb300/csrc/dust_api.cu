@@ -172,6 +172,19 @@ dust_status dust_jitter_apply(void* y, dust_dtype y_dtype, int64_t ld_y, int64_t
                                      static_cast<cudaStream_t>(stream)));
 }
 
+dust_status dust_local_score(const void* g, dust_dtype g_dtype, const void* delta_o,
+                             dust_dtype o_dtype, int64_t K, int64_t T, int64_t d,
+                             float* delta, void* stream) {
+    if (K < 0 || T < 0 || d < 0) return DUST_ERR_INVALID_ARG;
+    if ((g_dtype != DUST_F32 && g_dtype != DUST_BF16) ||
+        (o_dtype != DUST_F32 && o_dtype != DUST_BF16))
+        return DUST_ERR_INVALID_ARG;
+    if (K * T == 0) return DUST_OK;
+    if (!delta || (d > 0 && (!g || !delta_o))) return DUST_ERR_INVALID_ARG;
+    return cuda_status(launch_local_score(g, g_dtype == DUST_BF16, delta_o, o_dtype == DUST_BF16,
+                                          K, T, d, delta, static_cast<cudaStream_t>(stream)));
+}
+
 dust_status dust_credit_scan_workspace(size_t* bytes, int64_t K, int64_t T) {
     if (!bytes || K < 1 || T < 0) return DUST_ERR_INVALID_ARG;
     if (K > DUST_MAX_DRAWS) return DUST_ERR_RANGE;

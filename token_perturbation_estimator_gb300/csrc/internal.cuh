@@ -17,7 +17,8 @@ unsigned int* status_word();
 // Kernel families timed by dust_profile_read.
 enum Stage {
     kStageScanLocal, kStageScanCarry, kStageScanFixup, kStageWeight, kStageGemmSimt,
-    kStageReduce, kStageGemmTc, kStageFused, kStageNoise, kStageJitter, kStageZero, kStageCount
+    kStageReduce, kStageGemmTc, kStageFused, kStageNoise, kStageJitter, kStageZero, kStageScore,
+    kStageCount
 };
 
 // Brackets the launches issued during its lifetime with profiling events
@@ -159,6 +160,10 @@ cudaError_t launch_fused(const ScanBuffers& b, const void* X, int64_t K, int64_t
                          int64_t d_out, uint64_t seed, int kind, int64_t draw_begin, float coef,
                          bool anti, float scale, bool accumulate, float* gW, float* partials,
                          cudaStream_t s);
+
+// delta[k][t] = <g[t], dO[k][t]> (local scores as loss changes), rows of d.
+cudaError_t launch_local_score(const void* g, int g_bf16, const void* dO, int o_bf16, int64_t K,
+                               int64_t T, int64_t d, float* out, cudaStream_t s);
 
 // Fill gW with zeros (T == 0) unless accumulating.
 cudaError_t launch_zero(float* p, int64_t n, cudaStream_t s);

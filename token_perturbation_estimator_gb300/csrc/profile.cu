@@ -15,7 +15,8 @@ namespace {
 
 const char* const kStageNames[kStageCount] = {"scan_local", "scan_carry", "scan_fixup", "weight",
                                               "gemm_simt",  "reduce",     "gemm_tc",    "fused",
-                                              "noise",      "jitter",     "zero"};
+                                              "noise",      "jitter",     "zero",
+                                              "score"};
 constexpr int kMaxRecords = 65536;
 
 struct Rec {
