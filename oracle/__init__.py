@@ -58,6 +58,7 @@ def lib():
                                                  i64, f64, f64, f64, u32, P]),
             "dust_oracle_jitter": (None, [P, i64, i64, i64, u64, i32, i64, f64, u32]),
             "dust_oracle_local_score": (None, [P, P, i64, i64, i64, P]),
+            "dust_oracle_scatter_gE": (i64, [P, P, i64, i64, i64, f64, P]),
             "dust_oracle_planted_delta": (None, [P, P, P, i64, i64, i64, u64, i32, i64, f64,
                                                  f64, u32]),
         }
@@ -217,6 +218,18 @@ def jitter(y, seed, kind, draw, sigma, flags=0):
     T, d_out = y.shape
     lib().dust_oracle_jitter(_p(y), d_out, T, d_out, seed, kind, draw, float(sigma), flags)
     return y
+
+
+def scatter_gE(g, ids, V, scale=1.0):
+    """gE[v] = scale * sum of g[t] over the tokens t with ids[t] == v, in token
+    order; ids outside [0, V) are skipped (their count is returned too)."""
+    g = _f64(g)
+    T, d = g.shape
+    ids = _i32(ids)
+    assert ids.shape == (T,)
+    out = np.empty((V, d), dtype=np.float64)
+    bad = lib().dust_oracle_scatter_gE(_p(g), _p(ids), T, d, V, float(scale), _p(out))
+    return out, int(bad)
 
 
 def local_score(g, delta_o):
