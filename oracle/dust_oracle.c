@@ -362,6 +362,27 @@ OR_EXPORT void dust_oracle_jitter(double* y, int64_t ld_y, int64_t T, int64_t d_
             y[t * ld_y + c] += sigma * or_noise_value(kind, seed, draw, t, c, d_out, flags);
 }
 
+/* Embedding reassembly ("Dust: every token is a member of the population",
+ * "What the released code actually does", step 7: "a scatter-add for an
+ * embedding"): the error estimate of token t adds into the row of its token
+ * id, gE[v][c] = scale * sum_{t : ids[t] = v} g[t][c], summed in token order.
+ * Returns the number of ids outside [0, V) (skipped). */
+OR_EXPORT int64_t dust_oracle_scatter_gE(const double* g, const int32_t* ids, int64_t T,
+                                         int64_t d, int64_t V, double scale, double* gE) {
+    int64_t bad = 0;
+    for (int64_t q = 0; q < V * d; ++q) gE[q] = 0.0;
+    for (int64_t t = 0; t < T; ++t) {
+        const int64_t v = ids[t];
+        if (v < 0 || v >= V) {
+            ++bad;
+            continue;
+        }
+        for (int64_t c = 0; c < d; ++c) gE[v * d + c] += g[t * d + c];
+    }
+    for (int64_t q = 0; q < V * d; ++q) gE[q] *= scale;
+    return bad;
+}
+
 /* Local scores of blocks whose output does not reach the loss directly
  * ("Dust: every token is a member of the population", section "What the
  * released code actually does", step 4): the score of a jittered draw at
