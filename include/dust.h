@@ -170,6 +170,50 @@ dust_status dust_local_score(const void* g, dust_dtype g_dtype, const void* delt
                              float* delta, void* stream);
 
 /*
+ * dust_scatter_gE_workspace / dust_scatter_gE — embedding reassembly ("Dust:
+ * every token is a member of the population", "What the released code
+ * actually does", step 7: the error estimate becomes a weight gradient by "a
+ * scatter-add for an embedding"): gE[v][c] = scale * sum over the tokens t
+ * with ids[t] = v of g[t][c].
+ *   g         device [T][d], DUST_F32 or DUST_BF16 (finite values).
+ *   ids       device int32 [T]; ids outside [0, V) are skipped and make
+ *             dust_last_error report DUST_ERR_INVALID_ARG.
+ *   gE        device f32 [V][d]; overwritten, or accumulated into with
+ *             DUST_ACCUMULATE (the only flag).
+ *   workspace device, >= dust_scatter_gE_workspace(V, d) bytes, 256-byte
+ *             aligned (about 8 V d bytes); contents on entry are ignored.
+ * Deterministic whatever the order in which tokens arrive: sums are kept in
+ * 64-bit fixed point with a step of 2^-s chosen per call so that
+ * max|g| * (largest count of one id) * 2^s < 2^61; each term is rounded once
+ * to that step, and the result is rounded to fp32 at the end.
+ */
+dust_status dust_scatter_gE_workspace(size_t* bytes, int64_t V, int64_t d);
+dust_status dust_scatter_gE(const void* g, dust_dtype g_dtype, const int32_t* ids, int64_t T,
+                            int64_t d, int64_t V, float scale, uint32_t flags, float* gE,
+                            void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * dust_estimate_gE_workspace / dust_estimate_gE — the whole path for an
+ * embedding E [V][d] whose looked-up rows are jittered: centring and the
+ * credit scan of delta (as dust_credit_scan), the reward weighting into an
+ * fp32 error g [T][d] (as dust_error_estimate; d plays d_out), and the
+ * scatter-add of g into gE by token id (as dust_scatter_gE).
+ *   ids          device int32 [T]; delta device f32 [K][T]; seq_offsets as
+ *                for dust_credit_scan.
+ *   kind         a value noise kind; flags DUST_CENTER, DUST_ANTITHETIC,
+ *                DUST_ACCUMULATE. Other arguments as for dust_estimate_gW.
+ *   workspace    device, >= dust_estimate_gE_workspace(...) bytes, 256-byte
+ *                aligned.
+ */
+dust_status dust_estimate_gE_workspace(size_t* bytes, int64_t T, int64_t d, int64_t V,
+                                       int64_t K);
+dust_status dust_estimate_gE(const int32_t* ids, int64_t T, int64_t V, const float* delta,
+                             int64_t K, int64_t d, const int32_t* seq_offsets, int64_t n_seq,
+                             uint64_t seed, dust_noise_kind kind, int64_t draw_begin,
+                             float sigma, float gamma, float scale, uint32_t flags, float* gE,
+                             void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * dust_credit_scan_workspace / dust_credit_scan — centring and the reverse
  * credit scan on their own (the r_t equation; centring as described above).
  *   delta       device f32 [K][T] loss changes.
@@ -342,8 +386,10 @@ dust_status dust_debug_inject_timeout(int32_t on);
 
 /*
  * dust_last_error — synchronise `stream`, then return and clear the device
- * status word (DUST_OK, or DUST_ERR_TIMEOUT when a kernel's bounded wait ran
- * out since the last call). DUST_ERR_CUDA if the synchronisation failed.
+ * status word (DUST_OK; DUST_ERR_TIMEOUT when a kernel's bounded wait ran out
+ * since the last call; DUST_ERR_INVALID_ARG when dust_scatter_gE or
+ * dust_estimate_gE met a token id outside [0, V)). DUST_ERR_CUDA if the
+ * synchronisation failed.
  */
 dust_status dust_last_error(void* stream);
 

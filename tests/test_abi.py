@@ -129,3 +129,28 @@ def test_packed_signs_accepted_where_values_are(L):
     assert L.dust_error_estimate(fake, 4, 0, 8, 0, P, 0, 1.0, 0, fake, dust.F32, NULL) == dust.OK
     assert L.dust_error_estimate(fake, 4, 8, 8, 0, 4, 0, 1.0, 0, fake, dust.F32, NULL) == \
         dust.ERR_INVALID_ARG
+
+
+def test_scatter_and_embedding_estimator_validation(L):
+    fake = C.c_void_p(1 << 20)
+    n = C.c_size_t(0)
+    assert L.dust_scatter_gE_workspace(C.byref(n), 4096, 512) == dust.OK
+    assert n.value >= 8 * 4096 * 512
+    assert L.dust_scatter_gE(fake, dust.U32, fake, 8, 4, 4, C.c_float(1.0), 0, fake, fake,
+                             1 << 30, NULL) == dust.ERR_INVALID_ARG
+    assert L.dust_scatter_gE(fake, dust.F32, fake, 8, 4, 4, C.c_float(1.0), dust.CENTER, fake,
+                             fake, 1 << 30, NULL) == dust.ERR_INVALID_ARG
+    assert L.dust_scatter_gE(fake, dust.F32, fake, 8, 4, 4, C.c_float(1.0), 0, fake, NULL, 0,
+                             NULL) == dust.ERR_WORKSPACE
+    assert L.dust_scatter_gE(fake, dust.F32, fake, 8, 4, 0, C.c_float(1.0), 0, NULL, NULL, 0,
+                             NULL) == dust.OK
+    assert L.dust_estimate_gE_workspace(C.byref(n), 16384, 512, 4096, 8) == dust.OK
+    assert L.dust_estimate_gE(fake, 8, 4, fake, 4, 4, fake, 1, 0, dust.GAUSSIAN, 0,
+                              C.c_float(0.0), C.c_float(0.0), C.c_float(1.0), 0, fake, fake,
+                              1 << 30, NULL) == dust.ERR_INVALID_ARG  # sigma 0
+    assert L.dust_estimate_gE(fake, 8, 4, fake, 3, 4, fake, 1, 0, dust.GAUSSIAN, 0,
+                              C.c_float(1.0), C.c_float(0.0), C.c_float(1.0), dust.ANTITHETIC,
+                              fake, fake, 1 << 30, NULL) == dust.ERR_INVALID_ARG  # odd K
+    assert L.dust_estimate_gE(fake, 8, 4, fake, 4, 4, fake, 1, 0, dust.RAW_WORDS, 0,
+                              C.c_float(1.0), C.c_float(0.0), C.c_float(1.0), 0, fake, fake,
+                              1 << 30, NULL) == dust.ERR_INVALID_ARG

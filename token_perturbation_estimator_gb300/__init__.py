@@ -65,6 +65,11 @@ def _signatures():
         "dust_credit_scan_noalloc_capacity": (SZ, []),
         "dust_credit_scan_noalloc": (i32, [P, i64, i64, P, i64, f32, u32, P, P]),
         "dust_local_score": (i32, [P, i32, P, i32, i64, i64, i64, P, P]),
+        "dust_scatter_gE_workspace": (i32, [PSZ, i64, i64]),
+        "dust_scatter_gE": (i32, [P, i32, P, i64, i64, i64, f32, u32, P, P, SZ, P]),
+        "dust_estimate_gE_workspace": (i32, [PSZ, i64, i64, i64, i64]),
+        "dust_estimate_gE": (i32, [P, i64, i64, P, i64, i64, P, i64, u64, i32, i64, f32, f32,
+                                   f32, u32, P, P, SZ, P]),
         "dust_debug_inject_timeout": (i32, [i32]),
         "dust_profile_enable": (i32, [i32]),
         "dust_profile_read": (i32, [P, i32]),
@@ -162,6 +167,43 @@ def dust_local_score(g, delta_o, out=None, stream=None):
     _check(lib().dust_local_score(_ptr(g), _dtype_code(g), _ptr(delta_o), _dtype_code(delta_o),
                                   K, T, d, _ptr(out), _stream(stream)), "dust_local_score")
     return out
+
+
+def dust_scatter_gE(g, ids, V, scale=1.0, flags=0, gE=None, workspace=None, stream=None):
+    """g: CUDA [T, d] (f32 or bf16); ids: CUDA int32 [T]; returns gE f32 [V, d]."""
+    import torch
+    _need_cuda(g, ids, gE)
+    T, d = g.shape
+    if gE is None:
+        gE = torch.empty((V, d), dtype=torch.float32, device=g.device)
+    n = C.c_size_t(0)
+    _check(lib().dust_scatter_gE_workspace(C.byref(n), V, d), "dust_scatter_gE_workspace")
+    if workspace is None:
+        workspace = _workspace(n.value, g.device)
+    _check(lib().dust_scatter_gE(_ptr(g), _dtype_code(g), _ptr(ids), T, d, V, float(scale),
+                                 flags, _ptr(gE), _ptr(workspace), workspace.numel(),
+                                 _stream(stream)), "dust_scatter_gE")
+    return gE
+
+
+def dust_estimate_gE(ids, delta, V, d, seq_offsets, seed, kind, draw_begin, sigma, gamma,
+                     scale=1.0, flags=CENTER, gE=None, workspace=None, stream=None):
+    """ids: CUDA int32 [T]; delta: f32 [K, T]; returns gE f32 [V, d]."""
+    import torch
+    _need_cuda(ids, delta, seq_offsets, gE)
+    T = ids.numel()
+    K = delta.shape[0]
+    if gE is None:
+        gE = torch.empty((V, d), dtype=torch.float32, device=ids.device)
+    n = C.c_size_t(0)
+    _check(lib().dust_estimate_gE_workspace(C.byref(n), T, d, V, K), "dust_estimate_gE_workspace")
+    if workspace is None:
+        workspace = _workspace(n.value, ids.device)
+    _check(lib().dust_estimate_gE(_ptr(ids), T, V, _ptr(delta), K, d, _ptr(seq_offsets),
+                                  seq_offsets.numel() - 1, seed, kind, draw_begin, float(sigma),
+                                  float(gamma), float(scale), flags, _ptr(gE), _ptr(workspace),
+                                  workspace.numel(), _stream(stream)), "dust_estimate_gE")
+    return gE
 
 
 def dust_credit_scan_workspace(K, T):

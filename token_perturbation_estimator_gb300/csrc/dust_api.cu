@@ -185,6 +185,90 @@ dust_status dust_local_score(const void* g, dust_dtype g_dtype, const void* delt
                                           K, T, d, delta, static_cast<cudaStream_t>(stream)));
 }
 
+dust_status dust_scatter_gE_workspace(size_t* bytes, int64_t V, int64_t d) {
+    if (!bytes || V < 0 || d < 0) return DUST_ERR_INVALID_ARG;
+    *bytes = a256(scatter_workspace_bytes(V, d));
+    return DUST_OK;
+}
+
+dust_status dust_scatter_gE(const void* g, dust_dtype g_dtype, const int32_t* ids, int64_t T,
+                            int64_t d, int64_t V, float scale, uint32_t flags, float* gE,
+                            void* workspace, size_t ws_bytes, void* stream) {
+    if (T < 0 || d < 0 || V < 0) return DUST_ERR_INVALID_ARG;
+    if (g_dtype != DUST_F32 && g_dtype != DUST_BF16) return DUST_ERR_INVALID_ARG;
+    if (flags & ~DUST_ACCUMULATE) return DUST_ERR_INVALID_ARG;
+    if (!finite(scale)) return DUST_ERR_INVALID_ARG;
+    if (T > 0 && (T > (int64_t(1) << 31) - 1 || (d > 0 && T > (int64_t(1) << 40) / d)))
+        return DUST_ERR_RANGE;
+    if (V * d == 0) return DUST_OK;
+    if (!gE) return DUST_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool acc = (flags & DUST_ACCUMULATE) != 0;
+    if (T == 0) return acc ? DUST_OK : cuda_status(launch_zero(gE, V * d, s));
+    if (!g || !ids) return DUST_ERR_INVALID_ARG;
+    size_t need = 0;
+    dust_scatter_gE_workspace(&need, V, d);
+    if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
+        return DUST_ERR_WORKSPACE;
+    return cuda_status(launch_scatter_gE(g, g_dtype == DUST_BF16, ids, T, d, V, scale, acc, gE,
+                                         workspace, s));
+}
+
+dust_status dust_estimate_gE_workspace(size_t* bytes, int64_t T, int64_t d, int64_t V,
+                                       int64_t K) {
+    if (!bytes || T < 0 || d < 0 || V < 0 || K < 1) return DUST_ERR_INVALID_ARG;
+    if (K > DUST_MAX_DRAWS) return DUST_ERR_RANGE;
+    *bytes = kSyncBytes + a256(scan_workspace_bytes(K, T)) +
+             a256(sizeof(float) * static_cast<size_t>(T) * static_cast<size_t>(d)) +
+             a256(scatter_workspace_bytes(V, d));
+    return DUST_OK;
+}
+
+dust_status dust_estimate_gE(const int32_t* ids, int64_t T, int64_t V, const float* delta,
+                             int64_t K, int64_t d, const int32_t* seq_offsets, int64_t n_seq,
+                             uint64_t seed, dust_noise_kind kind, int64_t draw_begin,
+                             float sigma, float gamma, float scale, uint32_t flags, float* gE,
+                             void* workspace, size_t ws_bytes, void* stream) {
+    if (T < 0 || V < 0 || d < 0 || K < 1) return DUST_ERR_INVALID_ARG;
+    if (K > DUST_MAX_DRAWS) return DUST_ERR_RANGE;
+    if (flags & ~(DUST_CENTER | DUST_ANTITHETIC | DUST_ACCUMULATE)) return DUST_ERR_INVALID_ARG;
+    if (!value_kind(kind)) return DUST_ERR_INVALID_ARG;
+    if (draw_begin < 0) return DUST_ERR_INVALID_ARG;
+    if (draw_begin > (int64_t(1) << 31) - K) return DUST_ERR_RANGE;
+    if ((flags & DUST_ANTITHETIC) && ((K & 1) || (draw_begin & 1))) return DUST_ERR_INVALID_ARG;
+    if (!finite(sigma) || sigma == 0.0f) return DUST_ERR_INVALID_ARG;
+    if (!finite(gamma) || std::fabs(gamma) > 1.0f || !finite(scale)) return DUST_ERR_INVALID_ARG;
+    dust_status st = counter_ok(T, d);
+    if (st != DUST_OK) return st;
+    if (T > 0 && (n_seq < 1 || n_seq > T)) return DUST_ERR_INVALID_ARG;
+    if (V * d == 0) return DUST_OK;
+    if (!gE) return DUST_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool acc = (flags & DUST_ACCUMULATE) != 0;
+    if (T == 0) return acc ? DUST_OK : cuda_status(launch_zero(gE, V * d, s));
+    if (!ids || !delta || !seq_offsets) return DUST_ERR_INVALID_ARG;
+    size_t need = 0;
+    dust_estimate_gE_workspace(&need, T, d, V, K);
+    if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
+        return DUST_ERR_WORKSPACE;
+    char* ws = static_cast<char*>(workspace);
+    unsigned int* sync = reinterpret_cast<unsigned int*>(ws);
+    ws += kSyncBytes;
+    ScanBuffers b = scan_carve(ws, K, T);
+    ws += a256(scan_workspace_bytes(K, T));
+    float* g = reinterpret_cast<float*>(ws);
+    ws += a256(sizeof(float) * static_cast<size_t>(T) * static_cast<size_t>(d));
+    const float coef = static_cast<float>(-1.0 / (static_cast<double>(K) * sigma));
+    if (cudaMemsetAsync(sync, 0, kSyncBytes, s) != cudaSuccess) return DUST_ERR_CUDA;
+    cudaError_t e = launch_scan(delta, K, T, seq_offsets, n_seq, gamma,
+                                (flags & DUST_CENTER) != 0, b, s, sync);
+    if (e == cudaSuccess)
+        e = launch_weight(b, true, K, T, d, seed, static_cast<int>(kind), draw_begin, coef,
+                          (flags & DUST_ANTITHETIC) != 0, g, 0, s);
+    if (e == cudaSuccess) e = launch_scatter_gE(g, 0, ids, T, d, V, scale, acc, gE, ws, s);
+    return cuda_status(e);
+}
+
 dust_status dust_credit_scan_workspace(size_t* bytes, int64_t K, int64_t T) {
     if (!bytes || K < 1 || T < 0) return DUST_ERR_INVALID_ARG;
     if (K > DUST_MAX_DRAWS) return DUST_ERR_RANGE;

@@ -18,7 +18,7 @@ unsigned int* status_word();
 enum Stage {
     kStageScanLocal, kStageScanCarry, kStageScanFixup, kStageWeight, kStageGemmSimt,
     kStageReduce, kStageGemmTc, kStageFused, kStageNoise, kStageJitter, kStageZero, kStageScore,
-    kStageCount
+    kStageScatter, kStageCount
 };
 
 // Brackets the launches issued during its lifetime with profiling events
@@ -164,6 +164,14 @@ cudaError_t launch_fused(const ScanBuffers& b, const void* X, int64_t K, int64_t
 // delta[k][t] = <g[t], dO[k][t]> (local scores as loss changes), rows of d.
 cudaError_t launch_local_score(const void* g, int g_bf16, const void* dO, int o_bf16, int64_t K,
                                int64_t T, int64_t d, float* out, cudaStream_t s);
+
+// Embedding reassembly gE[v] = scale * sum over tokens with id v of g[t]
+// (deterministic 64-bit fixed-point accumulation, k_scatter.cu); the
+// workspace (256-byte aligned, scatter_workspace_bytes) is cleared here.
+size_t scatter_workspace_bytes(int64_t V, int64_t d);
+cudaError_t launch_scatter_gE(const void* g, int g_bf16, const int32_t* ids, int64_t T,
+                              int64_t d, int64_t V, float scale, bool accumulate, float* gE,
+                              void* workspace, cudaStream_t s);
 
 // Fill gW with zeros (T == 0) unless accumulating.
 cudaError_t launch_zero(float* p, int64_t n, cudaStream_t s);

@@ -16,7 +16,7 @@ namespace {
 const char* const kStageNames[kStageCount] = {"scan_local", "scan_carry", "scan_fixup", "weight",
                                               "gemm_simt",  "reduce",     "gemm_tc",    "fused",
                                               "noise",      "jitter",     "zero",
-                                              "score"};
+                                              "score",      "scatter"};
 constexpr int kMaxRecords = 65536;
 
 struct Rec {
