@@ -180,14 +180,15 @@ dust_status dust_local_score(const void* g, dust_dtype g_dtype, const void* delt
  *             dust_last_error report DUST_ERR_INVALID_ARG.
  *   gE        device f32 [V][d]; overwritten, or accumulated into with
  *             DUST_ACCUMULATE (the only flag).
- *   workspace device, >= dust_scatter_gE_workspace(V, d) bytes, 256-byte
- *             aligned (about 8 V d bytes); contents on entry are ignored.
+ *   workspace device, >= dust_scatter_gE_workspace(T, V, d) bytes, 256-byte
+ *             aligned (about 8 V d + 4 T + 8 V bytes); contents on entry are
+ *             ignored.
  * Deterministic whatever the order in which tokens arrive: sums are kept in
  * 64-bit fixed point with a step of 2^-s chosen per call so that
  * max|g| * (largest count of one id) * 2^s < 2^61; each term is rounded once
  * to that step, and the result is rounded to fp32 at the end.
  */
-dust_status dust_scatter_gE_workspace(size_t* bytes, int64_t V, int64_t d);
+dust_status dust_scatter_gE_workspace(size_t* bytes, int64_t T, int64_t V, int64_t d);
 dust_status dust_scatter_gE(const void* g, dust_dtype g_dtype, const int32_t* ids, int64_t T,
                             int64_t d, int64_t V, float scale, uint32_t flags, float* gE,
                             void* workspace, size_t ws_bytes, void* stream);

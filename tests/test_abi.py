@@ -134,7 +134,7 @@ def test_packed_signs_accepted_where_values_are(L):
 def test_scatter_and_embedding_estimator_validation(L):
     fake = C.c_void_p(1 << 20)
     n = C.c_size_t(0)
-    assert L.dust_scatter_gE_workspace(C.byref(n), 4096, 512) == dust.OK
+    assert L.dust_scatter_gE_workspace(C.byref(n), 16384, 4096, 512) == dust.OK
     assert n.value >= 8 * 4096 * 512
     assert L.dust_scatter_gE(fake, dust.U32, fake, 8, 4, 4, C.c_float(1.0), 0, fake, fake,
                              1 << 30, NULL) == dust.ERR_INVALID_ARG

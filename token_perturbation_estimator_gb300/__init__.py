@@ -65,7 +65,7 @@ def _signatures():
         "dust_credit_scan_noalloc_capacity": (SZ, []),
         "dust_credit_scan_noalloc": (i32, [P, i64, i64, P, i64, f32, u32, P, P]),
         "dust_local_score": (i32, [P, i32, P, i32, i64, i64, i64, P, P]),
-        "dust_scatter_gE_workspace": (i32, [PSZ, i64, i64]),
+        "dust_scatter_gE_workspace": (i32, [PSZ, i64, i64, i64]),
         "dust_scatter_gE": (i32, [P, i32, P, i64, i64, i64, f32, u32, P, P, SZ, P]),
         "dust_estimate_gE_workspace": (i32, [PSZ, i64, i64, i64, i64]),
         "dust_estimate_gE": (i32, [P, i64, i64, P, i64, i64, P, i64, u64, i32, i64, f32, f32,
@@ -177,7 +177,7 @@ def dust_scatter_gE(g, ids, V, scale=1.0, flags=0, gE=None, workspace=None, stre
     if gE is None:
         gE = torch.empty((V, d), dtype=torch.float32, device=g.device)
     n = C.c_size_t(0)
-    _check(lib().dust_scatter_gE_workspace(C.byref(n), V, d), "dust_scatter_gE_workspace")
+    _check(lib().dust_scatter_gE_workspace(C.byref(n), T, V, d), "dust_scatter_gE_workspace")
     if workspace is None:
         workspace = _workspace(n.value, g.device)
     _check(lib().dust_scatter_gE(_ptr(g), _dtype_code(g), _ptr(ids), T, d, V, float(scale),

@@ -185,9 +185,9 @@ dust_status dust_local_score(const void* g, dust_dtype g_dtype, const void* delt
                                           K, T, d, delta, static_cast<cudaStream_t>(stream)));
 }
 
-dust_status dust_scatter_gE_workspace(size_t* bytes, int64_t V, int64_t d) {
-    if (!bytes || V < 0 || d < 0) return DUST_ERR_INVALID_ARG;
-    *bytes = a256(scatter_workspace_bytes(V, d));
+dust_status dust_scatter_gE_workspace(size_t* bytes, int64_t T, int64_t V, int64_t d) {
+    if (!bytes || T < 0 || V < 0 || d < 0) return DUST_ERR_INVALID_ARG;
+    *bytes = a256(scatter_workspace_bytes(T, V, d));
     return DUST_OK;
 }
 
@@ -207,7 +207,7 @@ dust_status dust_scatter_gE(const void* g, dust_dtype g_dtype, const int32_t* id
     if (T == 0) return acc ? DUST_OK : cuda_status(launch_zero(gE, V * d, s));
     if (!g || !ids) return DUST_ERR_INVALID_ARG;
     size_t need = 0;
-    dust_scatter_gE_workspace(&need, V, d);
+    dust_scatter_gE_workspace(&need, T, V, d);
     if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
         return DUST_ERR_WORKSPACE;
     return cuda_status(launch_scatter_gE(g, g_dtype == DUST_BF16, ids, T, d, V, scale, acc, gE,
@@ -220,7 +220,7 @@ dust_status dust_estimate_gE_workspace(size_t* bytes, int64_t T, int64_t d, int6
     if (K > DUST_MAX_DRAWS) return DUST_ERR_RANGE;
     *bytes = kSyncBytes + a256(scan_workspace_bytes(K, T)) +
              a256(sizeof(float) * static_cast<size_t>(T) * static_cast<size_t>(d)) +
-             a256(scatter_workspace_bytes(V, d));
+             a256(scatter_workspace_bytes(T, V, d));
     return DUST_OK;
 }
 

@@ -168,7 +168,7 @@ cudaError_t launch_local_score(const void* g, int g_bf16, const void* dO, int o_
 // Embedding reassembly gE[v] = scale * sum over tokens with id v of g[t]
 // (deterministic 64-bit fixed-point accumulation, k_scatter.cu); the
 // workspace (256-byte aligned, scatter_workspace_bytes) is cleared here.
-size_t scatter_workspace_bytes(int64_t V, int64_t d);
+size_t scatter_workspace_bytes(int64_t T, int64_t V, int64_t d);
 cudaError_t launch_scatter_gE(const void* g, int g_bf16, const int32_t* ids, int64_t T,
                               int64_t d, int64_t V, float scale, bool accumulate, float* gE,
                               void* workspace, cudaStream_t s);
