@@ -59,6 +59,8 @@ def lib():
             "dust_oracle_jitter": (None, [P, i64, i64, i64, u64, i32, i64, f64, u32]),
             "dust_oracle_local_score": (None, [P, P, i64, i64, i64, P]),
             "dust_oracle_scatter_gE": (i64, [P, P, i64, i64, i64, f64, P]),
+            "dust_oracle_forward_jitter": (None, [P, P, i64, i64, i64, u64, i32, i64, i64, f64,
+                                                  u32, i32, P]),
             "dust_oracle_planted_delta": (None, [P, P, P, i64, i64, i64, u64, i32, i64, f64,
                                                  f64, u32]),
         }
@@ -218,6 +220,21 @@ def jitter(y, seed, kind, draw, sigma, flags=0):
     T, d_out = y.shape
     lib().dust_oracle_jitter(_p(y), d_out, T, d_out, seed, kind, draw, float(sigma), flags)
     return y
+
+
+def forward_jitter(X, W, seed, kind, draw_begin, n_draws, sigma, flags=0, clean=False):
+    """y = X W^T and y + sigma a^(draw_begin + k) for k < n_draws, stacked
+    [clean + n_draws][T][d_out] (slice 0 = y when clean)."""
+    X = _f64(X)
+    W = _f64(W)
+    T, d_in = X.shape
+    d_out = W.shape[0]
+    assert W.shape == (d_out, d_in)
+    c = 1 if clean else 0
+    out = np.empty((c + n_draws, T, d_out), dtype=np.float64)
+    lib().dust_oracle_forward_jitter(_p(X), _p(W), T, d_in, d_out, seed, kind, draw_begin,
+                                     n_draws, float(sigma), flags, c, _p(out))
+    return out
 
 
 def scatter_gE(g, ids, V, scale=1.0):

@@ -362,6 +362,29 @@ OR_EXPORT void dust_oracle_jitter(double* y, int64_t ld_y, int64_t T, int64_t d_
             y[t * ld_y + c] += sigma * or_noise_value(kind, seed, draw, t, c, d_out, flags);
 }
 
+/* The jittered forward of a linear layer for several draws from one product
+ * ("Dust: every token is a member of the population", "Perturb the
+ * activations, not the weights": y_t -> y_t + sigma a_t, the jitter added
+ * after the layer's product): y = X W^T, then
+ *   out[clean + k][t][c] = y[t][c] + sigma a_t^(draw_begin + k)[c],
+ * with out[0] = y itself when clean = 1. X [T][d_in], W [d_out][d_in]. */
+OR_EXPORT void dust_oracle_forward_jitter(const double* X, const double* W, int64_t T,
+                                          int64_t d_in, int64_t d_out, uint64_t seed,
+                                          int32_t kind, int64_t draw_begin, int64_t n_draws,
+                                          double sigma, uint32_t flags, int32_t clean,
+                                          double* out) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t c = 0; c < d_out; ++c) {
+            double y = 0.0;
+            for (int64_t j = 0; j < d_in; ++j) y += X[t * d_in + j] * W[c * d_in + j];
+            if (clean) out[t * d_out + c] = y;
+            for (int64_t k = 0; k < n_draws; ++k)
+                out[((clean + k) * T + t) * d_out + c] =
+                    y + sigma * or_noise_value(kind, seed, draw_begin + k, t, c, d_out, flags);
+        }
+}
+
 /* Embedding reassembly ("Dust: every token is a member of the population",
  * "What the released code actually does", step 7: "a scatter-add for an
  * embedding"): the error estimate of token t adds into the row of its token
