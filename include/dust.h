@@ -150,6 +150,34 @@ dust_status dust_jitter_apply(void* y, dust_dtype y_dtype, int64_t ld_y, int64_t
                               int64_t draw, float sigma, uint32_t flags, void* stream);
 
 /*
+ * dust_forward_jitter — the jittered forward of a linear layer for several
+ * draws at once: the product y = X W^T is formed once on the tensor cores
+ * and each draw's output y + sigma * a_t^(draw) is written from it ("Dust:
+ * every token is a member of the population", section "Perturb the
+ * activations, not the weights": each population member runs the layer with
+ * its own jitter on the output; split form of "Scaling To Unfathomable
+ * Depth", section "Kernel Recipes"):
+ *   Y[s][t][c] = y[t][c]                                   s < clean
+ *   Y[s][t][c] = y[t][c] + sigma * a_t^(draw_begin + k)[c]  s = clean + k
+ * y is accumulated in fp32 from bf16 products; each output is rounded once
+ * to bf16 (nearest even) after the jitter is added in fp32.
+ *   X      device, bf16 [T][d_in] row-major.   W  device, bf16 [d_out][d_in].
+ *   Y      device, bf16 [clean + n_draws][T][d_out], written (not read).
+ *          X, W, Y 16-byte aligned; d_in > 0 and d_out multiples of 8
+ *          (else DUST_ERR_UNSUPPORTED). Caller owns all three.
+ *   kind   DUST_NOISE_RADEMACHER, DUST_NOISE_GAUSSIAN or
+ *          DUST_NOISE_RADEMACHER_PACKED; flags 0 or DUST_ANTITHETIC.
+ *   clean  0 or 1; n_draws in [0, DUST_MAX_DRAWS]; draw_begin >= 0 with
+ *          draw_begin + n_draws <= 2^31; T * d_out <= 2^32 (DUST_ERR_RANGE).
+ * Asynchronous on `stream`; a bounded device wait that runs out is reported
+ * by dust_last_error as DUST_ERR_TIMEOUT.
+ */
+dust_status dust_forward_jitter(const void* X, const void* W, int64_t T, int64_t d_in,
+                                int64_t d_out, uint64_t seed, dust_noise_kind kind,
+                                int64_t draw_begin, int64_t n_draws, float sigma,
+                                uint32_t flags, int32_t clean, void* Y, void* stream);
+
+/*
  * dust_local_score — loss changes of draws scored locally: for blocks whose
  * output does not reach the loss (attention internals), each jittered draw k
  * is scored at token s against the block output's estimated error ("Dust:

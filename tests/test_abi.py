@@ -154,3 +154,33 @@ def test_scatter_and_embedding_estimator_validation(L):
     assert L.dust_estimate_gE(fake, 8, 4, fake, 4, 4, fake, 1, 0, dust.RAW_WORDS, 0,
                               C.c_float(1.0), C.c_float(0.0), C.c_float(1.0), 0, fake, fake,
                               1 << 30, NULL) == dust.ERR_INVALID_ARG
+
+
+def test_forward_jitter_validation(L):
+    """Argument checks of dust_forward_jitter that return before any launch."""
+    fake = C.c_void_p(1 << 20)
+    odd = C.c_void_p((1 << 20) + 8)  # not 16-byte aligned
+    f = C.c_float
+
+    def call(X=fake, W=fake, T=64, d_in=64, d_out=64, kind=dust.GAUSSIAN, draw_begin=0,
+             n_draws=4, sigma=f(1e-3), flags=0, clean=1, Y=fake):
+        return L.dust_forward_jitter(X, W, T, d_in, d_out, 7, kind, draw_begin, n_draws, sigma,
+                                     flags, clean, Y, NULL)
+
+    assert call(kind=dust.RAW_WORDS) == dust.ERR_INVALID_ARG
+    assert call(kind=9) == dust.ERR_INVALID_ARG
+    assert call(flags=dust.CENTER) == dust.ERR_INVALID_ARG
+    assert call(clean=2) == dust.ERR_INVALID_ARG
+    assert call(T=-1) == dust.ERR_INVALID_ARG
+    assert call(sigma=f(float("nan"))) == dust.ERR_INVALID_ARG
+    assert call(n_draws=8193) == dust.ERR_RANGE
+    assert call(draw_begin=(1 << 31) - 2) == dust.ERR_RANGE
+    assert call(T=1 << 27, d_out=64) == dust.ERR_RANGE  # T d_out > 2^32
+    assert call(d_in=12) == dust.ERR_UNSUPPORTED
+    assert call(d_out=20) == dust.ERR_UNSUPPORTED
+    assert call(d_in=0) == dust.ERR_UNSUPPORTED
+    assert call(Y=odd) == dust.ERR_UNSUPPORTED
+    assert call(Y=NULL) == dust.ERR_INVALID_ARG
+    # nothing to write: OK without touching the device
+    assert call(T=0, X=NULL, Y=NULL) == dust.OK
+    assert call(n_draws=0, clean=0, X=NULL, W=NULL, Y=NULL) == dust.OK

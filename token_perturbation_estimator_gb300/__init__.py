@@ -7,6 +7,7 @@ device memory and streams. There is no fallback: if the library is missing
 the import of a function raises.
 
 Functions keep the C names: ``dust_noise``, ``dust_jitter_apply``,
+``dust_forward_jitter``,
 ``dust_credit_scan``, ``dust_error_estimate``, ``dust_estimate_gW``,
 ``dust_estimate_gW_host``, ``dust_last_error`` (plus the workspace queries).
 """
@@ -64,6 +65,8 @@ def _signatures():
         "dust_last_error": (i32, [P]),
         "dust_credit_scan_noalloc_capacity": (SZ, []),
         "dust_credit_scan_noalloc": (i32, [P, i64, i64, P, i64, f32, u32, P, P]),
+        "dust_forward_jitter": (i32, [P, P, i64, i64, i64, u64, i32, i64, i64, f32, u32, i32,
+                                      P, P]),
         "dust_local_score": (i32, [P, i32, P, i32, i64, i64, i64, P, P]),
         "dust_scatter_gE_workspace": (i32, [PSZ, i64, i64, i64]),
         "dust_scatter_gE": (i32, [P, i32, P, i64, i64, i64, f32, u32, P, P, SZ, P]),
@@ -152,6 +155,29 @@ def dust_jitter_apply(y, seed, kind, draw, sigma, flags=0, stream=None):
                                    draw, float(sigma), flags, _stream(stream)),
            "dust_jitter_apply")
     return y
+
+
+def dust_forward_jitter(X, W, seed, kind, draw_begin, n_draws, sigma, flags=0, clean=False,
+                        Y=None, stream=None):
+    """X: CUDA bf16 [T, d_in]; W: CUDA bf16 [d_out, d_in]; returns Y bf16
+    [clean + n_draws, T, d_out]: X W^T, then X W^T + sigma a^(draw_begin + k)."""
+    import torch
+    _need_cuda(X, W, Y)
+    T, d_in = X.shape
+    d_out = W.shape[0]
+    if W.dim() != 2 or W.shape[1] != d_in:
+        raise ValueError("W must be [d_out, d_in] matching X [T, d_in]")
+    c = 1 if clean else 0
+    if Y is None:
+        Y = torch.empty((c + n_draws, T, d_out), dtype=torch.bfloat16, device=X.device)
+    if X.dtype != torch.bfloat16 or W.dtype != torch.bfloat16 or Y.dtype != torch.bfloat16:
+        raise ValueError("X, W and Y must be bf16")
+    if tuple(Y.shape) != (c + n_draws, T, d_out):
+        raise ValueError("Y must be [clean + n_draws, T, d_out]")
+    _check(lib().dust_forward_jitter(_ptr(X), _ptr(W), T, d_in, d_out, seed, kind, draw_begin,
+                                     n_draws, float(sigma), flags, c, _ptr(Y), _stream(stream)),
+           "dust_forward_jitter")
+    return Y
 
 
 def dust_local_score(g, delta_o, out=None, stream=None):

@@ -172,6 +172,30 @@ dust_status dust_jitter_apply(void* y, dust_dtype y_dtype, int64_t ld_y, int64_t
                                      static_cast<cudaStream_t>(stream)));
 }
 
+dust_status dust_forward_jitter(const void* X, const void* W, int64_t T, int64_t d_in,
+                                int64_t d_out, uint64_t seed, dust_noise_kind kind,
+                                int64_t draw_begin, int64_t n_draws, float sigma,
+                                uint32_t flags, int32_t clean, void* Y, void* stream) {
+    if (T < 0 || d_in < 0 || d_out < 0 || draw_begin < 0 || n_draws < 0) return DUST_ERR_INVALID_ARG;
+    if (clean != 0 && clean != 1) return DUST_ERR_INVALID_ARG;
+    if (!value_kind(kind)) return DUST_ERR_INVALID_ARG;
+    if (flags & ~DUST_ANTITHETIC) return DUST_ERR_INVALID_ARG;
+    if (!finite(sigma)) return DUST_ERR_INVALID_ARG;
+    if (n_draws > DUST_MAX_DRAWS) return DUST_ERR_RANGE;
+    if (draw_begin > (int64_t(1) << 31) - n_draws) return DUST_ERR_RANGE;
+    dust_status st = counter_ok(T, d_out);
+    if (st != DUST_OK) return st;
+    if (d_in == 0 || d_in % 8 != 0 || d_out % 8 != 0) return DUST_ERR_UNSUPPORTED;
+    if (T * d_out * (clean + n_draws) == 0) return DUST_OK;
+    if (!X || !W || !Y) return DUST_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(W) |
+         reinterpret_cast<uintptr_t>(Y)) % 16 != 0)
+        return DUST_ERR_UNSUPPORTED;
+    return cuda_status(launch_forward(X, W, T, d_in, d_out, seed, static_cast<int>(kind),
+                                      draw_begin, n_draws, sigma, (flags & DUST_ANTITHETIC) != 0,
+                                      clean, Y, static_cast<cudaStream_t>(stream)));
+}
+
 dust_status dust_local_score(const void* g, dust_dtype g_dtype, const void* delta_o,
                              dust_dtype o_dtype, int64_t K, int64_t T, int64_t d,
                              float* delta, void* stream) {

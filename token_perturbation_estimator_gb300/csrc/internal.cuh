@@ -18,7 +18,7 @@ unsigned int* status_word();
 enum Stage {
     kStageScanLocal, kStageScanCarry, kStageScanFixup, kStageWeight, kStageGemmSimt,
     kStageReduce, kStageGemmTc, kStageFused, kStageNoise, kStageJitter, kStageZero, kStageScore,
-    kStageScatter, kStageCount
+    kStageScatter, kStageForward, kStageCount
 };
 
 // Brackets the launches issued during its lifetime with profiling events
@@ -113,6 +113,12 @@ cudaError_t launch_noise(void* out, int out_kind /*0 f32, 1 bf16, 2 u32*/, uint6
 cudaError_t launch_jitter(void* y, int y_bf16, int64_t ld_y, int64_t T, int64_t d_out,
                           uint64_t seed, int kind, int64_t draw, float sigma, uint32_t flags,
                           cudaStream_t s);
+// Jittered forward (k_forward.cu): Y[s] = X W^T (s < clean) and
+// X W^T + sigma a^(draw_begin + s - clean); bf16 X [T][d_in], W [d_out][d_in],
+// Y [clean + n_draws][T][d_out]; d_in, d_out multiples of 8, 16-byte aligned.
+cudaError_t launch_forward(const void* X, const void* W, int64_t T, int64_t d_in, int64_t d_out,
+                           uint64_t seed, int kind, int64_t draw_begin, int64_t n_draws,
+                           float sigma, bool anti, int clean, void* Y, cudaStream_t s);
 
 // Centring + chunk-local scan + chunk carries. After it, r holds chunk-local
 // values; the true r is r[t][i] + P[t] * carry[t / kScanChunk][i].

@@ -16,7 +16,7 @@ namespace {
 const char* const kStageNames[kStageCount] = {"scan_local", "scan_carry", "scan_fixup", "weight",
                                               "gemm_simt",  "reduce",     "gemm_tc",    "fused",
                                               "noise",      "jitter",     "zero",
-                                              "score",      "scatter"};
+                                              "score",      "scatter",    "forward"};
 constexpr int kMaxRecords = 65536;
 
 struct Rec {

@@ -201,5 +201,40 @@ __host__ __device__ constexpr uint32_t idesc_bf16_mn(uint32_t M, uint32_t N) {
            | ((M >> 4) << 24);  // M / 16
 }
 
+// As idesc_bf16_mn with both operands K-major (the reduction dimension
+// contiguous in memory, e.g. X [T][d_in] and W [d_out][d_in] row-major).
+__host__ __device__ constexpr uint32_t idesc_bf16_k(uint32_t M, uint32_t N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// ---------------------------------------------------------------- TMA stores
+
+// Shared -> global tile store through a 3-D tensor map, tracked by the
+// issuing thread's bulk-async groups.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int32_t x,
+                                             int32_t y, int32_t z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until at most N of this thread's committed bulk groups still read
+// their shared-memory source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Wait until every committed bulk group of this thread has completed.
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 }  // namespace tc
 }  // namespace dust
