@@ -52,8 +52,10 @@ def parse_args(argv=None):
                    help="extra dust_estimate_gW flags (e.g. force a path)")
     p.add_argument("--workload", default="mlp_up",
                    choices=["mlp_up", "toy", "qkv", "square_r", "square_g", "square_rp",
-                            "sweep"],
-                   help="mlp_up is the measured headline; the others are for study")
+                            "sweep", "forward_g", "forward_r", "forward_rp"],
+                   help="mlp_up is the measured headline; forward_* time the jittered "
+                        "forward (8 draws + the clean output) of the same layer; the "
+                        "others are for study")
     return p.parse_args(argv)
 
 
@@ -178,7 +180,12 @@ WORKLOADS = {
     "square_g": "square_4096_T32768_K64_gaussian",
     "square_rp": "square_4096_T32768_K64_rademacher_packed",
     "sweep": "sweep_12x4_sites_T65536_K32_gaussian",
+    "forward_g": "forward_mlp_up_512to2048_T16384_8draws+clean_gaussian",
+    "forward_r": "forward_mlp_up_512to2048_T16384_8draws+clean_rademacher",
+    "forward_rp": "forward_mlp_up_512to2048_T16384_8draws+clean_rademacher_packed",
 }
+FORWARD_KIND = {"forward_g": 1, "forward_r": 0, "forward_rp": 3}
+FORWARD_METRIC = "Dust jittered-forward token-draws/s at 1 GB300 (y = XW^T once, y + sigma a per draw)"
 
 
 def workload_sites(name):
@@ -269,10 +276,37 @@ def load_peaks():
                 "fallback": True}
 
 
+def forward_roofline(ms, T, d_in, d_out, K, clean, kind, peaks):
+    """Roofline of one jittered forward launch (k_forward):
+      algorithmic bytes = 2 (T d_in + d_out d_in + (clean + K) T d_out): X and
+        W read once, every output slice written once (bf16);
+      Gaussian: 2 XU ops per element-draw (K T d_out), as for the weighting
+        kernel -> bound "alu" against 16 XU ops/clk/SM x 152 SMs x 2.07 GHz
+        when that fraction is the larger one;
+      signs: bound "hbm" against the measured copy bandwidth."""
+    s = ms / 1000.0
+    byts = 2.0 * (T * d_in + d_out * d_in + (clean + K) * T * d_out)
+    hbm = peaks.get("hbm_gbs", 6800.0) * 1e9
+    out = {"bound": "hbm", "achieved": byts / s / 1e9, "peak": hbm / 1e9, "unit": "GB/s",
+           "frac": byts / s / hbm, "traffic": None, "kernel": "forward",
+           "algorithmic_per_step": byts,
+           "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)"}
+    if kind == 1:
+        ops, peak = 2.0 * K * T * d_out, 16 * 152 * 2.07e9
+        if ops / s / peak > out["frac"]:
+            out = {"bound": "alu", "achieved": ops / s / 1e9, "peak": peak / 1e9,
+                   "unit": "Gop/s", "frac": ops / s / peak, "traffic": None,
+                   "kernel": "forward", "algorithmic_per_step": ops,
+                   "hbm_frac": byts / s / hbm,
+                   "peak_source": "derived: 16 XU ops/clk/SM x 152 SMs x 2.07 GHz"}
+    return out
+
+
 KERNEL_SOURCES = {
     "weight": ["k_weight.cu", "noise.cuh", "internal.cuh"],
     "gemm_tc": ["k_gemm_tc.cu", "tc_common.cuh", "internal.cuh"],
     "fused": ["k_fused.cu", "noise.cuh", "tc_common.cuh", "internal.cuh"],
+    "forward": ["k_forward.cu", "noise.cuh", "tc_common.cuh", "internal.cuh"],
 }
 
 
@@ -567,11 +601,209 @@ def run_gb300(args):
     return 0
 
 
+# ----------------------------------------------------- jittered forward ----
+
+def forward_inputs():
+    import workloads as wl
+    w = wl.MLP_UP
+    X = wl.to_bf16_exact(wl.make_X(w))
+    W = wl.to_bf16_exact(wl.make_W(w))
+    return w, X, W
+
+
+def cpu_forward_rate(kind, target_s):
+    """The fp64 oracle's jittered forward on a bounded sample: the first Ts
+    tokens of the layer (all channels, all draws, the clean slice), Ts grown
+    until the sample takes about target_s."""
+    import numpy as np
+    import oracle
+    w, X, W = forward_inputs()
+
+    def run(Ts):
+        t0 = time.perf_counter()
+        oracle.forward_jitter(X[:Ts], W, w.seed, kind, 0, w.K, w.sigma, clean=True)
+        return time.perf_counter() - t0
+
+    t1 = run(64)
+    Ts = int(max(64, min(w.T, 64 * round(target_s / max(t1, 1e-3)))))
+    dt = run(Ts)
+    return {"value": w.K * Ts / dt, "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": "first %d of %d tokens, %d draws + clean, all %d channels; %.1f s"
+                      % (Ts, w.T, w.K, w.d_out, dt)}
+
+
+def run_forward_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    w, X, W = forward_inputs()
+    kind = FORWARD_KIND[args.workload]
+    Ts = 128  # one token tile per step: the oracle's full path on it
+
+    def step():
+        oracle.forward_jitter(X[:Ts], W, w.seed, kind, 0, w.K, w.sigma, clean=True)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = w.K * Ts * args.steps / dt
+    line = {
+        "impl": "reference", "metric": FORWARD_METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOADS[args.workload], "sample_tokens_per_step": Ts},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": "%d tokens per step, all draws and channels" % Ts},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_forward(args):
+    """One step = one dust_forward_jitter call: y = X W^T of the MLP
+    up-projection layer (16384 tokens, 512 -> 2048, bf16) and its 8 jittered
+    outputs plus the clean one, all written to HBM."""
+    import torch
+    rank, world, local = dist_env()
+    from __graft_entry__ import build
+    build()
+    import token_perturbation_estimator_gb300 as dust
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl", device_id=dev)
+        pg = tdist
+
+    def max_over_ranks(x):
+        if pg is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+
+    kind = FORWARD_KIND[args.workload]
+    w, Xn, Wn = forward_inputs()
+    K, T = w.K, w.T
+    X = torch.from_numpy(Xn).to(dev).to(torch.bfloat16)
+    W = torch.from_numpy(Wn).to(dev).to(torch.bfloat16)
+    Y = torch.empty((K + 1, T, w.d_out), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    units = K * T
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)  # 256 MB > L2
+
+    def step():
+        dust.dust_forward_jitter(X, W, w.seed, kind, 0, K, w.sigma, clean=True, Y=Y,
+                                 stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    st = dust.dust_last_error()
+    if st != dust.OK:
+        raise RuntimeError("device status after warm-up: " + dust.status_string(st))
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for k in range(args.steps):
+            flush.zero_()
+            starts[k].record(stream)
+            step()
+            ends[k].record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms_total = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+    value, ms_per_step = aggregate(units, ms_total, args.steps, world, max_over_ranks)
+
+    dust.dust_profile_enable(True)
+    dust.dust_profile_read()
+    for k in range(args.steps):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    prof = dust.dust_profile_read()
+    dust.dust_profile_enable(False)
+    launches, fwd_ms = prof["forward"]
+    roof = forward_roofline(fwd_ms / launches, T, w.d_in, w.d_out, K, 1, kind, load_peaks())
+    roof["launches_per_step"] = launches / args.steps
+    roof["traffic"] = traffic_from_profiles("forward")
+
+    # end to end: X and W from pinned host memory, every output slice back
+    Xh, Wh = X.cpu().pin_memory(), W.cpu().pin_memory()
+    Yh = torch.empty(tuple(Y.shape), dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step():
+        X.copy_(Xh, non_blocking=True)
+        W.copy_(Wh, non_blocking=True)
+        step()
+        Yh.copy_(Y, non_blocking=True)
+        stream.synchronize()
+
+    n_e2e = max(3, min(args.e2e_steps, 50))
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        e2e_step()
+    e2e_s = max_over_ranks(time.perf_counter() - t0)
+    e2e_value = world * units * n_e2e / e2e_s
+    if not torch.equal(Yh, Y.cpu()):
+        raise RuntimeError("host copy of the outputs disagrees with the device")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_forward_rate(kind, args.cpu_seconds)
+    if rank == 0:
+        cfg = {"workload": WORKLOADS[args.workload], "d_in": w.d_in, "d_out": w.d_out, "T": T,
+               "draws": K, "clean_slice": True, "sigma": w.sigma,
+               "noise": {0: "rademacher", 1: "gaussian", 3: "rademacher_packed"}[kind],
+               "x_dtype": "bf16", "y_dtype": "bf16",
+               "parallelism": "replicas" if world > 1 else "single",
+               "l2": "flushed (256 MB write) between timed steps"}
+        line = {
+            "metric": FORWARD_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": cfg, "roofline": roof, "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT,
+                    "h2d_bytes_per_step": (Xh.numel() + Wh.numel()) * 2,
+                    "d2h_bytes_per_step": Yh.numel() * 2},
+            "gpu_launches": int(launches),
+            "clocks": clocks.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
+    forward = args.workload.startswith("forward_")
     if args.impl == "reference":
-        return run_reference(args)
-    return run_gb300(args)
+        return run_forward_reference(args) if forward else run_reference(args)
+    return run_forward(args) if forward else run_gb300(args)
 
 
 if __name__ == "__main__":

@@ -45,7 +45,13 @@ namespace {
 #define DUST_FWD_BN 256  // channels per tile (columns of one TMEM accumulator)
 #endif
 #ifndef DUST_FWD_EW
-#define DUST_FWD_EW 16  // epilogue warps
+#define DUST_FWD_EW 24  // epilogue warps
+#endif
+#ifndef DUST_FWD_SUB_G
+#define DUST_FWD_SUB_G 8  // TMEM columns an epilogue thread holds at a time (Gaussian)
+#endif
+#ifndef DUST_FWD_SUB_R
+#define DUST_FWD_SUB_R 16  // (signs)
 #endif
 #ifndef DUST_FWD_DEEP_KSTEPS
 #define DUST_FWD_DEEP_KSTEPS 32  // k-steps from which the deeper ring pays
@@ -60,20 +66,19 @@ constexpr int kThreads = 64 + 32 * kEW;
 // warp (short reductions, where the stores dominate), or 3 stages and 2
 // buffers (long reductions, where the tensor cores need the deeper ring).
 constexpr int kMaxStages = 3;
+template <int KIND> constexpr int sub_cols() { return KIND == 1 ? DUST_FWD_SUB_G : DUST_FWD_SUB_R; }
 constexpr int kABytes = kBM * kBK * 2;
 constexpr int kBBytes = kBN * kBK * 2;
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kBufBytes = 32 * 32 * 2;  // 32 tokens x 32 channels of bf16
-constexpr int kSplitBytes = (2 * kStageBytes + kEW * 3 * kBufBytes) >
-                                    (3 * kStageBytes + kEW * 2 * kBufBytes)
-                                ? 2 * kStageBytes + kEW * 3 * kBufBytes
-                                : 3 * kStageBytes + kEW * 2 * kBufBytes;
+constexpr int kSplitBytes = 3 * kStageBytes + 64 * 1024;  // ring + staging buffers
+constexpr int kPerQuarter = kEW / 4;  // epilogue warps reading one TMEM lane quarter
 constexpr int kChunks = kBN / 32;
 constexpr int kKeyTable = 64;           // per-draw keys kept in shared memory
 constexpr int kSmemBytes = kSplitBytes + kKeyTable * 8 + 256 + 1024;
 static_assert(kBN == 128 || kBN == 256, "two accumulators of kBN columns fit TMEM");
 static_assert(kEW % 4 == 0, "epilogue warps cover the four TMEM lane quarters");
-static_assert(kEW / 4 <= kChunks, "every epilogue warp reads at least one block");
+static_assert(kSplitBytes - 3 * kStageBytes >= kEW * kBufBytes, "a staging buffer per warp");
 static_assert(kStageBytes % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 static_assert(kThreads <= 1024, "one CTA");
@@ -138,33 +143,38 @@ __device__ __forceinline__ uint32_t counter_f(uint32_t n_row, uint32_t nf_row, u
     return ALIGNED ? (nf_row ^ j) : fold16(n_row + j);
 }
 
-// One slice of a 32-channel block: out = bf16(y + ss a) for the channels
-// [c0, c0 + 32) of token t, n_row = t d_out + c0 the block's first counter.
-template <int KIND, bool ALIGNED>
-__device__ __forceinline__ void jitter_block(const float (&y)[32], uint32_t n_row, uint32_t kf0,
-                                             uint32_t kf1, float ss, uint32_t (&pk)[16]) {
-    const uint32_t nf_row = fold16(n_row);
+// Channels [c0 + j0, c0 + j0 + N) of one slice: pk[p] = bf16x2 of y + ss a
+// for the channel pair (j0 + 2p, j0 + 2p + 1). n_row = t d_out + c0 is the
+// counter of the 32-channel block's first channel (nf_row folded); w is the
+// block's hash word (packed signs).
+template <int KIND, bool ALIGNED, int N>
+__device__ __forceinline__ void jitter_sub(const float (&y)[N], uint32_t n_row, uint32_t nf_row,
+                                           int j0, uint32_t kf0, uint32_t kf1, uint32_t w,
+                                           float ss, uint32_t (&pk)[N / 2]) {
     if (KIND == 1) {
 #pragma unroll
-        for (int p = 0; p < 16; ++p) {
-            const uint32_t nf = counter_f<ALIGNED>(n_row, nf_row, 2u * p);
-            float ae, ao;
-            gauss_pair(unit_ff(kf0, nf), unit_ff(kf1, nf), ae, ao);
-            pk[p] = pack_bf16(fmaf(ss, ae, y[2 * p]), fmaf(ss, ao, y[2 * p + 1]));
+        for (int p = 0; p < N / 2; ++p) {
+            // Box-Muller as in gauss_pair, with sigma folded into the radius:
+            // y + (ss rho) cos, y + (ss rho) sin.
+            const uint32_t nf = counter_f<ALIGNED>(n_row, nf_row, j0 + 2u * p);
+            const float sr = ss * neg_radius(unit_ff(kf0, nf));
+            float sn, cs;
+            __sincosf(centred_angle(unit_ff(kf1, nf)), &sn, &cs);
+            pk[p] = pack_bf16(fmaf(sr, cs, y[2 * p]), fmaf(sr, sn, y[2 * p + 1]));
         }
     } else if (KIND == 3) {
-        const uint32_t w = word_ff(kf0, nf_row);  // the block is one 32-channel group
         const uint32_t sb = __float_as_uint(ss);
 #pragma unroll
-        for (int p = 0; p < 16; ++p)
-            pk[p] = pack_bf16(y[2 * p] + __uint_as_float(sb ^ packed_sign_bit(w, 2 * p)),
-                              y[2 * p + 1] + __uint_as_float(sb ^ packed_sign_bit(w, 2 * p + 1)));
+        for (int p = 0; p < N / 2; ++p)
+            pk[p] = pack_bf16(y[2 * p] + __uint_as_float(sb ^ packed_sign_bit(w, j0 + 2 * p)),
+                              y[2 * p + 1] +
+                                  __uint_as_float(sb ^ packed_sign_bit(w, j0 + 2 * p + 1)));
     } else {
         const uint32_t sb = __float_as_uint(ss);
 #pragma unroll
-        for (int p = 0; p < 16; ++p) {
-            const uint32_t s0 = sign_ff(kf0, counter_f<ALIGNED>(n_row, nf_row, 2u * p));
-            const uint32_t s1 = sign_ff(kf0, counter_f<ALIGNED>(n_row, nf_row, 2u * p + 1u));
+        for (int p = 0; p < N / 2; ++p) {
+            const uint32_t s0 = sign_ff(kf0, counter_f<ALIGNED>(n_row, nf_row, j0 + 2u * p));
+            const uint32_t s1 = sign_ff(kf0, counter_f<ALIGNED>(n_row, nf_row, j0 + 2u * p + 1u));
             pk[p] = pack_bf16(y[2 * p] + __uint_as_float(sb ^ s0),
                               y[2 * p + 1] + __uint_as_float(sb ^ s1));
         }
@@ -278,14 +288,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------- epilogue
+        // The work of a tile's lane quarter is kChunks x n_slices items (one
+        // 32-channel block of one slice each), dealt round robin to the
+        // quarter's kPerQuarter warps; the deal continues across tiles so no
+        // warp is always the one with an extra item. An item reloads its y
+        // block from TMEM kSub columns at a time, so that a thread holds few
+        // registers and many warps fit on the SM.
         const int ew = warp - 2;
-        const int q = warp & 3;  // TMEM lane quarter this warp may read
+        const int q = warp & 3;   // TMEM lane quarter this warp may read
+        const int h = ew >> 2;    // this warp's place among the quarter's warps
         const int nbuf = a.nbuf;
         unsigned char* bufs = staging + ew * (nbuf * kBufBytes);
         const uint32_t swz = (lane >> 1) & 3;  // 64-byte swizzle of this lane's row
+        constexpr int kSub = sub_cols<KIND>();
         const int n_slices = a.clean + static_cast<int>(a.n_draws);
+        const int items = kChunks * n_slices;
         uint32_t used = 0;  // staging buffers this warp has filled
         int bi = 0;         // the next one, used % nbuf
+        int rot = 0;        // items dealt before this tile, mod kPerQuarter
         int j = 0;
         for (int64_t tile = blockIdx.x; tile < a.n_tiles; tile += gridDim.x, ++j) {
             const int acc = j & 1;
@@ -299,55 +319,69 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t n0 = (tile % a.n_tn) * kBN;
             const int64_t t = t0 + 32 * q + lane;
             const int32_t row_box = static_cast<int32_t>(t0 + 32 * q);
+            const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16) + acc * kBN;
             // A lane quarter wholly past T has nothing to store (a tensor
             // store is never started outside the tensor).
             const bool rows_live = t0 + 32 * q < a.T;
-            for (int cb = ew >> 2; cb < kChunks; cb += kEW / 4) {
+            int it = h - rot;
+            if (it < 0) it += kPerQuarter;
+            rot = (rot + items) % kPerQuarter;
+            for (; it < items; it += kPerQuarter) {
+                const int cb = it % kChunks;
+                const int s = it / kChunks;
                 const int64_t c0 = n0 + 32 * cb;
-                float y[32];
-                tc::tmem_ld_32x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + acc * kBN + 32 * cb,
-                                  y);
-                if (cb + kEW / 4 >= kChunks) {  // this warp's last read of the accumulator
-                    tc::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(&ctl->tempty[acc]);
-                }
                 if (!rows_live || c0 >= a.d_out) continue;
                 const uint32_t n_row = static_cast<uint32_t>(t * a.d_out + c0);
-                for (int s = 0; s < n_slices; ++s) {
-                    uint32_t pk[16];
-                    if (s < a.clean) {
-#pragma unroll
-                        for (int p = 0; p < 16; ++p) pk[p] = pack_bf16(y[2 * p], y[2 * p + 1]);
-                    } else {
-                        uint32_t kf0, kf1;
-                        float ss;
-                        draw_keys(a, s_keys, s - a.clean, kf0, kf1, ss);
-                        jitter_block<KIND, ALIGNED>(y, n_row, kf0, kf1, ss, pk);
-                    }
-                    unsigned char* buf = bufs + bi * kBufBytes;
-                    bi = (bi + 1 == nbuf) ? 0 : bi + 1;
-                    if (used >= static_cast<uint32_t>(nbuf)) {
-                        if (lane == 0) {
-                            if (nbuf == 3) tc::bulk_wait_read<2>();
-                            else tc::bulk_wait_read<1>();
-                        }
-                        __syncwarp();
-                    }
-                    const uint32_t row = tc::smem_u32(buf) + lane * 64;
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        st_shared_v4(row + ((u ^ swz) << 4), pk[4 * u], pk[4 * u + 1],
-                                     pk[4 * u + 2], pk[4 * u + 3]);
-                    tc::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tc::tma_store_3d(&tmY, buf, static_cast<int32_t>(c0), row_box, s);
-                        tc::bulk_commit();
-                    }
-                    ++used;
+                const uint32_t nf_row = fold16(n_row);
+                const bool clean_slice = s < a.clean;
+                uint32_t kf0 = 0, kf1 = 0, w = 0;
+                float ss = 0.0f;
+                if (!clean_slice) {
+                    draw_keys(a, s_keys, s - a.clean, kf0, kf1, ss);
+                    if (KIND == 3) w = word_ff(kf0, nf_row);  // one word per 32-channel block
                 }
+                unsigned char* buf = bufs + bi * kBufBytes;
+                bi = (bi + 1 == nbuf) ? 0 : bi + 1;
+                if (used >= static_cast<uint32_t>(nbuf)) {
+                    if (lane == 0) {
+                        if (nbuf == 3) tc::bulk_wait_read<2>();
+                        else if (nbuf == 2) tc::bulk_wait_read<1>();
+                        else tc::bulk_wait_read<0>();
+                    }
+                    __syncwarp();
+                }
+                const uint32_t row = tc::smem_u32(buf) + lane * 64;
+#pragma unroll
+                for (int u = 0; u < 32 / kSub; ++u) {
+                    float y[kSub];
+                    tc::tmem_ld_32xN<kSub>(tq + 32 * cb + kSub * u, y);
+                    uint32_t pk[kSub / 2];
+                    if (clean_slice) {
+#pragma unroll
+                        for (int p = 0; p < kSub / 2; ++p) pk[p] = pack_bf16(y[2 * p], y[2 * p + 1]);
+                    } else {
+                        jitter_sub<KIND, ALIGNED, kSub>(y, n_row, nf_row, kSub * u, kf0, kf1, w,
+                                                        ss, pk);
+                    }
+#pragma unroll
+                    for (int v = 0; v < kSub / 8; ++v) {
+                        const uint32_t piece = u * (kSub / 8) + v;  // 16-byte piece of the row
+                        st_shared_v4(row + ((piece ^ swz) << 4), pk[4 * v], pk[4 * v + 1],
+                                     pk[4 * v + 2], pk[4 * v + 3]);
+                    }
+                }
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tc::tma_store_3d(&tmY, buf, static_cast<int32_t>(c0), row_box, s);
+                    tc::bulk_commit();
+                }
+                ++used;
             }
+            // This warp's reads of the accumulator are done: free it.
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&ctl->tempty[acc]);
         }
         if (lane == 0) tc::bulk_wait_all();
         __syncwarp();
@@ -433,7 +467,8 @@ cudaError_t launch_forward(const void* X, const void* W, int64_t T, int64_t d_in
     fa.n_tiles = fa.n_tn * ((T + kBM - 1) / kBM);
     const bool deep = (d_in + kBK - 1) / kBK >= DUST_FWD_DEEP_KSTEPS;
     fa.stages = deep ? 3 : 2;
-    fa.nbuf = deep ? 2 : 3;
+    const int nbuf = (kSplitBytes - fa.stages * kStageBytes) / (kEW * kBufBytes);
+    fa.nbuf = nbuf > 3 ? 3 : nbuf;
     fa.skey = seed_key(seed);
     fa.draw_begin = draw_begin;
     fa.n_draws = n_draws;

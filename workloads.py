@@ -9,7 +9,8 @@ loss changes), the caller computes the two per-(draw, token) reductions
 Workloads follow the five synthetic configurations measured by this project:
 a toy fp32 layer, an MLP up-projection, a fused QKV projection with credit
 decay, a large square layer (Rademacher and Gaussian), and a 12-layer sweep
-of 48 linear sites. Seeds: estimator 0, X 1, planted error 2, loss noise 3.
+of 48 linear sites. Seeds: estimator 0, X 1, planted error 2, loss noise 3,
+layer weight 4 (the jittered forward).
 """
 from __future__ import annotations
 
@@ -21,7 +22,7 @@ RADEMACHER = 0
 GAUSSIAN = 1
 RADEMACHER_PACKED = 3  # 32 signs per hash word
 
-SEED_EST, SEED_X, SEED_PLANT, SEED_EPS = 0, 1, 2, 3
+SEED_EST, SEED_X, SEED_PLANT, SEED_EPS, SEED_W = 0, 1, 2, 3, 4
 
 
 @dataclass(frozen=True)
@@ -115,6 +116,14 @@ def make_X(w: Workload, seed: int = SEED_X) -> np.ndarray:
         s = rng.uniform(0.5, 2.0, size=w.d_in).astype(np.float32)
         X *= s[None, :]
     return X
+
+
+def make_W(w: Workload, seed: int = SEED_W) -> np.ndarray:
+    """Layer weight W [d_out, d_in] ~ N(0, 1/d_in) as float32 (the jittered
+    forward's second operand; round it to bf16 with `to_bf16_exact`)."""
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal((w.d_out, w.d_in), dtype=np.float32)
+            / np.float32(np.sqrt(w.d_in))).astype(np.float32)
 
 
 def make_dplant(w: Workload, seed: int = SEED_PLANT) -> np.ndarray:
