@@ -347,3 +347,41 @@ def test_sweep_site_full_size_sampled(site):
     want = oracle.gW_entries(X, r, w.d_out, chan, col, w.seed, w.kind, 0, np.float32(w.sigma),
                              1.0, oracle.CENTER)
     assert rel_fro(got[chan, col], want) <= 1e-2
+
+
+DIRECT_CASES = [
+    # T, d_in, d_out, K, kind, flags, x dtype
+    (4096, 512, 2048, 8, 1, dust.CENTER, "bf16"),
+    (1003, 64, 200, 32, 0, dust.CENTER, "bf16"),               # the most draws read directly
+    (1003, 64, 200, 33, 0, dust.CENTER, "bf16"),               # one more: through the scan
+    (517, 64, 96, 65, 1, dust.CENTER, "bf16"),                 # two draw groups
+    (777, 96, 320, 16, 3, dust.CENTER | dust.ANTITHETIC, "bf16"),
+    (300, 40, 72, 6, 1, 0, "f32"),                              # no centring, fp32 path
+    (129, 64, 64, 1, 0, dust.CENTER, "f32"),                    # K = 1: centring is a no-op
+]
+
+
+@pytest.mark.parametrize("T,d_in,d_out,K,kind,flags,xd", DIRECT_CASES)
+def test_gamma_zero_skips_the_scan_bit_for_bit(T, d_in, d_out, K, kind, flags, xd):
+    """With gamma = 0 the credit scan is the identity and dust_estimate_gW
+    centres the loss changes inside the weighting kernel (no scan kernel).
+    The result must equal, bit for bit, the staged path through the scan:
+    dust_credit_scan -> dust_error_estimate -> dust_contract."""
+    import torch
+    dev = cuda()
+    rng = np.random.default_rng(T + K + kind)
+    so = torch.from_numpy(offsets_from_lengths(random_lengths(rng, T, 250))).to(dev)
+    X = torch.from_numpy(rng.standard_normal((T, d_in)).astype(np.float32)).to(dev)
+    if xd == "bf16":
+        X = X.to(torch.bfloat16)
+    delta = torch.from_numpy((0.05 * rng.standard_normal((K, T))).astype(np.float32)).to(dev)
+    seed, draw_begin, sigma, scale = 21, 4, 1e-3, 0.5
+    got = dust.dust_estimate_gW(X, delta, d_out, so, seed, kind, draw_begin, sigma, 0.0, scale,
+                                flags)
+    r = dust.dust_credit_scan(delta, so, 0.0, flags & dust.CENTER)
+    g = dust.dust_error_estimate(r, d_out, seed, kind, draw_begin, sigma,
+                                 flags & dust.ANTITHETIC, g_dtype=X.dtype)
+    want = dust.dust_contract(g, X, scale)
+    torch.cuda.synchronize()
+    assert dust.dust_last_error() == dust.OK
+    assert torch.equal(got, want)

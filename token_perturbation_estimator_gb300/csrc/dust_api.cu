@@ -19,6 +19,10 @@ constexpr uint32_t kKnownFlags = DUST_CENTER | DUST_ANTITHETIC | DUST_ACCUMULATE
 
 size_t a256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// With gamma = 0 and at most this many draws the weighting kernel reads the
+// loss changes itself (one staging group) and no scan kernel runs.
+constexpr int64_t kDirectMaxDraws = 32;
+
 bool finite(float x) { return std::isfinite(x); }
 
 int popcount3(uint32_t f) {
@@ -283,12 +287,17 @@ dust_status dust_estimate_gE(const int32_t* ids, int64_t T, int64_t V, const flo
     float* g = reinterpret_cast<float*>(ws);
     ws += a256(sizeof(float) * static_cast<size_t>(T) * static_cast<size_t>(d));
     const float coef = static_cast<float>(-1.0 / (static_cast<double>(K) * sigma));
-    if (cudaMemsetAsync(sync, 0, kSyncBytes, s) != cudaSuccess) return DUST_ERR_CUDA;
-    cudaError_t e = launch_scan(delta, K, T, seq_offsets, n_seq, gamma,
-                                (flags & DUST_CENTER) != 0, b, s, sync);
+    const bool direct = gamma == 0.0f && K <= kDirectMaxDraws;  // scan = identity
+    const bool center = (flags & DUST_CENTER) != 0;
+    cudaError_t e = cudaSuccess;
+    if (!direct) {
+        if (cudaMemsetAsync(sync, 0, kSyncBytes, s) != cudaSuccess) return DUST_ERR_CUDA;
+        e = launch_scan(delta, K, T, seq_offsets, n_seq, gamma, center, b, s, sync);
+    }
     if (e == cudaSuccess)
         e = launch_weight(b, true, K, T, d, seed, static_cast<int>(kind), draw_begin, coef,
-                          (flags & DUST_ANTITHETIC) != 0, g, 0, s);
+                          (flags & DUST_ANTITHETIC) != 0, g, 0, s, direct ? delta : nullptr,
+                          center);
     if (e == cudaSuccess) e = launch_scatter_gE(g, 0, ids, T, d, V, scale, acc, gE, ws, s);
     return cuda_status(e);
 }
@@ -453,10 +462,16 @@ dust_status estimate(const void* X, dust_dtype x_dtype, int64_t T, int64_t d_in,
     const float coef = static_cast<float>(-1.0 / (static_cast<double>(K) * sigma));
     const bool anti = (flags & DUST_ANTITHETIC) != 0;
 
-    if (cudaMemsetAsync(sync, 0, kSyncBytes, s) != cudaSuccess) return DUST_ERR_CUDA;
-    cudaError_t e = launch_scan(delta, K, T, seq_offsets, n_seq, gamma,
-                                (flags & DUST_CENTER) != 0, b, s, sync);
-    if (e != cudaSuccess) return DUST_ERR_CUDA;
+    // With gamma = 0 the credit scan is the identity (r_t = c_t): the
+    // weighting kernel then centres the loss changes itself and no scan runs.
+    const bool direct = gamma == 0.0f && K <= kDirectMaxDraws && L.path != DUST_PATH_FUSED_TC;
+    const bool center = (flags & DUST_CENTER) != 0;
+    if (!direct) {
+        if (cudaMemsetAsync(sync, 0, kSyncBytes, s) != cudaSuccess) return DUST_ERR_CUDA;
+        if (launch_scan(delta, K, T, seq_offsets, n_seq, gamma, center, b, s, sync) != cudaSuccess)
+            return DUST_ERR_CUDA;
+    }
+    cudaError_t e = cudaSuccess;
     if (L.path == DUST_PATH_FUSED_TC) {
         float* fpart = reinterpret_cast<float*>(ws + L.scan);
         if (x_ready && cudaStreamWaitEvent(s, x_ready, 0) != cudaSuccess) return DUST_ERR_CUDA;
@@ -464,7 +479,7 @@ dust_status estimate(const void* X, dust_dtype x_dtype, int64_t T, int64_t d_in,
                                         draw_begin, coef, anti, scale, acc, gW, fpart, s));
     }
     e = launch_weight(b, true, K, T, d_out, seed, static_cast<int>(kind), draw_begin, coef, anti,
-                      g, L.g_bf16, s);
+                      g, L.g_bf16, s, direct ? delta : nullptr, center);
     if (e != cudaSuccess) return DUST_ERR_CUDA;
     if (x_ready && cudaStreamWaitEvent(s, x_ready, 0) != cudaSuccess) return DUST_ERR_CUDA;
     if (L.path == DUST_PATH_UNFUSED_TC && tc_gemm_supported(g, X, d_in, d_out))

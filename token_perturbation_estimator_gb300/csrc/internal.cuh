@@ -131,9 +131,13 @@ cudaError_t launch_scan_fixup(const ScanBuffers& b, int64_t K, int64_t T, cudaSt
 
 // g[t][c] = coef * sum_i r[t][i] a_t^(draw_begin+i)[c]; with `fix` the scan
 // fix-up is applied while staging r.
+// Rewards from the scan buffers (b.r, plus P and carry when fix), or, when
+// delta is given, straight from the loss changes Delta [K][T] (gamma = 0, where
+// the scan is the identity), centred over the draws when center.
 cudaError_t launch_weight(const ScanBuffers& b, bool fix, int64_t K, int64_t T, int64_t d_out,
                           uint64_t seed, int kind, int64_t draw_begin, float coef,
-                          bool anti, void* g, int g_bf16, cudaStream_t s);
+                          bool anti, void* g, int g_bf16, cudaStream_t s,
+                          const float* delta = nullptr, bool center = false);
 
 // CUDA-core contraction: partial[s][c][j] = sum_{t in slice s} g[t][c] x[t][j]
 // followed by gW = scale * sum_s partial (+ gW).

@@ -71,16 +71,21 @@ __global__ void __launch_bounds__(256) k_scan_local(const float* __restrict__ de
     }
     // Loads are issued in batches of independent registers before they are
     // used, so a thread waits for one memory latency per batch rather than one
-    // per draw (the sum itself stays in draw order).
+    // per draw. The sum's order: each batch of 8 draws summed in draw order,
+    // then the batch sums in order (the weighting kernel's direct path, which
+    // centres without a scan, sums in the same order, so both give the same
+    // bits).
     float mean = 0.0f;
     if (center && K > 1 && t < T) {
         for (int64_t i0 = 0; i0 < K; i0 += 8) {
             float v[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) v[j] = (i0 + j < K) ? delta[(i0 + j) * T + t] : 0.0f;
+            float part = 0.0f;
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-                if (i0 + j < K) mean += v[j];
+                if (i0 + j < K) part += v[j];
+            mean += part;
         }
         mean /= static_cast<float>(K);
     }

@@ -13,6 +13,16 @@
 // memory 64 draws at a time and read as warp-wide broadcasts. The per-channel counters are pre-folded once
 // per thread, so each element-draw costs the hash tail plus one FMA
 // (Rademacher: the sign bit is xor-ed into the reward's sign bit).
+//
+// Reward sources (SRC): the credit scan's token-major rewards r [T][K]
+// (0), the same plus the scan's chunk carry P[t] carry[chunk][i] (1), or,
+// when gamma = 0 and the scan is the identity (r_t = c_t), the loss changes
+// themselves, Delta [K][T], centred over the draws here (2): c = -(Delta -
+// mean), the mean of a token's K changes summed in draw order as the scan
+// does. Source 2 takes K <= 64 (one staging group; the library uses it up to
+// K = 32, beyond which the longer prologue costs more than the scan): the
+// CTA's 8 x K loss changes are loaded into shared memory at once, coalesced
+// along the tokens.
 #include "internal.cuh"
 #include "noise.cuh"
 
@@ -79,13 +89,16 @@ __device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16* g, int64_t 
     }
 }
 
-template <int KIND, bool FIX, bool ANTI, typename OutT>
+template <int KIND, int SRC, bool ANTI, typename OutT>
 __global__ void __launch_bounds__(256, KIND == 1 ? kMinBlocksG : kMinBlocksR)
     k_weight(const float* __restrict__ r, const float* __restrict__ P,
              const float* __restrict__ carry, int64_t K, int64_t T, int64_t d_out, uint32_t skey,
-             int64_t draw_begin, float coef, OutT* __restrict__ g, bool vec_ok) {
+             int64_t draw_begin, float coef, OutT* __restrict__ g, bool vec_ok, int center) {
     __shared__ uint2 s_key[kGroup];  // folded keys of streams 0 and 1
     __shared__ float s_r[kTok][kGroup];
+    __shared__ float s_raw[SRC == 2 ? kTok : 1][kGroup + 1];  // Delta of the CTA's tokens
+    __shared__ float s_mean[kTok];
+    __shared__ float s_part[SRC == 2 ? kTok : 1][kGroup / 8];
     pdl_wait();
     pdl_trigger();
 
@@ -113,9 +126,40 @@ __global__ void __launch_bounds__(256, KIND == 1 ? kMinBlocksG : kMinBlocksR)
     // b, so each base draw's noise is evaluated once, weighted by the
     // difference of the pair's rewards: the loop runs over Kb = K / 2 base
     // draws (draw_begin is even).
-    auto reward = [&](int64_t tt, int64_t i) {
+    if (SRC == 2) {
+        // The CTA's loss changes, then each token's mean over its K draws
+        // (centring), summed in draw order.
+        const int kk = static_cast<int>(K);
+        for (int e = tid; e < kTok * kk; e += blockDim.x) {
+            const int k = e / kTok, tok = e - k * kTok;
+            s_raw[tok][k] = (tb + tok < T) ? r[static_cast<int64_t>(k) * T + tb + tok] : 0.0f;
+        }
+        __syncthreads();
+        // Sums of 8 draws each in draw order (one thread per token and batch),
+        // then the batch sums in order: the credit scan's order.
+        const int nb = (kk + 7) / 8;
+        if (center && kk > 1 && tid < kTok * nb) {
+            const int tok = tid / nb, q = tid - tok * nb;
+            float part = 0.0f;
+            for (int k = 8 * q; k < 8 * q + 8 && k < kk; ++k) part += s_raw[tok][k];
+            s_part[tok][q] = part;
+        }
+        __syncthreads();
+        if (tid < kTok) {
+            float mean = 0.0f;
+            if (center && kk > 1) {
+                for (int q = 0; q < nb; ++q) mean += s_part[tid][q];
+                mean /= static_cast<float>(kk);
+            }
+            s_mean[tid] = mean;
+        }
+        __syncthreads();
+    }
+    auto reward = [&](int tok, int64_t i) {
+        if (SRC == 2) return -(s_raw[SRC == 2 ? tok : 0][i] - s_mean[tok]);
+        const int64_t tt = tb + tok;
         float v = r[tt * K + i];
-        if (FIX) v = fmaf(P[tt], carry[(tt / kScanChunk) * K + i], v);
+        if (SRC == 1) v = fmaf(P[tt], carry[(tt / kScanChunk) * K + i], v);
         return v;
     };
     const int64_t Kb = ANTI ? K / 2 : K;
@@ -129,14 +173,13 @@ __global__ void __launch_bounds__(256, KIND == 1 ? kMinBlocksG : kMinBlocksR)
         }
         for (int e = tid; e < kTok * gn; e += blockDim.x) {
             const int tok = e / gn, k = e - tok * gn;
-            const int64_t tt = tb + tok;
             float v = 0.0f;
-            if (tt < T) {
+            if (tb + tok < T) {
                 if (ANTI) {
                     const int64_t i = 2 * (g0 + k);
-                    v = (reward(tt, i) - reward(tt, i + 1)) * coef;
+                    v = (reward(tok, i) - reward(tok, i + 1)) * coef;
                 } else {
-                    v = reward(tt, g0 + k) * coef;
+                    v = reward(tok, g0 + k) * coef;
                 }
             }
             s_r[tok][k] = v;
@@ -191,43 +234,55 @@ __global__ void __launch_bounds__(256, KIND == 1 ? kMinBlocksG : kMinBlocksR)
     }
 }
 
-template <int KIND, bool FIX>
-cudaError_t launch_kind(const ScanBuffers& b, int64_t K, int64_t T, int64_t d_out, uint32_t skey,
-                        int64_t draw_begin, float coef, bool anti, void* g, int g_bf16,
-                        cudaStream_t s) {
+template <int KIND, int SRC>
+cudaError_t launch_kind(const float* r, const ScanBuffers& b, int64_t K, int64_t T, int64_t d_out,
+                        uint32_t skey, int64_t draw_begin, float coef, bool anti, int center,
+                        void* g, int g_bf16, cudaStream_t s) {
     constexpr int ch = 32 * cpt_of(KIND);  // channels per CTA
     dim3 grid(static_cast<unsigned>((T + kTok - 1) / kTok),
               static_cast<unsigned>((d_out + ch - 1) / ch));
     const bool vec_ok = (d_out % 8 == 0) && (reinterpret_cast<uintptr_t>(g) % 16 == 0);
     ProfScope ps(kStageWeight, s);
     auto go = [&](auto kernel, auto* out) {
-        return launch_pdl(kernel, grid, dim3(256), 0, s, b.r, b.P, b.carry, K, T, d_out, skey,
-                          draw_begin, coef, out, vec_ok);
+        return launch_pdl(kernel, grid, dim3(256), 0, s, r, b.P, b.carry, K, T, d_out, skey,
+                          draw_begin, coef, out, vec_ok, center);
     };
     auto* gb = static_cast<__nv_bfloat16*>(g);
     auto* gf = static_cast<float*>(g);
     if (g_bf16)
-        return anti ? go(k_weight<KIND, FIX, true, __nv_bfloat16>, gb)
-                    : go(k_weight<KIND, FIX, false, __nv_bfloat16>, gb);
-    return anti ? go(k_weight<KIND, FIX, true, float>, gf)
-                : go(k_weight<KIND, FIX, false, float>, gf);
+        return anti ? go(k_weight<KIND, SRC, true, __nv_bfloat16>, gb)
+                    : go(k_weight<KIND, SRC, false, __nv_bfloat16>, gb);
+    return anti ? go(k_weight<KIND, SRC, true, float>, gf)
+                : go(k_weight<KIND, SRC, false, float>, gf);
+}
+
+template <int KIND>
+cudaError_t launch_src(const float* delta, const ScanBuffers& b, bool fix, int64_t K, int64_t T,
+                       int64_t d_out, uint32_t skey, int64_t draw_begin, float coef, bool anti,
+                       int center, void* g, int g_bf16, cudaStream_t s) {
+    if (delta)
+        return launch_kind<KIND, 2>(delta, b, K, T, d_out, skey, draw_begin, coef, anti, center,
+                                    g, g_bf16, s);
+    if (fix)
+        return launch_kind<KIND, 1>(b.r, b, K, T, d_out, skey, draw_begin, coef, anti, 0, g,
+                                    g_bf16, s);
+    return launch_kind<KIND, 0>(b.r, b, K, T, d_out, skey, draw_begin, coef, anti, 0, g, g_bf16,
+                                s);
 }
 
 }  // namespace
 
 cudaError_t launch_weight(const ScanBuffers& b, bool fix, int64_t K, int64_t T, int64_t d_out,
                           uint64_t seed, int kind, int64_t draw_begin, float coef, bool anti,
-                          void* g, int g_bf16, cudaStream_t s) {
+                          void* g, int g_bf16, cudaStream_t s, const float* delta, bool center) {
     if (T == 0 || d_out == 0) return cudaSuccess;
     const uint32_t skey = seed_key(seed);
+    const int c = center ? 1 : 0;
     if (kind == 1)
-        return fix ? launch_kind<1, true>(b, K, T, d_out, skey, draw_begin, coef, anti, g, g_bf16, s)
-                   : launch_kind<1, false>(b, K, T, d_out, skey, draw_begin, coef, anti, g, g_bf16, s);
+        return launch_src<1>(delta, b, fix, K, T, d_out, skey, draw_begin, coef, anti, c, g, g_bf16, s);
     if (kind == 3)
-        return fix ? launch_kind<3, true>(b, K, T, d_out, skey, draw_begin, coef, anti, g, g_bf16, s)
-                   : launch_kind<3, false>(b, K, T, d_out, skey, draw_begin, coef, anti, g, g_bf16, s);
-    return fix ? launch_kind<0, true>(b, K, T, d_out, skey, draw_begin, coef, anti, g, g_bf16, s)
-               : launch_kind<0, false>(b, K, T, d_out, skey, draw_begin, coef, anti, g, g_bf16, s);
+        return launch_src<3>(delta, b, fix, K, T, d_out, skey, draw_begin, coef, anti, c, g, g_bf16, s);
+    return launch_src<0>(delta, b, fix, K, T, d_out, skey, draw_begin, coef, anti, c, g, g_bf16, s);
 }
 
 }  // namespace dust
