@@ -27,6 +27,9 @@ W_CASES = [
     (64, 64, 1000, 0, 0, 0),
     (65, 31, 513, 1, 123, 0),
     (16, 200, 2048, 1, 0, 0),
+    (66, 77, 1024, 1, 4, dust.ANTITHETIC),  # two draw groups, ragged T
+    (8, 77, 1024, 1, 4, 0),                 # 32 channels per lane (<= 8 noise draws)
+    (16, 45, 2048, 1, 2, dust.ANTITHETIC),  # the same with 8 antithetic pairs
     (130, 17, 64, 0, 2, dust.ANTITHETIC),
     # packed signs: one 32-sign word per lane, 1024 channels per CTA
     (8, 100, 77, 3, 0, 0),            # a 13-channel last word

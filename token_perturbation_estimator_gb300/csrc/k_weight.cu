@@ -5,8 +5,9 @@
 // from the hash for every (draw, token, channel) and used once; nothing of it
 // is stored.
 //
-// Mapping: one warp per token, kCpt channels per lane (kCpt/2 Box-Muller pairs
-// or kCpt signs; packed signs: the 32 channels of one hash word), 8 tokens x
+// Mapping: one warp per token, CPT channels per lane (CPT/2 Box-Muller pairs
+// or CPT signs; packed signs: the 32 channels of one hash word; Gaussian with
+// d_out a multiple of 1024: 32 channels), 8 tokens x
 // 32 lanes' channels per CTA. The per-draw keys and the
 // per-token rewards (already multiplied by -1/(K sigma); for antithetic pairs,
 // the pair's reward difference, one per base draw) are staged in shared
@@ -41,6 +42,13 @@ namespace {
 #ifndef DUST_WEIGHT_MINB_R
 #define DUST_WEIGHT_MINB_R 4
 #endif
+// Gaussian with 32 channels per lane (16 Box-Muller pairs per draw, for d_out
+// a multiple of 1024 and at most 8 noise draws per token): the per-draw
+// shared-memory reads and the per-thread setup and store spread over twice
+// the pairs, at 3 resident CTAs per SM.
+#ifndef DUST_WEIGHT_MINB_GW
+#define DUST_WEIGHT_MINB_GW 3
+#endif
 #ifndef DUST_WEIGHT_UNROLL
 #define DUST_WEIGHT_UNROLL 2
 #endif
@@ -49,10 +57,12 @@ constexpr int kMinBlocksR = DUST_WEIGHT_MINB_R;
 constexpr int kUnrollW = DUST_WEIGHT_UNROLL;
 constexpr int kTok = 8;                 // tokens per CTA (one per warp)
 constexpr int kCpt = DUST_WEIGHT_CPT;   // channels per lane (8 or 16)
-// Channels per lane for a noise kind: one 32-sign word for packed signs.
-constexpr int cpt_of(int kind) { return kind == 3 ? 32 : kCpt; }
+constexpr int kCptWide = 32;            // channels per lane: packed signs, wide Gaussian
 constexpr int kGroup = 64;              // draws staged per pass
 static_assert(kCpt % 8 == 0, "channels per lane must be a multiple of 8");
+constexpr int min_blocks(int kind, int cpt) {
+    return kind == 1 ? (cpt == kCptWide ? DUST_WEIGHT_MINB_GW : kMinBlocksG) : kMinBlocksR;
+}
 
 template <typename OutT>
 __device__ __forceinline__ void store8(OutT* g, int64_t row, int64_t d_out, int64_t c0,
@@ -89,8 +99,8 @@ __device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16* g, int64_t 
     }
 }
 
-template <int KIND, int SRC, bool ANTI, typename OutT>
-__global__ void __launch_bounds__(256, KIND == 1 ? kMinBlocksG : kMinBlocksR)
+template <int KIND, int CPT, int SRC, bool ANTI, typename OutT>
+__global__ void __launch_bounds__(256, min_blocks(KIND, CPT))
     k_weight(const float* __restrict__ r, const float* __restrict__ P,
              const float* __restrict__ carry, int64_t K, int64_t T, int64_t d_out, uint32_t skey,
              int64_t draw_begin, float coef, OutT* __restrict__ g, bool vec_ok, int center) {
@@ -102,8 +112,9 @@ __global__ void __launch_bounds__(256, KIND == 1 ? kMinBlocksG : kMinBlocksR)
     pdl_wait();
     pdl_trigger();
 
-    // Channels per lane: one 32-sign word for the packed signs, else kCpt.
-    constexpr int cpt = cpt_of(KIND);
+    // Channels per lane: one 32-sign word for the packed signs.
+    constexpr int cpt = CPT;
+    static_assert(KIND != 3 || CPT == 32, "packed signs: one word per lane");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t tb = static_cast<int64_t>(blockIdx.x) * kTok;
     const int64_t t = tb + warp;
@@ -234,11 +245,11 @@ __global__ void __launch_bounds__(256, KIND == 1 ? kMinBlocksG : kMinBlocksR)
     }
 }
 
-template <int KIND, int SRC>
+template <int KIND, int CPT, int SRC>
 cudaError_t launch_kind(const float* r, const ScanBuffers& b, int64_t K, int64_t T, int64_t d_out,
                         uint32_t skey, int64_t draw_begin, float coef, bool anti, int center,
                         void* g, int g_bf16, cudaStream_t s) {
-    constexpr int ch = 32 * cpt_of(KIND);  // channels per CTA
+    constexpr int ch = 32 * CPT;  // channels per CTA
     dim3 grid(static_cast<unsigned>((T + kTok - 1) / kTok),
               static_cast<unsigned>((d_out + ch - 1) / ch));
     const bool vec_ok = (d_out % 8 == 0) && (reinterpret_cast<uintptr_t>(g) % 16 == 0);
@@ -250,24 +261,24 @@ cudaError_t launch_kind(const float* r, const ScanBuffers& b, int64_t K, int64_t
     auto* gb = static_cast<__nv_bfloat16*>(g);
     auto* gf = static_cast<float*>(g);
     if (g_bf16)
-        return anti ? go(k_weight<KIND, SRC, true, __nv_bfloat16>, gb)
-                    : go(k_weight<KIND, SRC, false, __nv_bfloat16>, gb);
-    return anti ? go(k_weight<KIND, SRC, true, float>, gf)
-                : go(k_weight<KIND, SRC, false, float>, gf);
+        return anti ? go(k_weight<KIND, CPT, SRC, true, __nv_bfloat16>, gb)
+                    : go(k_weight<KIND, CPT, SRC, false, __nv_bfloat16>, gb);
+    return anti ? go(k_weight<KIND, CPT, SRC, true, float>, gf)
+                : go(k_weight<KIND, CPT, SRC, false, float>, gf);
 }
 
-template <int KIND>
+template <int KIND, int CPT>
 cudaError_t launch_src(const float* delta, const ScanBuffers& b, bool fix, int64_t K, int64_t T,
                        int64_t d_out, uint32_t skey, int64_t draw_begin, float coef, bool anti,
                        int center, void* g, int g_bf16, cudaStream_t s) {
     if (delta)
-        return launch_kind<KIND, 2>(delta, b, K, T, d_out, skey, draw_begin, coef, anti, center,
-                                    g, g_bf16, s);
+        return launch_kind<KIND, CPT, 2>(delta, b, K, T, d_out, skey, draw_begin, coef, anti,
+                                         center, g, g_bf16, s);
     if (fix)
-        return launch_kind<KIND, 1>(b.r, b, K, T, d_out, skey, draw_begin, coef, anti, 0, g,
-                                    g_bf16, s);
-    return launch_kind<KIND, 0>(b.r, b, K, T, d_out, skey, draw_begin, coef, anti, 0, g, g_bf16,
-                                s);
+        return launch_kind<KIND, CPT, 1>(b.r, b, K, T, d_out, skey, draw_begin, coef, anti, 0, g,
+                                         g_bf16, s);
+    return launch_kind<KIND, CPT, 0>(b.r, b, K, T, d_out, skey, draw_begin, coef, anti, 0, g,
+                                     g_bf16, s);
 }
 
 }  // namespace
@@ -278,11 +289,22 @@ cudaError_t launch_weight(const ScanBuffers& b, bool fix, int64_t K, int64_t T, 
     if (T == 0 || d_out == 0) return cudaSuccess;
     const uint32_t skey = seed_key(seed);
     const int c = center ? 1 : 0;
+    // Wide Gaussian lanes where a token has few noise draws (the per-draw and
+    // per-thread overheads then weigh most) and the CTAs of 1024 channels are
+    // whole; with more draws the narrower lanes' occupancy wins (measured:
+    // K 8 weighting 139 -> 135.5 us; K 16 and 64 about 1 % slower wide).
+    const int64_t noise_draws = anti ? K / 2 : K;
+    if (kind == 1 && d_out % (32 * kCptWide) == 0 && noise_draws <= 8)
+        return launch_src<1, kCptWide>(delta, b, fix, K, T, d_out, skey, draw_begin, coef, anti, c,
+                                       g, g_bf16, s);
     if (kind == 1)
-        return launch_src<1>(delta, b, fix, K, T, d_out, skey, draw_begin, coef, anti, c, g, g_bf16, s);
+        return launch_src<1, kCpt>(delta, b, fix, K, T, d_out, skey, draw_begin, coef, anti, c, g,
+                                   g_bf16, s);
     if (kind == 3)
-        return launch_src<3>(delta, b, fix, K, T, d_out, skey, draw_begin, coef, anti, c, g, g_bf16, s);
-    return launch_src<0>(delta, b, fix, K, T, d_out, skey, draw_begin, coef, anti, c, g, g_bf16, s);
+        return launch_src<3, kCptWide>(delta, b, fix, K, T, d_out, skey, draw_begin, coef, anti, c,
+                                       g, g_bf16, s);
+    return launch_src<0, kCpt>(delta, b, fix, K, T, d_out, skey, draw_begin, coef, anti, c, g,
+                               g_bf16, s);
 }
 
 }  // namespace dust
