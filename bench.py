@@ -536,6 +536,18 @@ def run_gb300(args):
                      "ms_per_launch": v["total_ms"] / v["launches"],
                      "share": v["total_ms"] / tot_ms}
                  for k, v in prof.items()}
+    # The metric's two named fractions: the contraction against the tensor
+    # peak, the noise/weighting stage against HBM (its bytes: the loss changes
+    # or rewards read, g written).
+    stage_fracs = {}
+    if "gemm_tc" in prof:
+        g = roofline_for("gemm_tc", prof["gemm_tc"]["total_ms"] / prof_steps, sites, peaks)
+        stage_fracs["gemm_tc_tensor_frac"] = g["frac"]
+    if "weight" in prof:
+        byts = float(sum(4 * w.K * w.T + (2 if w.x_dtype == "bf16" else 4) * w.T * w.d_out
+                         for w in sites))
+        s_w = prof["weight"]["total_ms"] / prof_steps / 1000.0
+        stage_fracs["weight_hbm_frac"] = byts / s_w / (peaks.get("hbm_gbs", 6800.0) * 1e9)
 
     # ---- end to end through the host-buffer C ABI entry point
     hosts = []
@@ -599,6 +611,8 @@ def run_gb300(args):
             "gpu_launches": int(round(launches_per_step * args.steps)),
             "clocks": clocks.summary(),
             "breakdown": breakdown,
+            "stage_fractions": stage_fracs,
+            "gw_updates_per_s": len(sites) * 1000.0 / ms_per_step,
             "profiled_ms_per_step": tot_ms / prof_steps,
             "profiled_steps": prof_steps,
         }
