@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int32_t n0 = static_cast<int32_t>((tile % a.n_tn) * kBN);
                 for (int kb = 0; kb < n_kb; ++kb, ++it) {
                     const int st = it % n_stages;
-                    if (!tc::mbar_wait_sleep(&ctl->empty[st], ((it / n_stages) & 1) ^ 1) ||
+                    if (!tc::mbar_wait(&ctl->empty[st], ((it / n_stages) & 1) ^ 1) ||
                         *abort_flag) {
                         *abort_flag = 1;
                         break;
@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t d = tmem + acc * kBN;
                 for (int kb = 0; kb < n_kb; ++kb, ++it) {
                     const int st = it % n_stages;
-                    if (!tc::mbar_wait_sleep(&ctl->full[st], (it / n_stages) & 1) || *abort_flag) {
+                    if (!tc::mbar_wait(&ctl->full[st], (it / n_stages) & 1) || *abort_flag) {
                         *abort_flag = 1;
                         break;
                     }
