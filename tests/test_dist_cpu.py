@@ -4,7 +4,11 @@
    rank estimates GW from its own sequences with the oracle (the scan never
    crosses a sequence and the hash uses global token indices), one all-reduce
    sums the shards, and the sum equals the unsharded estimate.
-2. The benchmark's whole-job aggregation: the max over ranks of the timed
+2. Sharding by draws (the split the pages' eight GPUs use): rank r owns a
+   range of absolute draw indices (draw_begin), the loss changes are centred
+   once over all K draws, and each shard's estimate, scaled by its share of
+   the draws, sums to the unsharded centred estimate.
+3. The benchmark's whole-job aggregation: the max over ranks of the timed
    region and units summed over ranks.
 """
 import os
@@ -47,6 +51,13 @@ def _worker(rank, world, port, out_dir):
     part = oracle.estimate_gW(Xs, delta, d_out, so, 5, 1, 0, 0.01, 0.9, 1.0, oracle.CENTER)
     t = torch.from_numpy(part)
     dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    # draws [2r, 2r + 2) on rank r, centred over all K beforehand (CENTER off)
+    centred = delta - delta.mean(axis=0, keepdims=True)
+    d0, d1 = 2 * rank, 2 * rank + 2
+    dpart = oracle.estimate_gW(X, centred[d0:d1], d_out, so, 5, 1, d0, 0.01, 0.9,
+                               (d1 - d0) / K, 0)
+    td = torch.from_numpy(dpart)
+    dist.all_reduce(td, op=dist.ReduceOp.SUM)
 
     def max_over_ranks(x):
         v = torch.tensor([x], dtype=torch.float64)
@@ -58,6 +69,7 @@ def _worker(rank, world, port, out_dir):
     if rank == 0:
         full = oracle.estimate_gW(X, delta, d_out, so, 5, 1, 0, 0.01, 0.9, 1.0, oracle.CENTER)
         np.save(os.path.join(out_dir, "sum.npy"), t.numpy())
+        np.save(os.path.join(out_dir, "dsum.npy"), td.numpy())
         np.save(os.path.join(out_dir, "full.npy"), full)
         np.save(os.path.join(out_dir, "agg.npy"), np.array([value, ms_per_step]))
     dist.barrier()
@@ -73,6 +85,8 @@ def test_sequence_sharded_estimate_and_bench_aggregation(tmp_path):
     s = np.load(tmp_path / "sum.npy")
     f = np.load(tmp_path / "full.npy")
     assert np.allclose(s, f, rtol=1e-12, atol=1e-12 * np.abs(f).max())
+    ds = np.load(tmp_path / "dsum.npy")
+    assert np.allclose(ds, f, rtol=1e-10, atol=1e-10 * np.abs(f).max())
     value, ms_per_step = np.load(tmp_path / "agg.npy")
     assert ms_per_step == pytest.approx(15.0)          # max over ranks: 150 ms / 10 steps
     assert value == pytest.approx(2 * 1000.0 * 10 / 0.150)

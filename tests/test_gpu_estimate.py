@@ -239,6 +239,31 @@ def test_sequence_sharding_sums_to_whole():
     assert rel_fro(acc.cpu().numpy(), full.cpu().numpy()) <= 1e-6
 
 
+def test_draw_sharding_sums_to_whole():
+    """Sharding by draws: each shard takes a range of absolute draw indices
+    (draw_begin); the loss changes are centred once over all K draws and
+    passed without DUST_CENTER, and each shard's estimate is scaled by its
+    share of the draws, so the shards accumulate to the unsharded centred
+    estimate."""
+    import torch
+    dev = cuda()
+    rng = np.random.default_rng(23)
+    so = offsets_from_lengths([120, 80, 200])
+    T, d_in, d_out, K = int(so[-1]), 24, 40, 12
+    X = torch.from_numpy(rng.standard_normal((T, d_in)).astype(np.float32)).to(dev)
+    delta = rng.standard_normal((K, T)).astype(np.float32)
+    sod = torch.from_numpy(so).to(dev)
+    full = dust.dust_estimate_gW(X, torch.from_numpy(delta).to(dev), d_out, sod, 4, 1, 0, 0.01,
+                                 0.9, 1.0, dust.CENTER)
+    centred = (delta - delta.mean(axis=0, keepdims=True)).astype(np.float32)
+    acc = torch.zeros_like(full)
+    for d0, d1 in ((0, 4), (4, 10), (10, 12)):
+        dust.dust_estimate_gW(X, torch.from_numpy(np.ascontiguousarray(centred[d0:d1])).to(dev),
+                              d_out, sod, 4, 1, d0, 0.01, 0.9, (d1 - d0) / K, dust.ACCUMULATE,
+                              gW=acc)
+    assert rel_fro(acc.cpu().numpy(), full.cpu().numpy()) <= 1e-5
+
+
 # ----------------------------------------------- full sizes, sampled entries --
 
 FULL = [wl.TOY, wl.MLP_UP, wl.QKV_DECAY, wl.SQUARE_R, wl.SQUARE_G]
