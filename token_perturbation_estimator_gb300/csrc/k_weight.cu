@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(256, min_blocks(KIND, CPT))
                     }
                 }
             } else if (KIND == 3) {
-#pragma unroll 2
+#pragma unroll 8  // 2: 813 us, 4: 774 us, 8: 766 us on the 4096^2 layer, 64 draws
                 for (int k = 0; k < gn; ++k) {
                     const uint32_t rb = __float_as_uint(s_r[warp][k]);
                     const uint32_t w = word_ff(s_key[k].x, nf[0]);
