@@ -386,6 +386,8 @@ DIRECT_CASES = [
     (777, 96, 320, 16, 3, dust.CENTER | dust.ANTITHETIC, "bf16"),
     (300, 40, 72, 6, 1, 0, "f32"),                              # no centring, fp32 path
     (129, 64, 64, 1, 0, dust.CENTER, "f32"),                    # K = 1: centring is a no-op
+    (2003, 64, 1024, 16, 1, dust.CENTER | dust.ANTITHETIC, "bf16"),  # persistent, 8 pairs
+    (500, 40, 1024, 8, 1, dust.CENTER, "f32"),                 # persistent, fp32 g
 ]
 
 
