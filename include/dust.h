@@ -335,6 +335,13 @@ dust_status dust_contract(const void* g, const void* X, dust_dtype dtype, int64_
  *               aligned; contents on entry are ignored.
  * The result is a deterministic function of the inputs (no floating-point
  * atomics): two calls with the same arguments give bit-identical gW.
+ * With gamma = 0 the credit scan is the identity (r = c); for K <= 32 the
+ * weighting kernel then centres delta itself and no scan kernel runs, with
+ * the same bits as the scan path (the per-token mean is summed in the same
+ * order). Sharding: calls over disjoint whole sequences (the other rows of X
+ * zero or excluded), or over disjoint draw ranges (draw_begin; delta centred
+ * over all K beforehand, DUST_CENTER off, scale = the range's share of K),
+ * accumulate (DUST_ACCUMULATE) to the unsharded estimate.
  * Graph replay: from the second call with identical arguments (every pointer
  * and scalar) on the current device, the call's launches are captured once
  * into a CUDA graph and later calls launch that graph on `stream`; it reads
