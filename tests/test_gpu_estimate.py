@@ -415,3 +415,18 @@ def test_gamma_zero_skips_the_scan_bit_for_bit(T, d_in, d_out, K, kind, flags, x
     torch.cuda.synchronize()
     assert dust.dust_last_error() == dust.OK
     assert torch.equal(got, want)
+
+
+@pytest.mark.parametrize("kind", [dust.GAUSSIAN, dust.RADEMACHER])
+def test_error_estimate_highest_draw_indices(kind):
+    """The weighting with the last legal draws (draw_begin + K = 2^31) and a
+    64-bit seed, against the oracle."""
+    import torch
+    dev = cuda()
+    rng = np.random.default_rng(31)
+    K, T, d_out = 70, 40, 130
+    db = (1 << 31) - K
+    r = rng.standard_normal((T, K)).astype(np.float32)
+    g = dust.dust_error_estimate(torch.from_numpy(r).to(dev), d_out, 2 ** 63 + 11, kind, db, 1e-2)
+    want = oracle.error_estimate(r.T.copy(), d_out, 2 ** 63 + 11, kind, db, np.float32(1e-2), 0)
+    assert rel_fro(g.cpu().numpy(), want) <= 1e-5

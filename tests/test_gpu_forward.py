@@ -205,3 +205,21 @@ def test_largest_counter_range_sampled(kind):
     assert (np.abs(got - want) <= 2.0 ** -8 * (np.abs(want) + e) + e).all()
     del Y
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("kind,flags", [(dust.GAUSSIAN, 0), (dust.RADEMACHER_PACKED, dust.ANTITHETIC)])
+def test_highest_draw_indices(kind, flags):
+    """The last legal draws (draw_begin + n_draws = 2^31): keys made from the
+    largest absolute indices, more of them than the shared key table holds."""
+    dev = cuda()
+    T, d_in, d_out = 200, 64, 96
+    X, W = _inputs(T, d_in, d_out, 13)
+    n = 66
+    db = (1 << 31) - n
+    got = dust.dust_forward_jitter(_to_dev(X, dev), _to_dev(W, dev), 2 ** 40 + 7, kind, db, n,
+                                   0.5, flags=flags)
+    assert dust.dust_last_error() == dust.OK
+    want = oracle.forward_jitter(X, W, 2 ** 40 + 7, kind, db, n, 0.5, flags=flags)
+    a = np.abs(want - (X @ W.T)[None]) / 0.5
+    err = np.abs(got.double().cpu().numpy() - want)
+    assert (err <= _bound(X, W, want, 0.5, a)).all()
