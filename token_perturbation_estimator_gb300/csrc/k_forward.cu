@@ -16,7 +16,8 @@
 //   warp 1, one thread: tcgen05.mma (M 128, N kBN, K 16) into one of two
 //     TMEM accumulators, so the next tile's product overlaps this tile's
 //     epilogue;
-//   kEW epilogue warps: each reads 32 tokens x 32 channels of y from TMEM
+//   24 epilogue warps (16 for packed signs, whose arithmetic is light, so each
+//     warp gets more staging buffers): each reads 32 tokens x 32 channels of y from TMEM
 //     (its lane quarter), frees the accumulator after its last read, adds
 //     sigma a per draw, rounds to bf16, stages the 32 x 32 block in shared
 //     memory (64-byte swizzle, no bank conflicts) and writes it with a TMA
@@ -45,7 +46,10 @@ namespace {
 #define DUST_FWD_BN 256  // channels per tile (columns of one TMEM accumulator)
 #endif
 #ifndef DUST_FWD_EW
-#define DUST_FWD_EW 24  // epilogue warps
+#define DUST_FWD_EW 24  // epilogue warps (Gaussian, per-channel signs)
+#endif
+#ifndef DUST_FWD_EW_PACKED
+#define DUST_FWD_EW_PACKED 16  // (packed signs: light arithmetic, more staging buffers each)
 #endif
 #ifndef DUST_FWD_SUB_G
 #define DUST_FWD_SUB_G 8  // TMEM columns an epilogue thread holds at a time (Gaussian)
@@ -60,7 +64,9 @@ constexpr int kBM = 128;
 constexpr int kBN = DUST_FWD_BN;
 constexpr int kBK = 64;  // d_in per k-step: one 128-byte swizzle row
 constexpr int kEW = DUST_FWD_EW;
-constexpr int kThreads = 64 + 32 * kEW;
+// Epilogue warps and threads of the kernel for a noise kind.
+constexpr int ew_of(int kind) { return kind == 3 ? DUST_FWD_EW_PACKED : kEW; }
+constexpr int threads_of(int kind) { return 64 + 32 * ew_of(kind); }
 // Shared memory is split between the k-step ring and the epilogue's staging
 // buffers in one of two ways, chosen per launch: 2 stages and 3 buffers per
 // warp (short reductions, where the stores dominate), or 3 stages and 2
@@ -72,16 +78,18 @@ constexpr int kBBytes = kBN * kBK * 2;
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kBufBytes = 32 * 32 * 2;  // 32 tokens x 32 channels of bf16
 constexpr int kSplitBytes = 3 * kStageBytes + 64 * 1024;  // ring + staging buffers
-constexpr int kPerQuarter = kEW / 4;  // epilogue warps reading one TMEM lane quarter
 constexpr int kChunks = kBN / 32;
 constexpr int kKeyTable = 64;           // per-draw keys kept in shared memory
 constexpr int kSmemBytes = kSplitBytes + kKeyTable * 8 + 256 + 1024;
 static_assert(kBN == 128 || kBN == 256, "two accumulators of kBN columns fit TMEM");
-static_assert(kEW % 4 == 0, "epilogue warps cover the four TMEM lane quarters");
-static_assert(kSplitBytes - 3 * kStageBytes >= kEW * kBufBytes, "a staging buffer per warp");
+static_assert(kEW % 4 == 0 && DUST_FWD_EW_PACKED % 4 == 0,
+              "epilogue warps cover the four TMEM lane quarters");
+static_assert(kSplitBytes - 3 * kStageBytes >= kEW * kBufBytes &&
+                  kSplitBytes - 3 * kStageBytes >= DUST_FWD_EW_PACKED * kBufBytes,
+              "a staging buffer per warp");
 static_assert(kStageBytes % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
-static_assert(kThreads <= 1024, "one CTA");
+static_assert(threads_of(0) <= 1024 && threads_of(3) <= 1024, "one CTA");
 
 struct Ctl {
     uint64_t full[kMaxStages];
@@ -182,7 +190,7 @@ __device__ __forceinline__ void jitter_sub(const float (&y)[N], uint32_t n_row, 
 }
 
 template <int KIND, bool ALIGNED>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_of(KIND), 1)
     k_forward(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
               const __grid_constant__ CUtensorMap tmY, const FwdArgs a) {
     extern __shared__ unsigned char smem_raw[];
@@ -203,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&ctl->tfull[i], 1);
-            tc::mbar_init(&ctl->tempty[i], kEW);
+            tc::mbar_init(&ctl->tempty[i], ew_of(KIND));
         }
         tc::mbar_init(&ctl->never, 1);
         ctl->abort = 0;
@@ -288,6 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------- epilogue
+        constexpr int kPerQuarter = ew_of(KIND) / 4;  // warps reading one TMEM lane quarter
         // The work of a tile's lane quarter is kChunks x n_slices items (one
         // 32-channel block of one slice each), dealt round robin to the
         // quarter's kPerQuarter warps; the deal continues across tiles so no
@@ -441,8 +450,11 @@ cudaError_t launch_kind(const CUtensorMap& tx, const CUtensorMap& tw, const CUte
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     });
     if (attr != cudaSuccess) return attr;
-    return launch_pdl(k_forward<KIND, ALIGNED>, grid, dim3(kThreads), kSmemBytes, s, tx, tw, ty,
-                      fa);
+    FwdArgs f = fa;
+    const int nbuf = (kSplitBytes - f.stages * kStageBytes) / (ew_of(KIND) * kBufBytes);
+    f.nbuf = nbuf > 3 ? 3 : nbuf;
+    return launch_pdl(k_forward<KIND, ALIGNED>, grid, dim3(threads_of(KIND)), kSmemBytes, s, tx,
+                      tw, ty, f);
 }
 
 }  // namespace
@@ -467,8 +479,6 @@ cudaError_t launch_forward(const void* X, const void* W, int64_t T, int64_t d_in
     fa.n_tiles = fa.n_tn * ((T + kBM - 1) / kBM);
     const bool deep = (d_in + kBK - 1) / kBK >= DUST_FWD_DEEP_KSTEPS;
     fa.stages = deep ? 3 : 2;
-    const int nbuf = (kSplitBytes - fa.stages * kStageBytes) / (kEW * kBufBytes);
-    fa.nbuf = nbuf > 3 ? 3 : nbuf;
     fa.skey = seed_key(seed);
     fa.draw_begin = draw_begin;
     fa.n_draws = n_draws;
