@@ -325,16 +325,17 @@ def kernel_source_hash(kernel):
     return h.hexdigest()[:16]
 
 
-def traffic_from_profiles(kernel):
+def traffic_from_profiles(kernel, entry=None):
     """DRAM bytes (read + write) per launch from a committed ncu capture, if
-    the kernel's sources are unchanged since the capture (else None)."""
+    the kernel's sources are unchanged since the capture (else None).  `entry`
+    names a capture of one workload of the kernel (default: the kernel)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
     except (OSError, ValueError):
         return None
-    e = d.get(kernel)
+    e = d.get(entry or kernel)
     if not e or e.get("source_hash") != kernel_source_hash(kernel):
         return None
     return e.get("dram_bytes_per_launch")
@@ -767,7 +768,7 @@ def run_forward(args):
     launches, fwd_ms = prof["forward"]
     roof = forward_roofline(fwd_ms / launches, T, w.d_in, w.d_out, K, 1, kind, load_peaks())
     roof["launches_per_step"] = launches / args.steps
-    roof["traffic"] = traffic_from_profiles("forward")
+    roof["traffic"] = traffic_from_profiles("forward", args.workload)
 
     # end to end: X and W from pinned host memory, every output slice back
     Xh, Wh = X.cpu().pin_memory(), W.cpu().pin_memory()
