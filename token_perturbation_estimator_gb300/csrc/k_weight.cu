@@ -20,10 +20,11 @@
 // when gamma = 0 and the scan is the identity (r_t = c_t), the loss changes
 // themselves, Delta [K][T], centred over the draws here (2): c = -(Delta -
 // mean), the mean of a token's K changes summed in draw order as the scan
-// does. Source 2 takes K <= 64 (one staging group; the library uses it up to
-// K = 32, beyond which the longer prologue costs more than the scan): the
-// CTA's 8 x K loss changes are loaded into shared memory at once, coalesced
-// along the tokens.
+// does. Source 2 takes K <= 32 (the library uses it up to K = 32, beyond
+// which the longer prologue costs more than the scan): each warp loads its
+// own token's K loss changes, one per lane, and centres them with shuffles,
+// so no CTA barrier is taken (the narrow Gaussian lanes, short of registers,
+// stage them through shared memory instead, CTA-wide).
 #include "internal.cuh"
 #include "noise.cuh"
 
@@ -52,6 +53,13 @@ namespace {
 #ifndef DUST_WEIGHT_UNROLL
 #define DUST_WEIGHT_UNROLL 2
 #endif
+// Loss changes read by each warp for its own token and centred with warp
+// shuffles (no CTA barrier), for reward source 2 (K <= 32); 0: staged
+// through shared memory by the whole CTA.
+#ifndef DUST_WEIGHT_WARP_SRC
+#define DUST_WEIGHT_WARP_SRC 1
+#endif
+constexpr bool kWarpSrc = DUST_WEIGHT_WARP_SRC != 0;
 constexpr int kMinBlocksG = DUST_WEIGHT_MINB_G;
 constexpr int kMinBlocksR = DUST_WEIGHT_MINB_R;
 constexpr int kUnrollW = DUST_WEIGHT_UNROLL;
@@ -103,11 +111,46 @@ __device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16* g, int64_t 
     }
 }
 
+// Folded stream keys of up to 32 base draws, made on the host for reward
+// source 2 and read in the draw loop with a warp-uniform index.
+struct DrawKeys {
+    uint2 k[32];
+};
+
+// One draw's contribution to a lane's channels: rr is the draw's weighted
+// reward for the token, key its folded stream keys.
+template <int KIND, int CPT, int NF>
+__device__ __forceinline__ void add_draw(float (&acc)[CPT], const uint32_t (&nf)[NF], float rr,
+                                         uint2 key) {
+    if (KIND == 1) {
+#pragma unroll
+        for (int p = 0; p < CPT / 2; ++p) {
+            const float f0 = unit_ff(key.x, nf[p]);
+            const float f1 = unit_ff(key.y, nf[p]);
+            const float tr = rr * neg_radius(f0);
+            float sn, cs;
+            __sincosf(centred_angle(f1), &sn, &cs);
+            acc[2 * p] = fmaf(tr, cs, acc[2 * p]);
+            acc[2 * p + 1] = fmaf(tr, sn, acc[2 * p + 1]);
+        }
+    } else if (KIND == 3) {
+        const uint32_t rb = __float_as_uint(rr);
+        const uint32_t w = word_ff(key.x, nf[0]);
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) acc[j] += __uint_as_float(rb ^ packed_sign_bit(w, j));
+    } else {
+        const uint32_t rb = __float_as_uint(rr);
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) acc[j] += __uint_as_float(rb ^ sign_ff(key.x, nf[j]));
+    }
+}
+
 template <int KIND, int CPT, int SRC, bool ANTI, typename OutT>
 __global__ void __launch_bounds__(256, min_blocks(KIND, CPT))
     k_weight(const float* __restrict__ r, const float* __restrict__ P,
              const float* __restrict__ carry, int64_t K, int64_t T, int64_t d_out, uint32_t skey,
-             int64_t draw_begin, float coef, OutT* __restrict__ g, bool vec_ok, int center) {
+             int64_t draw_begin, float coef, OutT* __restrict__ g, bool vec_ok, int center,
+             const DrawKeys keys) {
     __shared__ uint2 s_key[kGroup];  // folded keys of streams 0 and 1
     __shared__ float s_r[kTok][kGroup];
     __shared__ float s_raw[SRC == 2 ? kTok : 1][kGroup + 1];  // Delta of the CTA's tokens
@@ -141,6 +184,60 @@ __global__ void __launch_bounds__(256, min_blocks(KIND, CPT))
     // b, so each base draw's noise is evaluated once, weighted by the
     // difference of the pair's rewards: the loop runs over Kb = K / 2 base
     // draws (draw_begin is even).
+    // (Not for the narrow Gaussian lanes: their 40-register budget would spill.)
+    if constexpr (SRC == 2 && kWarpSrc && !(KIND == 1 && CPT != kCptWide)) {
+        // Lane k holds the token's loss change of draw k (K <= 32). The mean
+        // over the draws is summed in the credit scan's order (sums of 8
+        // draws in draw order, then those sums in order), so the result
+        // equals the scan path's bit for bit. Lane b then holds base draw b's
+        // weighted reward, broadcast draw by draw.
+        constexpr unsigned kAll = 0xffffffffu;
+        const int kk = static_cast<int>(K);
+        const bool tok_ok = t < T;  // the same for the whole warp
+        float dv = 0.0f;
+        if (tok_ok && lane < kk) dv = r[static_cast<int64_t>(lane) * T + t];
+        float mean = 0.0f;
+        if (center && kk > 1) {
+            for (int q = 0; 8 * q < kk; ++q) {
+                const int hi = (8 * q + 8 < kk) ? 8 * q + 8 : kk;
+                float part = 0.0f;
+                for (int k = 8 * q; k < hi; ++k) part += __shfl_sync(kAll, dv, k);
+                mean += part;
+            }
+            mean /= static_cast<float>(kk);
+        }
+        const int kb = ANTI ? kk / 2 : kk;
+        const int i0 = ANTI ? 2 * lane : lane;
+        const float d0 = __shfl_sync(kAll, dv, i0 & 31);
+        const float d1 = __shfl_sync(kAll, dv, (i0 + 1) & 31);
+        float v = 0.0f;
+        if (lane < kb) {
+            const float r0 = -(d0 - mean);
+            if (ANTI) {
+                const float r1 = -(d1 - mean);
+                v = (r0 - r1) * coef;
+            } else {
+                v = r0 * coef;
+            }
+        }
+        if (tok_ok) {
+            // Lanes past d_out run the loop too (no memory access in it) so
+            // that every shuffle has the whole warp; they store nothing.
+            if (KIND == 1) {
+#pragma unroll unroll_of(CPT)
+                for (int k = 0; k < kb; ++k)
+                    add_draw<KIND, cpt, kNf>(acc, nf, __shfl_sync(kAll, v, k), keys.k[k]);
+            } else if (KIND == 3) {
+#pragma unroll 8
+                for (int k = 0; k < kb; ++k)
+                    add_draw<KIND, cpt, kNf>(acc, nf, __shfl_sync(kAll, v, k), keys.k[k]);
+            } else {
+#pragma unroll 2
+                for (int k = 0; k < kb; ++k)
+                    add_draw<KIND, cpt, kNf>(acc, nf, __shfl_sync(kAll, v, k), keys.k[k]);
+            }
+        }
+    } else {
     if (SRC == 2) {
         // The CTA's loss changes, then each token's mean over its K draws
         // (centring), summed in draw order.
@@ -203,41 +300,17 @@ __global__ void __launch_bounds__(256, min_blocks(KIND, CPT))
         if (active) {
             if (KIND == 1) {
 #pragma unroll unroll_of(CPT)
-                for (int k = 0; k < gn; ++k) {
-                    const float rr = s_r[warp][k];
-                    const uint2 key = s_key[k];
-#pragma unroll
-                    for (int p = 0; p < cpt / 2; ++p) {
-                        const float f0 = unit_ff(key.x, nf[p]);
-                        const float f1 = unit_ff(key.y, nf[p]);
-                        const float tr = rr * neg_radius(f0);
-                        float sn, cs;
-                        __sincosf(centred_angle(f1), &sn, &cs);
-                        acc[2 * p] = fmaf(tr, cs, acc[2 * p]);
-                        acc[2 * p + 1] = fmaf(tr, sn, acc[2 * p + 1]);
-                    }
-                }
+                for (int k = 0; k < gn; ++k) add_draw<KIND, cpt, kNf>(acc, nf, s_r[warp][k], s_key[k]);
             } else if (KIND == 3) {
 #pragma unroll 8  // 2: 813 us, 4: 774 us, 8: 766 us on the 4096^2 layer, 64 draws
-                for (int k = 0; k < gn; ++k) {
-                    const uint32_t rb = __float_as_uint(s_r[warp][k]);
-                    const uint32_t w = word_ff(s_key[k].x, nf[0]);
-#pragma unroll
-                    for (int j = 0; j < cpt; ++j)
-                        acc[j] += __uint_as_float(rb ^ packed_sign_bit(w, j));
-                }
+                for (int k = 0; k < gn; ++k) add_draw<KIND, cpt, kNf>(acc, nf, s_r[warp][k], s_key[k]);
             } else {
 #pragma unroll 2
-                for (int k = 0; k < gn; ++k) {
-                    const uint32_t rb = __float_as_uint(s_r[warp][k]);
-                    const uint32_t k0 = s_key[k].x;
-#pragma unroll
-                    for (int j = 0; j < cpt; ++j)
-                        acc[j] += __uint_as_float(rb ^ sign_ff(k0, nf[j]));
-                }
+                for (int k = 0; k < gn; ++k) add_draw<KIND, cpt, kNf>(acc, nf, s_r[warp][k], s_key[k]);
             }
         }
         __syncthreads();
+    }
     }
     if (active) {
         const bool vec = vec_ok;  // 16-byte aligned rows (host-checked)
@@ -254,13 +327,21 @@ cudaError_t launch_kind(const float* r, const ScanBuffers& b, int64_t K, int64_t
                         uint32_t skey, int64_t draw_begin, float coef, bool anti, int center,
                         void* g, int g_bf16, cudaStream_t s) {
     constexpr int ch = 32 * CPT;  // channels per CTA
+    DrawKeys keys = {};
+    if (SRC == 2) {  // K <= 32 (checked by the caller)
+        const int64_t kb = anti ? K / 2 : K;
+        const int64_t b0 = anti ? draw_begin / 2 : draw_begin;
+        for (int64_t i = 0; i < kb; ++i)
+            keys.k[i] = make_uint2(fold16(draw_key(skey, b0 + i, 0)),
+                                   KIND == 1 ? fold16(draw_key(skey, b0 + i, 1)) : 0u);
+    }
     dim3 grid(static_cast<unsigned>((T + kTok - 1) / kTok),
               static_cast<unsigned>((d_out + ch - 1) / ch));
     const bool vec_ok = (d_out % 8 == 0) && (reinterpret_cast<uintptr_t>(g) % 16 == 0);
     ProfScope ps(kStageWeight, s);
     auto go = [&](auto kernel, auto* out) {
         return launch_pdl(kernel, grid, dim3(256), 0, s, r, b.P, b.carry, K, T, d_out, skey,
-                          draw_begin, coef, out, vec_ok, center);
+                          draw_begin, coef, out, vec_ok, center, keys);
     };
     auto* gb = static_cast<__nv_bfloat16*>(g);
     auto* gf = static_cast<float*>(g);
@@ -275,9 +356,11 @@ template <int KIND, int CPT>
 cudaError_t launch_src(const float* delta, const ScanBuffers& b, bool fix, int64_t K, int64_t T,
                        int64_t d_out, uint32_t skey, int64_t draw_begin, float coef, bool anti,
                        int center, void* g, int g_bf16, cudaStream_t s) {
-    if (delta)
+    if (delta) {
+        if (K > 32) return cudaErrorInvalidValue;  // one loss change per lane
         return launch_kind<KIND, CPT, 2>(delta, b, K, T, d_out, skey, draw_begin, coef, anti,
                                          center, g, g_bf16, s);
+    }
     if (fix)
         return launch_kind<KIND, CPT, 1>(b.r, b, K, T, d_out, skey, draw_begin, coef, anti, 0, g,
                                          g_bf16, s);
