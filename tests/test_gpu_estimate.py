@@ -28,8 +28,11 @@ W_CASES = [
     (65, 31, 513, 1, 123, 0),
     (16, 200, 2048, 1, 0, 0),
     (66, 77, 1024, 1, 4, dust.ANTITHETIC),  # two draw groups, ragged T
-    (8, 77, 1024, 1, 4, 0),                 # 32 channels per lane (<= 8 noise draws)
+    (8, 77, 1024, 1, 4, 0),                 # 32 channels per lane (d_out % 1024 == 0)
     (16, 45, 2048, 1, 2, dust.ANTITHETIC),  # the same with 8 antithetic pairs
+    (64, 50, 1024, 1, 3, 0),                # wide lanes, one whole group of 64 draws
+    (128, 33, 1024, 1, 2, dust.ANTITHETIC),  # wide lanes, 64 base draws
+    (100, 40, 1024, 1, 0, 0),               # more than 64 noise draws: narrow lanes
     (130, 17, 64, 0, 2, dust.ANTITHETIC),
     # packed signs: one 32-sign word per lane, 1024 channels per CTA
     (8, 100, 77, 3, 0, 0),            # a 13-channel last word
@@ -386,8 +389,12 @@ DIRECT_CASES = [
     (777, 96, 320, 16, 3, dust.CENTER | dust.ANTITHETIC, "bf16"),
     (300, 40, 72, 6, 1, 0, "f32"),                              # no centring, fp32 path
     (129, 64, 64, 1, 0, dust.CENTER, "f32"),                    # K = 1: centring is a no-op
-    (2003, 64, 1024, 16, 1, dust.CENTER | dust.ANTITHETIC, "bf16"),  # persistent, 8 pairs
-    (500, 40, 1024, 8, 1, dust.CENTER, "f32"),                 # persistent, fp32 g
+    (2003, 64, 1024, 16, 1, dust.CENTER | dust.ANTITHETIC, "bf16"),  # wide lanes, 8 pairs
+    (500, 40, 1024, 8, 1, dust.CENTER, "f32"),                 # wide lanes, fp32 g
+    (1500, 64, 2048, 32, 1, dust.CENTER, "bf16"),              # wide lanes, a draw in every lane
+    (900, 64, 1024, 32, 1, dust.CENTER | dust.ANTITHETIC, "bf16"),  # wide lanes, 16 pairs
+    (700, 64, 1024, 32, 3, dust.CENTER, "bf16"),               # packed signs, 32 draws
+    (333, 48, 1000, 32, 1, dust.CENTER, "bf16"),               # narrow Gaussian lanes, staged
 ]
 
 

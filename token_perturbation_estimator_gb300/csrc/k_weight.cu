@@ -376,12 +376,14 @@ cudaError_t launch_weight(const ScanBuffers& b, bool fix, int64_t K, int64_t T, 
     if (T == 0 || d_out == 0) return cudaSuccess;
     const uint32_t skey = seed_key(seed);
     const int c = center ? 1 : 0;
-    // Wide Gaussian lanes where a token has few noise draws (the per-draw and
-    // per-thread overheads then weigh most) and the CTAs of 1024 channels are
-    // whole; with more draws the narrower lanes' occupancy wins (measured:
-    // K 8 weighting 139 -> 135.5 us; K 16 and 64 about 1 % slower wide).
+    // Wide Gaussian lanes where the CTAs of 1024 channels are whole: the
+    // per-draw shared-memory or shuffle reads and the per-thread setup and
+    // store spread over twice the pairs. Measured on 8 to 64 noise draws
+    // (weighting: up-projection K 8 139 -> 135.5 us, K 16 257 -> 250 us,
+    // K 64 957 -> 942 us; 4096^2 K 64 3775 -> 3739 us; qkv K 16 373 -> 368 us);
+    // longer draw loops keep the narrow lanes.
     const int64_t noise_draws = anti ? K / 2 : K;
-    if (kind == 1 && d_out % (32 * kCptWide) == 0 && noise_draws <= 8)
+    if (kind == 1 && d_out % (32 * kCptWide) == 0 && noise_draws <= 64)
         return launch_src<1, kCptWide>(delta, b, fix, K, T, d_out, skey, draw_begin, coef, anti, c,
                                        g, g_bf16, s);
     if (kind == 1)
