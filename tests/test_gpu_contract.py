@@ -25,6 +25,8 @@ SHAPES = [
     (8192, 512, 4096),     # 2 slices
     (4096, 512, 1152),     # 8 slices
     (2048, 512, 2560),     # 3 slices: row blocks of 43, 43, 42
+    (2000, 256, 3840),     # 5 slices: row blocks of 26, the last 24
+    (2000, 256, 2688),     # 7 slices: row blocks of 19, the last 14
     (16384, 256, 256),     # 64 slices: partials
 ]
 

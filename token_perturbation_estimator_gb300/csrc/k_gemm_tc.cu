@@ -40,7 +40,11 @@ namespace {
 #ifndef DUST_GEMM_CLUSTER_REDUCE
 #define DUST_GEMM_CLUSTER_REDUCE 1  // reduce the token slices in a cluster (else partials)
 #endif
+#ifndef DUST_GEMM_PULL
+#define DUST_GEMM_PULL 1  // slices pulled by the summing CTA (else pushed to it)
+#endif
 constexpr bool kClusterReduce = DUST_GEMM_CLUSTER_REDUCE != 0;
+constexpr bool kPull = DUST_GEMM_PULL != 0;
 constexpr int kMT = DUST_GEMM_MT;
 constexpr int kBM = 128 * kMT, kBN = DUST_GEMM_BN, kBK = DUST_GEMM_BK, kStages = DUST_GEMM_STAGES;
 constexpr int kBoxBytes = 64 * kBK * 2;                 // one 64-wide bf16 box of kBK rows
@@ -153,6 +157,87 @@ __device__ void cluster_reduce(unsigned char* smem, uint32_t tmem, bool ok, int6
         }
         *p = o;
     }
+}
+
+__device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_shared_v4f(uint32_t addr, float a, float b, float c, float d) {
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c),
+                 "f"(d)
+                 : "memory");
+}
+
+static_assert(128 * kRowPad * 4 <= kStages * kStageBytes, "a whole tile fits in the stage buffers");
+
+// The same reduction with each CTA's whole fp32 tile staged in its own shared
+// memory (one row per lane, local stores) and the row blocks pulled: CTA d
+// reads its rows from every CTA of the cluster, in slice order, with loads
+// that run along the rows. A third cluster barrier keeps every tile in place
+// until all its readers are done.
+__device__ void cluster_reduce_pull(unsigned char* smem, uint32_t tmem, bool ok, int64_t m0,
+                                    int64_t n0, int64_t d_in, int64_t d_out,
+                                    float* __restrict__ gW, float scale, bool accumulate) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = static_cast<int>(gridDim.z);
+    const int R = (128 + S - 1) / S;  // rows summed by each CTA (the last may have fewer)
+    const uint32_t me = cluster_rank();
+    const int r0 = static_cast<int>(me) * R;
+    const int R_me = (128 - r0 < R) ? 128 - r0 : R;
+    float* tile = reinterpret_cast<float*>(smem);  // [128][kRowPad]
+    cluster_sync_all();  // every CTA's main loop is over: its stage buffers are free
+    if (warp >= 2 && ok) {
+        const int q = warp & 3;
+        const uint32_t dst = tc::smem_u32(tile + (32 * q + lane) * kRowPad);
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+            float v[32];
+            tc::tmem_ld_32x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + c * 32, v);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                st_shared_v4f(dst + 4u * (c * 32 + 4 * u), v[4 * u], v[4 * u + 1], v[4 * u + 2],
+                              v[4 * u + 3]);
+        }
+    }
+    cluster_sync_all();  // every tile is in place
+    const uint32_t base = tc::smem_u32(tile);
+    const int n4 = kBN / 4;
+    for (int e = threadIdx.x; e < R_me * n4; e += blockDim.x) {
+        const int rr = e / n4, c4 = e - rr * n4;
+        const int64_t row = m0 + r0 + rr;
+        const int64_t col = n0 + 4 * c4;
+        if (row >= d_out || col >= d_in) continue;
+        const uint32_t a = base + 4u * static_cast<uint32_t>((r0 + rr) * kRowPad + 4 * c4);
+        // All S loads issued before the sums, which then run in slice order.
+        float4 w[kMaxClusterSlices];
+#pragma unroll
+        for (int z = 0; z < kMaxClusterSlices; ++z)
+            if (z < S) w[z] = ld_cluster_v4(map_to_rank(a, static_cast<uint32_t>(z)));
+        float4 v = w[0];
+#pragma unroll
+        for (int z = 1; z < kMaxClusterSlices; ++z) {
+            if (z < S) {
+                v.x += w[z].x;
+                v.y += w[z].y;
+                v.z += w[z].z;
+                v.w += w[z].w;
+            }
+        }
+        float4 o = make_float4(scale * v.x, scale * v.y, scale * v.z, scale * v.w);
+        float4* p = reinterpret_cast<float4*>(gW + row * d_in + col);  // d_in % 8 == 0
+        if (accumulate) {
+            const float4 a = *p;
+            o = make_float4(a.x + o.x, a.y + o.y, a.z + o.z, a.w + o.w);
+        }
+        *p = o;
+    }
+    cluster_sync_all();  // no CTA leaves while another still reads its tile
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -310,8 +395,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (mode >= 3) {
         __syncthreads();
-        cluster_reduce(smem, tmem, !*abort_flag && n_k > 0, m0, n0, d_in, d_out, out, scale,
-                       mode == 4);
+        if (kPull)
+            cluster_reduce_pull(smem, tmem, !*abort_flag && n_k > 0, m0, n0, d_in, d_out, out,
+                                scale, mode == 4);
+        else
+            cluster_reduce(smem, tmem, !*abort_flag && n_k > 0, m0, n0, d_in, d_out, out, scale,
+                           mode == 4);
     }
     tc::tc_fence_before();
     __syncthreads();
