@@ -340,49 +340,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) *abort_flag = 1;
         if (ok && !*abort_flag && n_k > 0 && mode < 3) {
             const int q = warp & 3;  // TMEM lane quarter this warp may access
+            // The warp's 32 accumulator rows go through the idle stage buffers
+            // (one row per lane in, then rows out with consecutive lanes on
+            // consecutive columns), so each store instruction covers 512
+            // contiguous bytes of a row: also where GW is host memory mapped
+            // into the device, which takes scattered 16-byte writes slowly.
+            float* rows = reinterpret_cast<float*>(smem) + q * 32 * kRowPad;
+            const uint32_t rows_s = tc::smem_u32(rows) + 4u * static_cast<uint32_t>(lane * kRowPad);
 #pragma unroll 1
             for (int mt = 0; mt < kMT; ++mt) {
-                const int64_t row = m0 + 128 * mt + 32 * q + lane;
-                float* dst = nullptr;
-                if (row < d_out) {
-                    dst = (mode == 0)
-                              ? out + (static_cast<int64_t>(blockIdx.z) * d_out + row) * d_in
-                              : out + row * d_in;
-                }
 #pragma unroll 1
                 for (int c = 0; c < kBN / 32; ++c) {
                     float v[32];
                     tc::tmem_ld_32x32(
                         tmem + (static_cast<uint32_t>(32 * q) << 16) + mt * kBN + c * 32, v);
-                    const int64_t j0 = n0 + c * 32;
-                    if (!dst || j0 >= d_in) continue;
-                    if (j0 + 32 <= d_in) {
 #pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            float4 w4 = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2],
-                                                    v[4 * u + 3]);
-                            float4* p = reinterpret_cast<float4*>(dst + j0 + 4 * u);
-                            if (mode == 0) {
-                                *p = w4;
-                            } else if (mode == 1) {
-                                *p = make_float4(scale * w4.x, scale * w4.y, scale * w4.z,
-                                                 scale * w4.w);
-                            } else {
-                                float4 o = *p;
-                                *p = make_float4(o.x + scale * w4.x, o.y + scale * w4.y,
-                                                 o.z + scale * w4.z, o.w + scale * w4.w);
-                            }
-                        }
-                    } else {
+                    for (int u = 0; u < 8; ++u)
+                        st_shared_v4f(rows_s + 4u * (c * 32 + 4 * u), v[4 * u], v[4 * u + 1],
+                                      v[4 * u + 2], v[4 * u + 3]);
+                }
+                __syncwarp();
+#pragma unroll 1
+                for (int rr = 0; rr < 32; ++rr) {
+                    const int64_t row = m0 + 128 * mt + 32 * q + rr;
+                    if (row >= d_out) break;
+                    float* dst = (mode == 0)
+                                     ? out + (static_cast<int64_t>(blockIdx.z) * d_out + row) * d_in
+                                     : out + row * d_in;
 #pragma unroll
-                        for (int u = 0; u < 32; ++u) {
-                            if (j0 + u >= d_in) continue;
-                            if (mode == 0) dst[j0 + u] = v[u];
-                            else if (mode == 1) dst[j0 + u] = scale * v[u];
-                            else dst[j0 + u] += scale * v[u];
+                    for (int c4 = lane; c4 < kBN / 4; c4 += 32) {
+                        const int64_t col = n0 + 4 * c4;
+                        if (col >= d_in) break;  // d_in % 8 == 0: the float4 is whole
+                        const float4 w4 = *reinterpret_cast<const float4*>(rows + rr * kRowPad + 4 * c4);
+                        float4* p = reinterpret_cast<float4*>(dst + col);
+                        if (mode == 0) {
+                            *p = w4;
+                        } else if (mode == 1) {
+                            *p = make_float4(scale * w4.x, scale * w4.y, scale * w4.z,
+                                             scale * w4.w);
+                        } else {
+                            const float4 o = *p;
+                            *p = make_float4(o.x + scale * w4.x, o.y + scale * w4.y,
+                                             o.z + scale * w4.z, o.w + scale * w4.w);
                         }
                     }
                 }
+                __syncwarp();  // the rows are read before the next accumulator's land
             }
         }
     }
