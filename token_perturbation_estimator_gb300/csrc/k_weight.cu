@@ -44,9 +44,9 @@ namespace {
 #define DUST_WEIGHT_MINB_R 4
 #endif
 // Gaussian with 32 channels per lane (16 Box-Muller pairs per draw, for d_out
-// a multiple of 1024 and at most 8 noise draws per token): the per-draw
-// shared-memory reads and the per-thread setup and store spread over twice
-// the pairs, at 3 resident CTAs per SM.
+// a multiple of 1024 and at most 64 noise draws per token): the per-draw
+// reads and the per-thread setup and store spread over twice the pairs, at 3
+// resident CTAs per SM.
 #ifndef DUST_WEIGHT_MINB_GW
 #define DUST_WEIGHT_MINB_GW 3
 #endif
