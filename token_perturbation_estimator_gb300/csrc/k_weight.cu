@@ -7,13 +7,15 @@
 //
 // Mapping: one warp per token, CPT channels per lane (CPT/2 Box-Muller pairs
 // or CPT signs; packed signs: the 32 channels of one hash word; Gaussian with
-// d_out a multiple of 1024: 32 channels), 8 tokens x
-// 32 lanes' channels per CTA. The per-draw keys and the
-// per-token rewards (already multiplied by -1/(K sigma); for antithetic pairs,
-// the pair's reward difference, one per base draw) are staged in shared
-// memory 64 draws at a time and read as warp-wide broadcasts. The per-channel counters are pre-folded once
-// per thread, so each element-draw costs the hash tail plus one FMA
-// (Rademacher: the sign bit is xor-ed into the reward's sign bit).
+// d_out a multiple of 1024: 32 channels), 8 tokens x 32 lanes' channels per
+// CTA. The per-token rewards are already multiplied by -1/(K sigma); for
+// antithetic pairs they are the pair's reward difference, one per base draw.
+// They and the per-draw keys are staged in shared memory 64 draws at a time
+// and read as warp-wide broadcasts. Source 2 (below) is the exception: its
+// rewards are shuffled from lane to lane and its keys come from the host. The
+// per-channel counters are pre-folded once per thread, so each element-draw
+// costs the hash tail plus one FMA (Rademacher: the sign bit is xor-ed into
+// the reward's sign bit).
 //
 // Reward sources (SRC): the credit scan's token-major rewards r [T][K]
 // (0), the same plus the scan's chunk carry P[t] carry[chunk][i] (1), or,
