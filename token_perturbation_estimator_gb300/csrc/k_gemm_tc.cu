@@ -7,12 +7,14 @@
 // terms): A = g^T is read from g [T][d_out], B = X from X [T][d_in]. TMA
 // brings 64 x 64 boxes with the 128-byte swizzle into a 4-stage ring; one
 // thread issues the MMAs (M = 128 channels, N = 256 inputs, K = 16 tokens)
-// and commits each stage back to the loader; four warps drain TMEM.
+// and commits each stage back to the loader; four warps drain TMEM through
+// the idle stage buffers, so that GW is stored along its rows.
 //
 // Tile of one CTA: 128 channels x 256 inputs x one slice of the tokens. When
 // the output tiles alone cannot fill the GPU, the tokens are cut into S
-// fixed slices whose fp32 partials are summed afterwards in slice order, so
-// the result does not depend on scheduling.
+// fixed slices whose fp32 partials are summed in slice order, so the result
+// does not depend on scheduling: inside a thread-block cluster of the S CTAs
+// when all clusters fit at once, else by a reduction kernel.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
