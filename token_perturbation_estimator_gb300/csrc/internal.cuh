@@ -14,6 +14,11 @@ namespace dust {
 // device; read and cleared by dust_last_error. nullptr if the lookup failed.
 unsigned int* status_word();
 
+// Raises `kernel`'s dynamic shared-memory limit to at least `bytes` on the
+// current device. The attribute belongs to the device, so it is set once
+// per (kernel, device), under a lock, for processes that use several GPUs.
+cudaError_t ensure_smem_limit(const void* kernel, int bytes);
+
 // Kernel families timed by dust_profile_read.
 enum Stage {
     kStageScanLocal, kStageScanCarry, kStageScanFixup, kStageWeight, kStageGemmSimt,
@@ -99,7 +104,7 @@ struct ScanBuffers {
     float* r;       // [T][K] local (chunk) scan, or final after fix-up
     float* P;       // [T] product of the decay from t to its chunk's end
     float* A;       // [n_chunks][K] chunk summary: local r at the chunk start
-    float* B;       // [n_chunks]   chunk summary: decay product over the chunk
+    float* B;       // [n_chunks][2] chunk summary: decay product over the chunk, hi + lo
     float* carry;   // [n_chunks][K] true r at the first token after the chunk
     int64_t n_chunks;
 };

@@ -443,12 +443,8 @@ int sm_count() {
 template <int KIND, bool ALIGNED>
 cudaError_t launch_kind(const CUtensorMap& tx, const CUtensorMap& tw, const CUtensorMap& ty,
                         const FwdArgs& fa, dim3 grid, cudaStream_t s) {
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(k_forward<KIND, ALIGNED>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    });
+    const cudaError_t attr =
+        ensure_smem_limit(reinterpret_cast<const void*>(k_forward<KIND, ALIGNED>), kSmemBytes);
     if (attr != cudaSuccess) return attr;
     FwdArgs f = fa;
     const int nbuf = (kSplitBytes - f.stages * kStageBytes) / (ew_of(KIND) * kBufBytes);

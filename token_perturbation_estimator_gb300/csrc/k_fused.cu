@@ -423,16 +423,10 @@ cudaError_t launch_fused(const ScanBuffers& b, const void* X, int64_t K, int64_t
                          cudaStream_t s) {
     CUtensorMap tx;
     if (!make_tmap_bf16(&tx, X, T, d_in, kBK)) return cudaErrorInvalidValue;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(k_fused<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        kSmemBytes);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(k_fused<1>,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            kSmemBytes);
-    });
+    cudaError_t attr_err =
+        ensure_smem_limit(reinterpret_cast<const void*>(k_fused<0>), kSmemBytes);
+    if (attr_err == cudaSuccess)
+        attr_err = ensure_smem_limit(reinterpret_cast<const void*>(k_fused<1>), kSmemBytes);
     if (attr_err != cudaSuccess) return attr_err;
     unsigned int* st = status_word();
     if (!st) return cudaErrorUnknown;

@@ -486,9 +486,12 @@ namespace {
 // wave; the fp32 partials then win (measured on the 48-site sweep: 6-CTA
 // clusters 5.1 ms of contraction against 4.3 ms with partials).
 bool cluster_fits(int S, int64_t tiles) {
-    static int max_active[kMaxClusterSlices + 1] = {};
-    static std::once_flag once[kMaxClusterSlices + 1];
-    std::call_once(once[S], [S] {
+    constexpr int kMaxDev = 64;
+    static int max_active[kMaxDev][kMaxClusterSlices + 1] = {};
+    static std::once_flag once[kMaxDev][kMaxClusterSlices + 1];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return false;
+    std::call_once(once[dev][S], [S, dev] {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(1, 1, static_cast<unsigned>(S));
         cfg.blockDim = dim3(kThreads);
@@ -501,14 +504,14 @@ bool cluster_fits(int S, int64_t tiles) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes) != cudaSuccess ||
+        if (ensure_smem_limit(reinterpret_cast<const void*>(k_gemm_tc), kSmemBytes) !=
+                cudaSuccess ||
             cudaOccupancyMaxActiveClusters(&n, k_gemm_tc, &cfg) != cudaSuccess)
             n = 0;
         (void)cudaGetLastError();
-        max_active[S] = n;
+        max_active[dev][S] = n;
     });
-    return tiles <= max_active[S];
+    return tiles <= max_active[dev][S];
 }
 
 }  // namespace
@@ -519,12 +522,8 @@ cudaError_t launch_tc_gemm(const void* g, const void* X, int64_t T, int64_t d_in
     CUtensorMap ta, tb;
     if (!make_tmap_bf16(&ta, g, T, d_out, kBK) || !make_tmap_bf16(&tb, X, T, d_in, kBK))
         return cudaErrorInvalidValue;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        kSmemBytes);
-    });
+    const cudaError_t attr_err =
+        ensure_smem_limit(reinterpret_cast<const void*>(k_gemm_tc), kSmemBytes);
     if (attr_err != cudaSuccess) return attr_err;
     unsigned int* st = status_word();
     if (!st) return cudaErrorUnknown;

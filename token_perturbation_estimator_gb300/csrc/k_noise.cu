@@ -1,6 +1,8 @@
 // Materialising noise kernel (dust_noise) and the forward's jitter
 // y += sigma * a (dust_jitter_apply). Both walk channel pairs so one
 // Box-Muller evaluation serves both channels of a pair.
+#include <mutex>
+
 #include "internal.cuh"
 #include "noise.cuh"
 
@@ -179,6 +181,29 @@ unsigned int* status_word() {
         cache[dev] = static_cast<unsigned int*>(p);
     }
     return cache[dev];
+}
+
+cudaError_t ensure_smem_limit(const void* kernel, int bytes) {
+    struct Entry {
+        const void* kernel;
+        int dev;
+        int bytes;
+    };
+    constexpr int kMaxEntries = 256;
+    static Entry done[kMaxEntries];
+    static int n_done = 0;
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < n_done; ++i)
+        if (done[i].kernel == kernel && done[i].dev == dev && done[i].bytes >= bytes)
+            return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    if (n_done < kMaxEntries) done[n_done++] = Entry{kernel, dev, bytes};
+    return cudaSuccess;
 }
 
 cudaError_t launch_zero(float* p, int64_t n, cudaStream_t s) {

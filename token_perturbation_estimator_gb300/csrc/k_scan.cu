@@ -10,6 +10,16 @@
 //   chunks : one thread per draw walks the chunk maps from the end (k_carry).
 // A chunk's tokens then take r_true[t] = r_local[t] + P[t] * carry[chunk],
 // with P[t] the product of m from t to the chunk's last token.
+//
+// Precision of the decay products. A product of k factors gamma rounded to
+// fp32 after every factor drifts by up to about k/2 units in the last place,
+// and the drift of the chunk product B (the same for every full chunk)
+// compounds along the chunk carries: at gamma = 0.9999 over 300,000 tokens
+// that alone gave 3e-5 relative error in r. So P and B are multiplied out in
+// fp64 and each rounded once; B is kept as an fp32 pair hi + lo (hi the
+// rounded product, lo the rounded remainder), and each carry step applies
+// both, so the rounding of B no longer compounds. What remains is fp32
+// rounding of the sums, which does not drift.
 #include "internal.cuh"
 
 namespace dust {
@@ -19,6 +29,9 @@ namespace {
 constexpr int kDrawGroup = 32;       // draws staged in shared memory at once
 constexpr int64_t kCoopOffsets = 4096;  // up to this many sequences, scan all offsets
 constexpr size_t kCarrySmem = 96 * 1024;  // chunk summaries staged by k_carry
+// Chunks whose decay products (hi + lo pairs) the scan kernel's last CTA can
+// stage beside the draw summaries for the merged carry pass.
+constexpr int64_t kMergedChunks = 512;
 
 // m[t] for the 256 tokens of a chunk: 0 where t is the last token of its
 // sequence (t + 1 is an offset in seq_offsets[1..n_seq]) or t >= T.
@@ -34,6 +47,42 @@ __device__ float decay_of(int64_t t, int64_t T, const int32_t* __restrict__ so, 
         if (v < key) lo = mid + 1; else hi = mid - 1;
     }
     return gamma;
+}
+
+// dst[e] = src[e] for e < n, by the whole CTA, loads batched 8 deep (read
+// through L2: src was written by other CTAs of this grid or the previous one).
+__device__ __forceinline__ void stage_cg(float* dst, const float* __restrict__ src, int64_t n) {
+    for (int64_t e0 = threadIdx.x; e0 < n; e0 += 8 * static_cast<int64_t>(blockDim.x)) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int64_t e = e0 + u * static_cast<int64_t>(blockDim.x);
+            v[u] = e < n ? __ldcg(src + e) : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int64_t e = e0 + u * static_cast<int64_t>(blockDim.x);
+            if (e < n) dst[e] = v[u];
+        }
+    }
+}
+
+// carry[j][i] = A[j+1][i] + B[j+1] * carry[j+1][i], carry[last] = 0, one
+// thread per draw, with B[j] = hi + lo (Bp[2j], Bp[2j+1]) applied as two
+// fused steps so that B's rounding does not compound.
+__device__ __forceinline__ void carry_walk(const float* A, const float* Bp, int64_t K,
+                                           int64_t nc, float* __restrict__ carry) {
+    for (int64_t i = threadIdx.x; i < K; i += blockDim.x) {
+        float c = 0.0f;
+        carry[(nc - 1) * K + i] = 0.0f;
+        // Unrolled so that the loads of later steps are issued ahead of the
+        // serial chain of fused multiply-adds.
+#pragma unroll 8
+        for (int64_t j = nc - 1; j >= 1; --j) {
+            c = fmaf(Bp[2 * j + 1], c, fmaf(Bp[2 * j], c, A[j * K + i]));
+            carry[(j - 1) * K + i] = c;
+        }
+    }
 }
 
 __global__ void __launch_bounds__(256) k_scan_local(const float* __restrict__ delta, int64_t K,
@@ -91,32 +140,14 @@ __global__ void __launch_bounds__(256) k_scan_local(const float* __restrict__ de
     }
     __syncthreads();
 
-    // Lane maps of the decay products (draw-independent): P for the lane's 8
-    // tokens, then the suffix over the lanes after it.
+    // Lane map of the decay (draw-independent): the lane's product Bl of its
+    // 8 factors, for the per-draw composition below.
     float mloc[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) mloc[j] = s_m[lane * 8 + j];
     float Bl = 1.0f;
 #pragma unroll
     for (int j = 7; j >= 0; --j) Bl *= mloc[j];
-    // Inclusive suffix product of Bl over lanes >= lane.
-    float Bsuf = Bl;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const float o = __shfl_down_sync(0xffffffffu, Bsuf, off);
-        if (lane + off < 32) Bsuf *= o;
-    }
-    float Bnext = __shfl_down_sync(0xffffffffu, Bsuf, 1);
-    if (lane == 31) Bnext = 1.0f;
-    if (warp == 0) {
-        float p = Bnext;
-        for (int j = 7; j >= 0; --j) {
-            p *= mloc[j];
-            const int64_t tt = t0 + lane * 8 + j;
-            if (tt < T) P[tt] = p;
-        }
-        if (lane == 0) B[chunk] = Bsuf;
-    }
 
     for (int64_t g0 = 0; g0 < K; g0 += kDrawGroup) {
         const int gn = static_cast<int>(K - g0 < kDrawGroup ? K - g0 : kDrawGroup);
@@ -127,6 +158,35 @@ __global__ void __launch_bounds__(256) k_scan_local(const float* __restrict__ de
 #pragma unroll
             for (int k = 0; k < kDrawGroup; ++k)
                 v[k] = (k < gn && t < T) ? delta[(g0 + k) * T + t] : 0.0f;
+            // While the first group's loads are in flight, warp 0 multiplies
+            // out the chunk's decay products in fp64 (a chain of about 20
+            // dependent double-precision steps): the suffix over the lanes
+            // after each lane, P for the lane's 8 tokens, and the chunk
+            // product B as an fp32 pair.
+            if (g0 == 0 && warp == 0) {
+                double Bl_d = 1.0;
+#pragma unroll
+                for (int j = 7; j >= 0; --j) Bl_d *= static_cast<double>(mloc[j]);
+                double Bsuf = Bl_d;  // inclusive suffix product over lanes >= lane
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const double o = __shfl_down_sync(0xffffffffu, Bsuf, off);
+                    if (lane + off < 32) Bsuf *= o;
+                }
+                double p = __shfl_down_sync(0xffffffffu, Bsuf, 1);
+                if (lane == 31) p = 1.0;
+#pragma unroll
+                for (int j = 7; j >= 0; --j) {
+                    p *= static_cast<double>(mloc[j]);
+                    const int64_t tt = t0 + lane * 8 + j;
+                    if (tt < T) P[tt] = static_cast<float>(p);
+                }
+                if (lane == 0) {
+                    const float hi = static_cast<float>(Bsuf);
+                    B[2 * chunk] = hi;
+                    B[2 * chunk + 1] = static_cast<float>(Bsuf - static_cast<double>(hi));
+                }
+            }
 #pragma unroll
             for (int k = 0; k < kDrawGroup; ++k)
                 if (k < gn) s_c[k][tid] = (t < T) ? -(v[k] - mean) : 0.0f;
@@ -171,7 +231,8 @@ __global__ void __launch_bounds__(256) k_scan_local(const float* __restrict__ de
     }
     if (!ticket) return;
     // The last CTA to finish runs the carry pass over all chunk summaries
-    // (the host picks this form only when they fit in s_c).
+    // (the host picks this form only when the draw summaries fit in s_c and
+    // the chunk products in s_B).
     __shared__ unsigned int s_last;
     __threadfence();
     __syncthreads();
@@ -180,49 +241,33 @@ __global__ void __launch_bounds__(256) k_scan_local(const float* __restrict__ de
     if (!s_last) return;
     __threadfence();
     const int64_t nc = gridDim.x;
+    __shared__ float s_B[2 * kMergedChunks];
     float* sA = &s_c[0][0];
-    float* sB = sA + nc * K;
-    for (int64_t e = tid; e < nc * K; e += blockDim.x) sA[e] = __ldcg(A + e);
-    for (int64_t e = tid; e < nc; e += blockDim.x) sB[e] = __ldcg(B + e);
+    stage_cg(sA, A, nc * K);
+    stage_cg(s_B, B, 2 * nc);
     __syncthreads();
-    for (int64_t i = tid; i < K; i += blockDim.x) {
-        float c = 0.0f;
-        carry[(nc - 1) * K + i] = 0.0f;
-        for (int64_t j = nc - 1; j >= 1; --j) {
-            c = fmaf(sB[j], c, sA[j * K + i]);
-            carry[(j - 1) * K + i] = c;
-        }
-    }
+    carry_walk(sA, s_B, K, nc, carry);
 }
 
-// carry[j][i] = A[j+1][i] + B[j+1] * carry[j+1][i], carry[last] = 0.
-// The summaries are first staged in shared memory by all threads (when they
-// fit), so the serial chain of each draw runs at shared-memory latency.
+// The carry pass as its own one-CTA kernel (see carry_walk). The summaries
+// are first staged in shared memory by all threads (when they fit), so the
+// serial chain of each draw runs at shared-memory latency.
 __global__ void __launch_bounds__(256) k_carry(const float* __restrict__ A,
                                                const float* __restrict__ B, int64_t K,
                                                int64_t n_chunks, float* __restrict__ carry,
                                                int staged) {
     pdl_wait();
     pdl_trigger();
-    extern __shared__ float s_sum[];  // [n_chunks][K] A, then [n_chunks] B
-    const float* sA = A;
-    const float* sB = B;
+    extern __shared__ float s_sum[];  // [n_chunks][K] A, then [n_chunks][2] B
     if (staged) {
         float* dA = s_sum;
         float* dB = s_sum + n_chunks * K;
-        for (int64_t e = threadIdx.x; e < n_chunks * K; e += blockDim.x) dA[e] = A[e];
-        for (int64_t e = threadIdx.x; e < n_chunks; e += blockDim.x) dB[e] = B[e];
+        stage_cg(dA, A, n_chunks * K);
+        stage_cg(dB, B, 2 * n_chunks);
         __syncthreads();
-        sA = dA;
-        sB = dB;
-    }
-    for (int64_t i = threadIdx.x; i < K; i += blockDim.x) {
-        float c = 0.0f;
-        carry[(n_chunks - 1) * K + i] = 0.0f;
-        for (int64_t j = n_chunks - 1; j >= 1; --j) {
-            c = fmaf(sB[j], c, sA[j * K + i]);
-            carry[(j - 1) * K + i] = c;
-        }
+        carry_walk(dA, dB, K, n_chunks, carry);
+    } else {
+        carry_walk(A, B, K, n_chunks, carry);
     }
 }
 
@@ -248,7 +293,7 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 size_t scan_workspace_bytes(int64_t K, int64_t T) {
     const int64_t nc = (T + kScanChunk - 1) / kScanChunk;
     return align256(sizeof(float) * K * T + 16) + align256(sizeof(float) * T + 16) +
-           2 * align256(sizeof(float) * nc * K + 16) + align256(sizeof(float) * nc + 16);
+           2 * align256(sizeof(float) * nc * K + 16) + align256(sizeof(float) * 2 * nc + 16);
 }
 
 ScanBuffers scan_carve(void* ws, int64_t K, int64_t T) {
@@ -273,8 +318,8 @@ cudaError_t launch_scan(const float* delta, int64_t K, int64_t T, const int32_t*
     if (T == 0 || K == 0) return cudaSuccess;
     // Carry pass inside the scan kernel's last CTA when the chunk summaries
     // fit in its shared staging buffer and a zeroed ticket word is provided.
-    const bool merged =
-        ticket && b.n_chunks * (K + 1) <= static_cast<int64_t>(kDrawGroup) * (kScanChunk + 1);
+    const bool merged = ticket && b.n_chunks <= kMergedChunks &&
+                        b.n_chunks * K <= static_cast<int64_t>(kDrawGroup) * (kScanChunk + 1);
     cudaError_t e;
     {
     ProfScope ps(kStageScanLocal, s);
@@ -283,10 +328,10 @@ cudaError_t launch_scan(const float* delta, int64_t K, int64_t T, const int32_t*
                    merged ? ticket : nullptr);
     }
     if (e != cudaSuccess || merged) return e;
-    const size_t smem = sizeof(float) * static_cast<size_t>(b.n_chunks * (K + 1));
+    const size_t smem = sizeof(float) * static_cast<size_t>(b.n_chunks * (K + 2));
     const int staged = smem <= kCarrySmem ? 1 : 0;
-    static cudaError_t attr = cudaFuncSetAttribute(
-        k_carry, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kCarrySmem));
+    const cudaError_t attr =
+        ensure_smem_limit(reinterpret_cast<const void*>(k_carry), static_cast<int>(kCarrySmem));
     if (attr != cudaSuccess) return attr;
     ProfScope ps(kStageScanCarry, s);
     return launch_pdl(k_carry, dim3(1), dim3(256), staged ? smem : 0, s, b.A, b.B, K, b.n_chunks,

@@ -34,11 +34,11 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Bytes of scratch one scan of K draws over T tokens needs: P [T],
-// A [n_chunks][K], carry [n_chunks][K], B [n_chunks].
+// A [n_chunks][K], carry [n_chunks][K], B [n_chunks][2].
 size_t noalloc_need(int64_t K, int64_t T) {
     const int64_t nc = (T + kScanChunk - 1) / kScanChunk;
     return round256(sizeof(float) * T) + 2 * round256(sizeof(float) * nc * K) +
-           round256(sizeof(float) * nc);
+           round256(sizeof(float) * 2 * nc);
 }
 
 // Device address of g_noalloc_scratch on the current device (nullptr on
