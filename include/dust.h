@@ -389,6 +389,54 @@ dust_status dust_estimate_gW_host(const void* X_host, void* X_dev, dust_dtype x_
                                   void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * dust_estimate_gW_host_sites — dust_estimate_gW_host for several layers
+ * ("sites") in one stream-ordered pass, as in the page's section "What the
+ * released code actually does" (one update covers every linear layer):
+ * sites[i] is computed exactly as dust_estimate_gW_host would compute it with
+ * that site's arguments and the shared x_dtype, kind, draw_begin, scale and
+ * flags, and the results are bit-identical to such calls made one after
+ * another. What differs is the copying: the inputs of later sites travel
+ * host -> device while earlier sites compute. Site 0's loss changes and
+ * offsets are copied on `stream`; then, on the internal copy stream and after
+ * everything enqueued on `stream` before this call, X of site 0 and, for each
+ * later site, its loss changes, offsets and X, in site order. Each site's
+ * kernels wait for its own loss changes before they start and for its X
+ * before the contraction. Every copy of the call has completed when the
+ * call's work on `stream` has (also on error paths).
+ *
+ * Because the copy stream writes a site's staging buffers (X_dev of every
+ * site; delta_dev and seq_dev of sites after the first) while earlier sites
+ * compute, those buffers must not overlap any device buffer of the call
+ * (any site's X_dev, delta_dev, seq_dev, gW_dev or workspace): checked on the
+ * host, DUST_ERR_INVALID_ARG otherwise. Every argument of every site is
+ * checked before anything is enqueued. At most 4096 sites (DUST_ERR_RANGE).
+ * gW_host follows dust_estimate_gW_host's rule (written in place over the
+ * host link when page-locked and device-mapped, else through gW_dev).
+ */
+typedef struct {
+    const void* X_host;              /* host [T][d_in], x_dtype; page-locked for overlap */
+    void* X_dev;                     /* device staging [T][d_in] */
+    int64_t T, d_in, d_out;
+    const float* delta_host;         /* host [K][T] loss changes */
+    float* delta_dev;                /* device staging [K][T] */
+    int64_t K;
+    const int32_t* seq_offsets_host; /* host [n_seq + 1] */
+    int32_t* seq_dev;                /* device staging [n_seq + 1] */
+    int64_t n_seq;
+    uint64_t seed;                   /* this site's noise seed */
+    float sigma, gamma;
+    float* gW_host;                  /* host [d_out][d_in] result */
+    float* gW_dev;                   /* device [d_out][d_in] */
+    void* workspace;                 /* device, dust_estimate_gW_workspace bytes */
+    size_t ws_bytes;
+} dust_host_site;
+
+dust_status dust_estimate_gW_host_sites(const dust_host_site* sites, int64_t n_sites,
+                                        dust_dtype x_dtype, dust_noise_kind kind,
+                                        int64_t draw_begin, float scale, uint32_t flags,
+                                        void* stream);
+
+/*
  * Per-kernel timing for benchmarks (no counterpart on the pages: this is
  * measurement plumbing). While enabled, every kernel the library launches is
  * bracketed by two CUDA events recorded on its stream; dust_profile_read
@@ -407,6 +455,45 @@ dust_status dust_profile_enable(int32_t on);
 /* Writes up to max_entries entries; returns how many were written (>= 0) or a
  * negative dust_status. */
 int32_t dust_profile_read(dust_profile_entry* out, int32_t max_entries);
+
+/*
+ * Pipe-rate probes for rooflines (no counterpart on the pages: measurement
+ * plumbing). dust_pipe_probe enqueues on `stream` one launch of a
+ * throughput kernel that keeps every SM's schedulers busy with independent
+ * chains of one kind of operation, written in inline PTX:
+ *   DUST_PIPE_XU     lg2.approx, sqrt.approx, sin.approx, cos.approx
+ *                    (the transcendentals of a Box-Muller pair), counted ops
+ *                    = those four instructions;
+ *   DUST_PIPE_ALU    two shr.b32 and one lop3.b32 per step (the integer ALU
+ *                    pipe), ops = all three;
+ *   DUST_PIPE_FMA    fma.rn.f32, ops = FLOP (2 per FMA);
+ *   DUST_PIPE_ISSUE  three fma.rn.f32 per lop3.b32, ops = lane instructions
+ *                    (neither pipe binds before instruction issue does).
+ * Each chain is nonlinear in its own state, so the assembler cannot fold
+ * steps together.
+ *
+ * *ops receives the number of counted operations the launch performs; the
+ * caller times the launch with CUDA events on `stream` and divides. `sink`
+ * is a device float buffer of at least dust_pipe_probe_threads() elements:
+ * each thread stores its result there only when the result's bits match a
+ * fixed NaN pattern, which keeps the chains live (in practice almost never).
+ * `steps` (1 .. 2^30, rounded up to a multiple of 4, which *ops counts)
+ * sets the launch's length: about 2^14 steps take a few milliseconds on a
+ * GB300. Returns DUST_ERR_INVALID_ARG for an unknown pipe, a bad step count
+ * or a null pointer.
+ */
+typedef enum {
+    DUST_PIPE_XU = 0,
+    DUST_PIPE_ALU = 1,
+    DUST_PIPE_FMA = 2,
+    DUST_PIPE_ISSUE = 3
+} dust_pipe;
+
+dust_status dust_pipe_probe(int32_t pipe, int64_t steps, double* ops, void* sink,
+                            void* stream);
+/* Threads of one probe launch (SM count x 4 CTAs x 512), i.e. the size of
+ * `sink` in floats; a negative dust_status if the device cannot be queried. */
+int32_t dust_pipe_probe_threads(void);
 
 /*
  * dust_debug_inject_timeout — test hook for the device-side failure path (no

@@ -184,3 +184,67 @@ def test_forward_jitter_validation(L):
     # nothing to write: OK without touching the device
     assert call(T=0, X=NULL, Y=NULL) == dust.OK
     assert call(n_draws=0, clean=0, X=NULL, W=NULL, Y=NULL) == dust.OK
+
+
+def test_binding_rejects_wrong_dtype_and_shape():
+    """The binding checks dtypes and shapes before any C call: the C ABI takes
+    raw pointers and sizes, so a float64 delta would be misread and an r of
+    the wrong shape written past its end."""
+    import torch
+    with pytest.raises(ValueError, match="float32"):
+        dust._scan_inputs(torch.zeros((4, 8), dtype=torch.float64), torch.zeros(2, dtype=torch.int32))
+    with pytest.raises(ValueError, match="int32"):
+        dust._scan_inputs(torch.zeros((4, 8)), torch.zeros(2, dtype=torch.int64))
+    with pytest.raises(ValueError, match="dimensions"):
+        dust._scan_inputs(torch.zeros(8), torch.zeros(2, dtype=torch.int32))
+    with pytest.raises(ValueError, match="shape"):
+        dust._expect(torch.zeros((8, 3)), "r", (torch.float32,), shape=(8, 4))
+    dust._expect(torch.zeros((8, 4)), "r", (torch.float32,), shape=(8, 4))
+    dust._expect(torch.zeros((8, 4), dtype=torch.bfloat16), "g",
+                 (torch.float32, torch.bfloat16), shape=(8, 4))
+
+
+def test_host_sites_validation_without_a_device(L):
+    """Argument errors of the multi-site host entry point are found on the
+    host before anything is enqueued: staging that overlaps another buffer,
+    too many sites, a bad site argument, a null site array."""
+    T, d_in, d_out, K = 1024, 256, 512, 8
+    ws = C.c_size_t(0)
+    assert L.dust_estimate_gW_workspace(C.byref(ws), T, d_in, d_out, K, dust.BF16,
+                                        dust.CENTER) == dust.OK
+
+    def site(base, seed):
+        # fake, 256-aligned, disjoint device addresses from `base`
+        return dust.HostSite(0x1000, base, T, d_in, d_out, 0x2000, base + (1 << 24), K,
+                             0x3000, base + (2 << 24), 4, seed, 1e-3, 0.0, 0x4000,
+                             base + (3 << 24), base + (4 << 24), ws.value)
+
+    arr = (dust.HostSite * 2)(site(1 << 32, 1), site(2 << 32, 2))
+    arr[1].X_dev = arr[0].workspace  # overlaps site 0's workspace
+    call = lambda a, n: L.dust_estimate_gW_host_sites(C.cast(a, C.c_void_p), n, dust.BF16,
+                                                       dust.GAUSSIAN, 0, 1.0, dust.CENTER, NULL)
+    assert call(arr, 2) == dust.ERR_INVALID_ARG
+    arr[1].X_dev = (2 << 32) + 64  # 16-byte aligned, disjoint again, but site 0's delta_dev
+    arr[1].delta_dev = arr[0].delta_dev  # shared with a copy-stream write of site 1
+    assert call(arr, 2) == dust.ERR_INVALID_ARG
+    arr2 = (dust.HostSite * 1)(site(1 << 32, 1))
+    arr2[0].ws_bytes = 16  # too small
+    assert call(arr2, 1) == dust.ERR_WORKSPACE
+    arr2[0].ws_bytes = ws.value
+    arr2[0].sigma = 0.0
+    assert call(arr2, 1) == dust.ERR_INVALID_ARG
+    assert L.dust_estimate_gW_host_sites(NULL, 1, dust.BF16, dust.GAUSSIAN, 0, 1.0,
+                                         dust.CENTER, NULL) == dust.ERR_INVALID_ARG
+    assert call(arr2, 5000) == dust.ERR_RANGE
+
+
+def test_pipe_probe_rejects_bad_arguments(L):
+    ops = C.c_double(0.0)
+    sink = C.c_void_p(1 << 32)
+    assert L.dust_pipe_probe(7, 100, C.byref(ops), sink, NULL) == dust.ERR_INVALID_ARG
+    assert L.dust_pipe_probe(-1, 100, C.byref(ops), sink, NULL) == dust.ERR_INVALID_ARG
+    assert L.dust_pipe_probe(dust.PIPE_XU, 0, C.byref(ops), sink, NULL) == dust.ERR_INVALID_ARG
+    assert L.dust_pipe_probe(dust.PIPE_XU, 1 << 31, C.byref(ops), sink,
+                             NULL) == dust.ERR_INVALID_ARG
+    assert L.dust_pipe_probe(dust.PIPE_XU, 100, None, sink, NULL) == dust.ERR_INVALID_ARG
+    assert L.dust_pipe_probe(dust.PIPE_XU, 100, C.byref(ops), NULL, NULL) == dust.ERR_INVALID_ARG

@@ -99,3 +99,58 @@ def test_host_path_accumulate_and_empty():
     got, _ = _host_call(Xe, de, se, d_out, dust.CENTER, gW_host=z)
     torch.cuda.synchronize()
     assert torch.count_nonzero(got).item() == 0
+
+
+def _site(X, delta, so, d_out, seed, gamma, dev, pinned_gw=True):
+    import torch
+    T, d_in = X.shape
+    K = delta.shape[0]
+    ws = torch.empty(max(256, dust.dust_estimate_gW_workspace(T, d_in, d_out, K,
+                                                              dust.BF16, dust.CENTER)),
+                     dtype=torch.uint8, device=dev)
+    gh = torch.full((d_out, d_in), float("nan"))
+    return {"X_host": X.pin_memory(), "X_dev": torch.empty_like(X, device=dev),
+            "delta_host": delta.pin_memory(), "delta_dev": torch.empty_like(delta, device=dev),
+            "seq_host": so.pin_memory(), "seq_dev": torch.empty_like(so, device=dev),
+            "gW_host": gh.pin_memory() if pinned_gw else gh,
+            "gW_dev": torch.empty((d_out, d_in), dtype=torch.float32, device=dev),
+            "workspace": ws, "seed": seed, "sigma": 1e-3, "gamma": gamma}
+
+
+@pytest.mark.parametrize("pinned_gw", [True, False])
+def test_host_sites_match_device_calls(pinned_gw):
+    """Three layers of different shapes, decays and seeds in one pass, twice
+    in a row on a user stream: each result equals the device entry point's
+    for that site, bit for bit (mapped or copied-back ĜW)."""
+    import torch
+    dev = cuda()
+    shapes = [(4096, 512, 1536, 32, 0.9), (4096, 512, 512, 32, 0.0), (2048, 256, 1024, 8, 0.0)]
+    cases, wants = [], []
+    for i, (T, d_in, d_out, K, gamma) in enumerate(shapes):
+        X, delta, so = _case(10 + i, T, d_in, d_out, K)
+        cases.append((X, delta, so, d_out, 100 + i, gamma))
+        wants.append(dust.dust_estimate_gW(X.to(dev), delta.to(dev), d_out, so.to(dev), 100 + i,
+                                           dust.GAUSSIAN, 0, 1e-3, gamma, 1.0,
+                                           dust.CENTER).cpu())
+    sites = [_site(*c, dev, pinned_gw) for c in cases]
+    st = torch.cuda.Stream()
+    for rep in range(2):
+        for q in sites:
+            q["gW_host"].fill_(float("nan"))
+        dust.dust_estimate_gW_host_sites(sites, dust.GAUSSIAN, 0, 1.0, dust.CENTER, stream=st)
+        st.synchronize()
+        assert dust.dust_last_error() == dust.OK
+        for i, (q, want) in enumerate(zip(sites, wants)):
+            assert torch.equal(q["gW_host"], want), (rep, i)
+
+
+def test_host_sites_reject_overlapping_staging():
+    import torch
+    dev = cuda()
+    X, delta, so = _case(20, 1024, 256, 512, 8)
+    a = _site(X, delta, so, 512, 1, 0.0, dev)
+    b = _site(X, delta, so, 512, 2, 0.0, dev)
+    b["X_dev"] = a["workspace"][: X.numel() * 2].view(torch.bfloat16).view(X.shape)
+    with pytest.raises(dust.DustError) as e:
+        dust.dust_estimate_gW_host_sites([a, b], dust.GAUSSIAN, 0)
+    assert e.value.status == dust.ERR_INVALID_ARG

@@ -63,6 +63,7 @@ def _signatures():
         "dust_estimate_gW_host": (i32, [P, P, i32, i64, i64, P, P, i64, i64, P, P, i64, u64,
                                         i32, i64, f32, f32, f32, u32, P, P, P, SZ, P]),
         "dust_last_error": (i32, [P]),
+        "dust_estimate_gW_host_sites": (i32, [P, i64, i32, i32, i64, f32, u32, P]),
         "dust_credit_scan_noalloc_capacity": (SZ, []),
         "dust_credit_scan_noalloc": (i32, [P, i64, i64, P, i64, f32, u32, P, P]),
         "dust_forward_jitter": (i32, [P, P, i64, i64, i64, u64, i32, i64, i64, f32, u32, i32,
@@ -74,6 +75,8 @@ def _signatures():
         "dust_estimate_gE": (i32, [P, i64, i64, P, i64, i64, P, i64, u64, i32, i64, f32, f32,
                                    f32, u32, P, P, SZ, P]),
         "dust_debug_inject_timeout": (i32, [i32]),
+        "dust_pipe_probe": (i32, [i32, i64, C.POINTER(C.c_double), P, P]),
+        "dust_pipe_probe_threads": (i32, []),
         "dust_profile_enable": (i32, [i32]),
         "dust_profile_read": (i32, [P, i32]),
     }
@@ -135,6 +138,27 @@ def _need_cuda(*ts):
             raise ValueError("expected a CUDA tensor")
         if t is not None and not t.is_contiguous():
             raise ValueError("expected a contiguous tensor")
+
+
+def _expect(t, name, dtypes, shape=None, dim=None):
+    """Raise ValueError unless tensor t has one of `dtypes` and, when given,
+    exactly `shape` (a tuple) or `dim` dimensions: the C ABI takes raw pointers
+    and sizes, so a tensor of another dtype or shape would be misread, or
+    written past its end."""
+    if t.dtype not in dtypes:
+        raise ValueError("%s must be %s, got %s"
+                         % (name, " or ".join(str(d) for d in dtypes), t.dtype))
+    if dim is not None and t.dim() != dim:
+        raise ValueError("%s must have %d dimensions, got shape %s"
+                         % (name, dim, tuple(t.shape)))
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+
+
+def _scan_inputs(delta, seq_offsets):
+    import torch
+    _expect(delta, "delta", (torch.float32,), dim=2)
+    _expect(seq_offsets, "seq_offsets", (torch.int32,), dim=1)
 
 
 # ------------------------------------------------------------------ calls --
@@ -247,10 +271,12 @@ def dust_credit_scan(delta, seq_offsets, gamma, flags=CENTER, r=None, workspace=
                      stream=None):
     """delta: f32 [K, T]; seq_offsets: i32 [n_seq+1]; returns r f32 [T, K]."""
     import torch
-    _need_cuda(delta, seq_offsets)
+    _need_cuda(delta, seq_offsets, r, workspace)
+    _scan_inputs(delta, seq_offsets)
     K, T = delta.shape
     if r is None:
         r = torch.empty((T, K), dtype=torch.float32, device=delta.device)
+    _expect(r, "r", (torch.float32,), shape=(T, K))
     need = dust_credit_scan_workspace(K, T)
     if workspace is None:
         workspace = _workspace(need, delta.device)
@@ -267,9 +293,11 @@ def dust_credit_scan_noalloc(delta, seq_offsets, gamma, flags=CENTER, r=None, st
     convenience when omitted."""
     import torch
     _need_cuda(delta, seq_offsets, r)
+    _scan_inputs(delta, seq_offsets)
     K, T = delta.shape
     if r is None:
         r = torch.empty((T, K), dtype=torch.float32, device=delta.device)
+    _expect(r, "r", (torch.float32,), shape=(T, K))
     _check(lib().dust_credit_scan_noalloc(_ptr(delta), K, T, _ptr(seq_offsets),
                                           seq_offsets.numel() - 1, float(gamma), flags, _ptr(r),
                                           _stream(stream)), "dust_credit_scan_noalloc")
@@ -280,10 +308,12 @@ def dust_error_estimate(r, d_out, seed, kind, draw_begin, sigma, flags=0, g=None
                         g_dtype=None, stream=None):
     """r: f32 [T, K]; returns g [T, d_out] (f32 unless g_dtype=torch.bfloat16)."""
     import torch
-    _need_cuda(r)
+    _need_cuda(r, g)
+    _expect(r, "r", (torch.float32,), dim=2)
     T, K = r.shape
     if g is None:
         g = torch.empty((T, d_out), dtype=g_dtype or torch.float32, device=r.device)
+    _expect(g, "g", (torch.float32, torch.bfloat16), shape=(T, d_out))
     _check(lib().dust_error_estimate(_ptr(r), K, T, d_out, seed, kind, draw_begin, float(sigma),
                                      flags, _ptr(g), _dtype_code(g), _stream(stream)),
            "dust_error_estimate")
@@ -329,12 +359,16 @@ def dust_estimate_gW(X, delta, d_out, seq_offsets, seed, kind, draw_begin, sigma
                      scale=1.0, flags=CENTER, gW=None, workspace=None, stream=None):
     """X: [T, d_in] bf16 or f32; delta: f32 [K, T]; returns gW f32 [d_out, d_in]."""
     import torch
-    _need_cuda(X, delta, seq_offsets, gW)
+    _need_cuda(X, delta, seq_offsets, gW, workspace)
+    _expect(X, "X", (torch.float32, torch.bfloat16), dim=2)
+    _scan_inputs(delta, seq_offsets)
     T, d_in = X.shape
     K = delta.shape[0]
+    _expect(delta, "delta", (torch.float32,), shape=(K, T))
     xd = _dtype_code(X)
     if gW is None:
         gW = torch.empty((d_out, d_in), dtype=torch.float32, device=X.device)
+    _expect(gW, "gW", (torch.float32,), shape=(d_out, d_in))
     need = dust_estimate_gW_workspace(T, d_in, d_out, K, xd, flags)
     if workspace is None:
         workspace = _workspace(need, X.device)
@@ -364,6 +398,82 @@ def dust_estimate_gW_host(X_host, X_dev, delta_host, delta_dev, seq_host, seq_de
         float(sigma), float(gamma), float(scale), flags, _ptr(gW_host), _ptr(gW_dev),
         _ptr(workspace), workspace.numel(), _stream(stream)), "dust_estimate_gW_host")
     return gW_host
+
+
+PIPE_XU, PIPE_ALU, PIPE_FMA, PIPE_ISSUE = 0, 1, 2, 3
+
+
+def dust_pipe_probe(pipe, steps, sink, stream=None):
+    """Enqueue one pipe-rate probe launch; returns the number of counted
+    operations it performs (time it with CUDA events on `stream`). `sink`:
+    CUDA float tensor of at least dust_pipe_probe_threads() elements."""
+    _need_cuda(sink)
+    if sink.numel() < dust_pipe_probe_threads():
+        raise ValueError("sink must hold dust_pipe_probe_threads() floats")
+    ops = C.c_double(0.0)
+    _check(lib().dust_pipe_probe(int(pipe), int(steps), C.byref(ops), _ptr(sink),
+                                 _stream(stream)), "dust_pipe_probe")
+    return ops.value
+
+
+def dust_pipe_probe_threads():
+    n = lib().dust_pipe_probe_threads()
+    if n < 0:
+        raise DustError(-n, "dust_pipe_probe_threads")
+    return n
+
+
+class HostSite(C.Structure):
+    """dust_host_site of include/dust.h: one layer of a multi-site call."""
+    _fields_ = [("X_host", C.c_void_p), ("X_dev", C.c_void_p), ("T", C.c_int64),
+                ("d_in", C.c_int64), ("d_out", C.c_int64), ("delta_host", C.c_void_p),
+                ("delta_dev", C.c_void_p), ("K", C.c_int64), ("seq_offsets_host", C.c_void_p),
+                ("seq_dev", C.c_void_p), ("n_seq", C.c_int64), ("seed", C.c_uint64),
+                ("sigma", C.c_float), ("gamma", C.c_float), ("gW_host", C.c_void_p),
+                ("gW_dev", C.c_void_p), ("workspace", C.c_void_p), ("ws_bytes", C.c_size_t)]
+
+
+def dust_estimate_gW_host_sites(sites, kind, draw_begin, scale=1.0, flags=CENTER, stream=None):
+    """Several layers from host buffers in one pass (later sites' inputs are
+    copied while earlier sites compute). `sites`: list of dicts with the CPU
+    tensors X_host [T, d_in], delta_host f32 [K, T], seq_host i32 [n_seq+1],
+    gW_host f32 [d_out, d_in] (pinned for overlap), the CUDA staging tensors
+    X_dev, delta_dev, seq_dev, gW_dev of the same shapes, a CUDA uint8
+    `workspace` and the scalars seed, sigma, gamma. All X share one dtype.
+    The caller synchronises the stream before reading the gW_host tensors."""
+    import torch
+    arr = (HostSite * max(1, len(sites)))()
+    xd = None
+    for i, q in enumerate(sites):
+        Xh, Xd = q["X_host"], q["X_dev"]
+        _need_cuda(Xd, q["delta_dev"], q["seq_dev"], q["gW_dev"], q["workspace"])
+        _expect(Xh, "X_host", (torch.float32, torch.bfloat16), dim=2)
+        T, d_in = Xh.shape
+        d_out = q["gW_host"].shape[0]
+        K = q["delta_host"].shape[0]
+        n_seq = q["seq_host"].numel() - 1
+        _expect(Xd, "X_dev", (Xh.dtype,), shape=(T, d_in))
+        for nm in ("delta_host", "delta_dev"):
+            _expect(q[nm], nm, (torch.float32,), shape=(K, T))
+        for nm in ("seq_host", "seq_dev"):
+            _expect(q[nm], nm, (torch.int32,), shape=(n_seq + 1,))
+        for nm in ("gW_host", "gW_dev"):
+            _expect(q[nm], nm, (torch.float32,), shape=(d_out, d_in))
+        code = _dtype_code(Xh)
+        if xd is None:
+            xd = code
+        elif code != xd:
+            raise ValueError("every site's X must have the same dtype")
+        arr[i] = HostSite(_ptr(Xh), _ptr(Xd), T, d_in, d_out, _ptr(q["delta_host"]),
+                          _ptr(q["delta_dev"]), K, _ptr(q["seq_host"]), _ptr(q["seq_dev"]),
+                          n_seq, int(q["seed"]), float(q["sigma"]), float(q["gamma"]),
+                          _ptr(q["gW_host"]), _ptr(q["gW_dev"]), _ptr(q["workspace"]),
+                          q["workspace"].numel())
+    _check(lib().dust_estimate_gW_host_sites(C.cast(arr, C.c_void_p), len(sites),
+                                             BF16 if xd is None else xd, kind, draw_begin,
+                                             float(scale), flags, _stream(stream)),
+           "dust_estimate_gW_host_sites")
+    return [q["gW_host"] for q in sites]
 
 
 def dust_last_error(stream=None):

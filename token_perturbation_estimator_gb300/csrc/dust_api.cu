@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "dust.h"
 #include "internal.cuh"
@@ -418,15 +419,14 @@ int32_t dust_estimate_gW_path(int64_t T, int64_t d_in, int64_t d_out, int64_t K,
 
 namespace {
 
-// The whole estimator on `stream`. When x_ready is given, X is still being
-// copied on another stream: the stream waits for that event just before the
-// first kernel that reads X (the contraction), so the scan and the weighting
-// overlap the copy.
-dust_status estimate(const void* X, dust_dtype x_dtype, int64_t T, int64_t d_in,
-                     const float* delta, int64_t K, int64_t d_out, const int32_t* seq_offsets,
-                     int64_t n_seq, uint64_t seed, dust_noise_kind kind, int64_t draw_begin,
-                     float sigma, float gamma, float scale, uint32_t flags, float* gW,
-                     void* workspace, size_t ws_bytes, void* stream, cudaEvent_t x_ready) {
+// Every argument check of the estimator, with nothing enqueued: DUST_OK when
+// `estimate` would enqueue its work (or has nothing to do).
+dust_status estimate_check(const void* X, dust_dtype x_dtype, int64_t T, int64_t d_in,
+                           const float* delta, int64_t K, int64_t d_out,
+                           const int32_t* seq_offsets, int64_t n_seq, dust_noise_kind kind,
+                           int64_t draw_begin, float sigma, float gamma, float scale,
+                           uint32_t flags, const float* gW, const void* workspace,
+                           size_t ws_bytes) {
     dust_status st = check_estimate(T, d_in, d_out, K, x_dtype, flags);
     if (st != DUST_OK) return st;
     if (!value_kind(kind)) return DUST_ERR_INVALID_ARG;
@@ -440,9 +440,7 @@ dust_status estimate(const void* X, dust_dtype x_dtype, int64_t T, int64_t d_in,
     if (n_seq < 0) return DUST_ERR_INVALID_ARG;
     if (d_out * d_in == 0) return DUST_OK;
     if (!gW || (reinterpret_cast<uintptr_t>(gW) % 16)) return DUST_ERR_INVALID_ARG;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const bool acc = (flags & DUST_ACCUMULATE) != 0;
-    if (T == 0) return acc ? DUST_OK : cuda_status(launch_zero(gW, d_out * d_in, s));
+    if (T == 0) return DUST_OK;
     if (!X || !delta || !seq_offsets) return DUST_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(X) % 16) return DUST_ERR_INVALID_ARG;
     const Layout L = layout(T, d_in, d_out, K, x_dtype, flags);
@@ -452,6 +450,27 @@ dust_status estimate(const void* X, dust_dtype x_dtype, int64_t T, int64_t d_in,
         return DUST_ERR_UNSUPPORTED;
     if (!workspace || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255))
         return DUST_ERR_WORKSPACE;
+    return DUST_OK;
+}
+
+// The whole estimator on `stream`. When x_ready is given, X is still being
+// copied on another stream: the stream waits for that event just before the
+// first kernel that reads X (the contraction), so the scan and the weighting
+// overlap the copy.
+dust_status estimate(const void* X, dust_dtype x_dtype, int64_t T, int64_t d_in,
+                     const float* delta, int64_t K, int64_t d_out, const int32_t* seq_offsets,
+                     int64_t n_seq, uint64_t seed, dust_noise_kind kind, int64_t draw_begin,
+                     float sigma, float gamma, float scale, uint32_t flags, float* gW,
+                     void* workspace, size_t ws_bytes, void* stream, cudaEvent_t x_ready) {
+    const dust_status st =
+        estimate_check(X, x_dtype, T, d_in, delta, K, d_out, seq_offsets, n_seq, kind,
+                       draw_begin, sigma, gamma, scale, flags, gW, workspace, ws_bytes);
+    if (st != DUST_OK) return st;
+    if (d_out * d_in == 0) return DUST_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool acc = (flags & DUST_ACCUMULATE) != 0;
+    if (T == 0) return acc ? DUST_OK : cuda_status(launch_zero(gW, d_out * d_in, s));
+    const Layout L = layout(T, d_in, d_out, K, x_dtype, flags);
 
     char* ws = static_cast<char*>(workspace);
     unsigned int* sync = reinterpret_cast<unsigned int*>(ws);  // [0]: the scan's ticket
@@ -490,7 +509,7 @@ dust_status estimate(const void* X, dust_dtype x_dtype, int64_t T, int64_t d_in,
     return cuda_status(e);
 }
 
-// A copy stream and two events per device for dust_estimate_gW_host, created
+// A copy stream and per-site events per device for the host-buffer entry points, created
 // on first use and kept for the life of the process. The mutex covers one
 // call's whole enqueue sequence, so the events are re-recorded only after
 // every wait on them has been enqueued.
@@ -499,9 +518,11 @@ struct CopyLane {
     bool ready = false;
     cudaError_t err = cudaSuccess;
     cudaStream_t copy = nullptr;
-    cudaEvent_t fork = nullptr, x_done = nullptr;
+    cudaEvent_t fork = nullptr;
+    std::vector<cudaEvent_t> ev;  // per site: loss changes copied, X copied
 };
 constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxHostSites = 4096;
 CopyLane g_lanes[kMaxDevices];
 
 #ifndef DUST_HOST_DIRECT_GW
@@ -531,6 +552,9 @@ dust_status estimate_host(const void* X_host, void* X_dev, dust_dtype x_dtype, i
                           int64_t draw_begin, float sigma, float gamma, float scale,
                           uint32_t flags, float* gW_host, float* gW_dev, void* workspace,
                           size_t ws_bytes, void* stream);
+dust_status estimate_host_sites(const dust_host_site* sites, int64_t n, dust_dtype x_dtype,
+                                dust_noise_kind kind, int64_t draw_begin, float scale,
+                                uint32_t flags, void* stream);
 
 dust_status enqueue_device(const void* ctx, cudaStream_t s) {
     const CallArgs& a = *static_cast<const CallArgs*>(ctx);
@@ -624,65 +648,134 @@ dust_status dust_estimate_gW_host(const void* X_host, void* X_dev, dust_dtype x_
     return enqueue_host(&a, static_cast<cudaStream_t>(stream));
 }
 
+dust_status dust_estimate_gW_host_sites(const dust_host_site* sites, int64_t n_sites,
+                                        dust_dtype x_dtype, dust_noise_kind kind,
+                                        int64_t draw_begin, float scale, uint32_t flags,
+                                        void* stream) {
+    return estimate_host_sites(sites, n_sites, x_dtype, kind, draw_begin, scale, flags, stream);
+}
+
 }  // extern "C"
 
 namespace {
 
-dust_status estimate_host(const void* X_host, void* X_dev, dust_dtype x_dtype, int64_t T,
-                          int64_t d_in, const float* delta_host, float* delta_dev, int64_t K,
-                          int64_t d_out, const int32_t* seq_offsets_host, int32_t* seq_dev,
-                          int64_t n_seq, uint64_t seed, dust_noise_kind kind,
-                          int64_t draw_begin, float sigma, float gamma, float scale,
-                          uint32_t flags, float* gW_host, float* gW_dev, void* workspace,
-                          size_t ws_bytes, void* stream) {
-    dust_status st = check_estimate(T, d_in, d_out, K, x_dtype, flags);
-    if (st != DUST_OK) return st;
-    if (n_seq < 0 || (T > 0 && n_seq < 1)) return DUST_ERR_INVALID_ARG;
-    if (d_out * d_in > 0 && (!gW_host || !gW_dev)) return DUST_ERR_INVALID_ARG;
-    if (T > 0 && (!X_host || !X_dev || !delta_host || !delta_dev || !seq_offsets_host ||
-                  !seq_dev))
-        return DUST_ERR_INVALID_ARG;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
+// Device byte range [lo, hi) of one buffer of a multi-site call.
+struct Range {
+    uintptr_t lo, hi;
+    int64_t site;
+    bool async;  // written by the copy stream, out of `stream`'s order
+};
+
+bool overlap(const Range& a, const Range& b) { return a.lo < b.hi && b.lo < a.hi; }
+
+// The estimator for several sites from host buffers (see dust.h). Inputs go
+// host -> device over an internal copy stream that runs ahead of the compute
+// on `stream`: site 0's loss changes and offsets are copied on `stream` first
+// (the scan needs them at once); then the copy stream, after everything
+// enqueued on `stream` before this call, copies X of site 0 and, for every
+// later site i, its loss changes, offsets and X, recording an event after
+// each. Site i's kernels wait for its loss changes before its first kernel
+// and for its X only before its contraction, so every copy after the first
+// overlaps the compute of earlier sites.
+dust_status estimate_host_sites(const dust_host_site* sites, int64_t n, dust_dtype x_dtype,
+                                dust_noise_kind kind, int64_t draw_begin, float scale,
+                                uint32_t flags, void* stream) {
+    if (n < 0 || (n > 0 && !sites)) return DUST_ERR_INVALID_ARG;
+    if (n > kMaxHostSites) return DUST_ERR_RANGE;
     const size_t esz = (x_dtype == DUST_BF16) ? 2 : 4;
-    const size_t gw_bytes = sizeof(float) * static_cast<size_t>(d_out * d_in);
-    const size_t x_bytes = esz * static_cast<size_t>(T * d_in);
-    // The small inputs first, on `stream`: the scan needs them at once.
-    if (T > 0) {
-        if (cudaMemcpyAsync(delta_dev, delta_host, sizeof(float) * static_cast<size_t>(K * T),
-                            cudaMemcpyHostToDevice, s) != cudaSuccess ||
-            cudaMemcpyAsync(seq_dev, seq_offsets_host, sizeof(int32_t) * (n_seq + 1),
-                            cudaMemcpyHostToDevice, s) != cudaSuccess)
-            return DUST_ERR_CUDA;
+    // Every check before anything is enqueued.
+    for (int64_t i = 0; i < n; ++i) {
+        const dust_host_site& q = sites[i];
+        dust_status st = check_estimate(q.T, q.d_in, q.d_out, q.K, x_dtype, flags);
+        if (st != DUST_OK) return st;
+        if (q.n_seq < 0 || (q.T > 0 && q.n_seq < 1)) return DUST_ERR_INVALID_ARG;
+        if (q.d_out * q.d_in > 0 && (!q.gW_host || !q.gW_dev)) return DUST_ERR_INVALID_ARG;
+        if (q.T > 0 && (!q.X_host || !q.X_dev || !q.delta_host || !q.delta_dev ||
+                        !q.seq_offsets_host || !q.seq_dev))
+            return DUST_ERR_INVALID_ARG;
+        st = estimate_check(q.X_dev, x_dtype, q.T, q.d_in, q.delta_dev, q.K, q.d_out, q.seq_dev,
+                            q.n_seq, kind, draw_begin, q.sigma, q.gamma, scale, flags, q.gW_dev,
+                            q.workspace, q.ws_bytes);
+        if (st != DUST_OK) return st;
     }
-    // A page-locked, device-mapped gW_host is written (and, accumulating, read)
-    // by the kernels in place, over the host link, instead of through gW_dev
-    // and a copy back.
-    float* gw_target = gW_dev;
-    bool direct = false;
-#if DUST_HOST_DIRECT_GW
-    if (gw_bytes) {
-        cudaPointerAttributes pa;
-        if (cudaPointerGetAttributes(&pa, gW_host) == cudaSuccess &&
-            pa.type == cudaMemoryTypeHost && pa.devicePointer &&
-            reinterpret_cast<uintptr_t>(pa.devicePointer) % 16 == 0) {
-            gw_target = static_cast<float*>(pa.devicePointer);
-            direct = true;
+    // Buffers that the copy stream writes while `stream` computes must not
+    // overlap any other device buffer of the call.
+    if (n > 1) {
+        std::vector<Range> rs;
+        rs.reserve(static_cast<size_t>(5 * n));
+        auto add = [&](const void* p, size_t bytes, int64_t site, bool async) {
+            if (p && bytes) {
+                const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+                rs.push_back(Range{lo, lo + bytes, site, async});
+            }
+        };
+        for (int64_t i = 0; i < n; ++i) {
+            const dust_host_site& q = sites[i];
+            if (q.T == 0 || q.d_out * q.d_in == 0) continue;
+            add(q.X_dev, esz * static_cast<size_t>(q.T * q.d_in), i, true);
+            add(q.delta_dev, sizeof(float) * static_cast<size_t>(q.K * q.T), i, i > 0);
+            add(q.seq_dev, sizeof(int32_t) * static_cast<size_t>(q.n_seq + 1), i, i > 0);
+            add(q.gW_dev, sizeof(float) * static_cast<size_t>(q.d_out * q.d_in), i, false);
+            add(q.workspace, q.ws_bytes, i, false);
         }
-        (void)cudaGetLastError();
+        for (size_t a = 0; a < rs.size(); ++a) {
+            if (!rs[a].async) continue;
+            for (size_t b = 0; b < rs.size(); ++b)
+                if (b != a && overlap(rs[a], rs[b])) return DUST_ERR_INVALID_ARG;
+        }
     }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    // Per site: the device address ĜW goes to. A page-locked, device-mapped
+    // gW_host is written (and, accumulating, read) by the kernels in place,
+    // over the host link, instead of through gW_dev and a copy back.
+    std::vector<float*> target(static_cast<size_t>(n));
+    std::vector<char> direct(static_cast<size_t>(n), 0);
+    for (int64_t i = 0; i < n; ++i) {
+        const dust_host_site& q = sites[i];
+        target[i] = q.gW_dev;
+#if DUST_HOST_DIRECT_GW
+        if (q.d_out * q.d_in > 0) {
+            cudaPointerAttributes pa;
+            if (cudaPointerGetAttributes(&pa, q.gW_host) == cudaSuccess &&
+                pa.type == cudaMemoryTypeHost && pa.devicePointer &&
+                reinterpret_cast<uintptr_t>(pa.devicePointer) % 16 == 0) {
+                target[i] = static_cast<float*>(pa.devicePointer);
+                direct[i] = 1;
+            }
+            (void)cudaGetLastError();
+        }
 #endif
-    if ((flags & DUST_ACCUMULATE) && gw_bytes && !direct &&
-        cudaMemcpyAsync(gW_dev, gW_host, gw_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return DUST_ERR_CUDA;
-    // X, the large input, then goes over a second copy stream while delta is
-    // scanned and weighted; `stream` waits for it before the contraction and,
-    // in every case, before this call's work on `stream` ends. The copy starts
-    // after everything enqueued on `stream` so far: earlier work that may
-    // still read X_dev, and the small copies above (host-to-device copies
-    // share an engine, so an earlier X copy would hold the scan's inputs up).
+    }
+
+    auto small_copies = [&](const dust_host_site& q, cudaStream_t cs) {
+        if (q.T == 0) return true;
+        return cudaMemcpyAsync(q.delta_dev, q.delta_host,
+                               sizeof(float) * static_cast<size_t>(q.K * q.T),
+                               cudaMemcpyHostToDevice, cs) == cudaSuccess &&
+               cudaMemcpyAsync(q.seq_dev, q.seq_offsets_host,
+                               sizeof(int32_t) * static_cast<size_t>(q.n_seq + 1),
+                               cudaMemcpyHostToDevice, cs) == cudaSuccess;
+    };
+    auto gw_in = [&](int64_t i) {
+        const dust_host_site& q = sites[i];
+        const size_t gw_bytes = sizeof(float) * static_cast<size_t>(q.d_out * q.d_in);
+        if (!(flags & DUST_ACCUMULATE) || !gw_bytes || direct[i]) return true;
+        return cudaMemcpyAsync(q.gW_dev, q.gW_host, gw_bytes, cudaMemcpyHostToDevice, s) ==
+               cudaSuccess;
+    };
+    if (n > 0 && (!small_copies(sites[0], s) || !gw_in(0))) return DUST_ERR_CUDA;
+
+    // The copy lane: its stream and two events per site, created on first
+    // use and kept for the life of the process. The lock covers the whole
+    // enqueue sequence, so the events are re-recorded only after every wait
+    // on them has been enqueued.
+    bool any_x = false;
+    for (int64_t i = 0; i < n; ++i)
+        if (sites[i].T * sites[i].d_in > 0 && sites[i].d_out * sites[i].d_in > 0) any_x = true;
     CopyLane* lane = nullptr;
     std::unique_lock<std::mutex> lock;
-    if (x_bytes > 0) {
+    if (any_x) {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
             return DUST_ERR_CUDA;
@@ -692,31 +785,93 @@ dust_status estimate_host(const void* X_host, void* X_dev, dust_dtype x_dtype, i
             lane->err = cudaStreamCreateWithFlags(&lane->copy, cudaStreamNonBlocking);
             if (lane->err == cudaSuccess)
                 lane->err = cudaEventCreateWithFlags(&lane->fork, cudaEventDisableTiming);
-            if (lane->err == cudaSuccess)
-                lane->err = cudaEventCreateWithFlags(&lane->x_done, cudaEventDisableTiming);
-
             lane->ready = true;
         }
         if (lane->err != cudaSuccess) return DUST_ERR_CUDA;
+        while (lane->ev.size() < static_cast<size_t>(2 * n)) {
+            cudaEvent_t e = nullptr;
+            if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess)
+                return DUST_ERR_CUDA;
+            lane->ev.push_back(e);
+        }
         if (cudaEventRecord(lane->fork, s) != cudaSuccess ||
-            cudaStreamWaitEvent(lane->copy, lane->fork, 0) != cudaSuccess ||
-            cudaMemcpyAsync(X_dev, X_host, x_bytes, cudaMemcpyHostToDevice, lane->copy) !=
-                cudaSuccess ||
-            cudaEventRecord(lane->x_done, lane->copy) != cudaSuccess)
+            cudaStreamWaitEvent(lane->copy, lane->fork, 0) != cudaSuccess)
             return DUST_ERR_CUDA;
+        for (int64_t i = 0; i < n; ++i) {
+            const dust_host_site& q = sites[i];
+            if (i > 0 && (!small_copies(q, lane->copy) ||
+                          cudaEventRecord(lane->ev[2 * i], lane->copy) != cudaSuccess))
+                return DUST_ERR_CUDA;
+            const size_t x_bytes = esz * static_cast<size_t>(q.T * q.d_in);
+            if (x_bytes && q.d_out * q.d_in > 0 &&
+                cudaMemcpyAsync(q.X_dev, q.X_host, x_bytes, cudaMemcpyHostToDevice,
+                                lane->copy) != cudaSuccess)
+                return DUST_ERR_CUDA;
+            if (cudaEventRecord(lane->ev[2 * i + 1], lane->copy) != cudaSuccess)
+                return DUST_ERR_CUDA;
+        }
     }
-    auto join = [&]() {
-        return !lane || cudaStreamWaitEvent(s, lane->x_done, 0) == cudaSuccess;
-    };
-    st = estimate(X_dev, x_dtype, T, d_in, delta_dev, K, d_out, seq_dev, n_seq, seed, kind,
-                  draw_begin, sigma, gamma, scale, flags, gw_target, workspace, ws_bytes, stream,
-                  lane ? lane->x_done : nullptr);
-    if (!join()) return DUST_ERR_CUDA;
-    if (st != DUST_OK) return st;
-    if (gw_bytes && !direct &&
-        cudaMemcpyAsync(gW_host, gW_dev, gw_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    dust_status result = DUST_OK;
+    for (int64_t i = 0; i < n && result == DUST_OK; ++i) {
+        const dust_host_site& q = sites[i];
+        if (i > 0) {
+            if (lane) {
+                if (cudaStreamWaitEvent(s, lane->ev[2 * i], 0) != cudaSuccess) {
+                    result = DUST_ERR_CUDA;
+                    break;
+                }
+            } else if (!small_copies(q, s)) {
+                result = DUST_ERR_CUDA;
+                break;
+            }
+            if (!gw_in(i)) {
+                result = DUST_ERR_CUDA;
+                break;
+            }
+        }
+        result = estimate(q.X_dev, x_dtype, q.T, q.d_in, q.delta_dev, q.K, q.d_out, q.seq_dev,
+                          q.n_seq, q.seed, kind, draw_begin, q.sigma, q.gamma, scale, flags,
+                          target[i], q.workspace, q.ws_bytes, stream,
+                          lane ? lane->ev[2 * i + 1] : nullptr);
+        const size_t gw_bytes = sizeof(float) * static_cast<size_t>(q.d_out * q.d_in);
+        if (result == DUST_OK && gw_bytes && !direct[i] &&
+            cudaMemcpyAsync(q.gW_host, q.gW_dev, gw_bytes, cudaMemcpyDeviceToHost, s) !=
+                cudaSuccess)
+            result = DUST_ERR_CUDA;
+    }
+    // However the sequence ended, `stream` waits for every copy of the call.
+    if (lane && n > 0 && cudaStreamWaitEvent(s, lane->ev[2 * n - 1], 0) != cudaSuccess)
         return DUST_ERR_CUDA;
-    return DUST_OK;
+    return result;
+}
+
+dust_status estimate_host(const void* X_host, void* X_dev, dust_dtype x_dtype, int64_t T,
+                          int64_t d_in, const float* delta_host, float* delta_dev, int64_t K,
+                          int64_t d_out, const int32_t* seq_offsets_host, int32_t* seq_dev,
+                          int64_t n_seq, uint64_t seed, dust_noise_kind kind,
+                          int64_t draw_begin, float sigma, float gamma, float scale,
+                          uint32_t flags, float* gW_host, float* gW_dev, void* workspace,
+                          size_t ws_bytes, void* stream) {
+    dust_host_site q;
+    q.X_host = X_host;
+    q.X_dev = X_dev;
+    q.T = T;
+    q.d_in = d_in;
+    q.d_out = d_out;
+    q.delta_host = delta_host;
+    q.delta_dev = delta_dev;
+    q.K = K;
+    q.seq_offsets_host = seq_offsets_host;
+    q.seq_dev = seq_dev;
+    q.n_seq = n_seq;
+    q.seed = seed;
+    q.sigma = sigma;
+    q.gamma = gamma;
+    q.gW_host = gW_host;
+    q.gW_dev = gW_dev;
+    q.workspace = workspace;
+    q.ws_bytes = ws_bytes;
+    return estimate_host_sites(&q, 1, x_dtype, kind, draw_begin, scale, flags, stream);
 }
 
 }  // namespace
