@@ -1,20 +1,28 @@
 #!/usr/bin/env python
 """Benchmark of the Dust per-token weight-gradient estimator on GB300.
 
-One step = one dust_estimate_gW call on the MLP up-projection workload
-(d_in 512, d_out 2048, 16 x 1024 tokens, K = 8 draws, sigma 1e-3, gamma 0,
-Gaussian jitter, bf16 X): centring, credit scan, noise regeneration + reward
-weighting, and the contraction to GW, with inputs resident in HBM.
+Default workload: the whole-model sweep, the largest configuration. One step =
+48 dust_estimate_gW calls on one stream, one per linear site of a 12-layer
+transformer shape (d_model 512, MLP 2048; per layer QKV 512 -> 1536 with
+gamma 0.9, O 512 -> 512, up 512 -> 2048 and down 2048 -> 512 with gamma 0),
+each over 64 x 1024 tokens with K = 32 Gaussian draws, sigma 1e-3, bf16 X:
+centring, credit scan, noise regeneration + reward weighting and the
+contraction to GW, with inputs resident in HBM. `--workload` selects one
+layer instead (mlp_up, qkv, the 4096^2 layers, the toy fp32 layer) or the
+jittered forward (forward_*).
 
-Metric: token-draws/s = K * T / step time (whole job over all ranks).
-Prints one JSON line (rank 0). `--impl reference` times the fp64 CPU oracle
-on the same workload instead (rank 0 only).
+Metric: token-draws/s = sum over sites of K * T / step time (whole job over
+all ranks). Prints one JSON line (rank 0). `--impl reference` times the fp64
+CPU oracle on a bounded sample of the same workload instead (rank 0 only).
 
 Timing: W warm-up steps, then K timed steps, each bracketed by CUDA events on
 the launching stream with a 256 MB L2 flush between steps (outside the
 events); barrier + synchronize around the timed region; max over ranks.
-A second, profiled pass of the same K steps times every kernel with events
-(dust_profile_*) for the roofline of the dominant kernel.
+A second, profiled pass of the same steps times every kernel with events
+(dust_profile_*) for the roofline of the dominant kernel; the rooflines of
+the issue-bound kernels use pipe rates measured on the device by the
+library's probe kernels (dust_pipe_probe), scaled to the SM clock sampled
+during the timed region.
 """
 from __future__ import annotations
 
@@ -41,8 +49,11 @@ SMI_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.acti
 def parse_args(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=2000)
-    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--steps", type=int, default=None,
+                   help="timed steps (default per workload: sweep 20, square layers 100, "
+                        "qkv 300, the rest 2000)")
+    p.add_argument("--warmup", type=int, default=None,
+                   help="warm-up steps (default: sweep 3, the rest 20)")
     p.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -50,13 +61,28 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--flags", type=int, default=None,
                    help="extra dust_estimate_gW flags (e.g. force a path)")
-    p.add_argument("--workload", default="mlp_up",
-                   choices=["mlp_up", "toy", "qkv", "square_r", "square_g", "square_rp",
-                            "sweep", "forward_g", "forward_r", "forward_rp"],
-                   help="mlp_up is the measured headline; forward_* time the jittered "
-                        "forward (8 draws + the clean output) of the same layer; the "
-                        "others are for study")
-    return p.parse_args(argv)
+    p.add_argument("--workload", default="sweep",
+                   choices=["sweep", "mlp_up", "toy", "qkv", "square_r", "square_g",
+                            "square_rp", "sweep_qkv", "sweep_o", "sweep_up", "sweep_down",
+                            "forward_g", "forward_r", "forward_rp"],
+                   help="sweep (the 48-site whole-model pass, the largest configuration) is "
+                        "the headline; forward_* time the jittered forward (8 draws + the "
+                        "clean output) of the up-projection layer; the others are single "
+                        "layers (sweep_*: one site of each of the sweep's four shapes)")
+    p.add_argument("--no-pipe-probe", action="store_true",
+                   help="skip the pipe-rate probes (rooflines then use derived peaks)")
+    args = p.parse_args(argv)
+    steps, warm = DEFAULT_STEPS.get(args.workload, (2000, 20))
+    if args.steps is None:
+        args.steps = steps
+    if args.warmup is None:
+        args.warmup = warm
+    return args
+
+
+# (timed steps, warm-up steps) per workload: about a second of timed work.
+DEFAULT_STEPS = {"sweep": (20, 3), "square_r": (100, 10), "square_g": (100, 10),
+                 "square_rp": (100, 10), "qkv": (300, 20)}
 
 
 # --------------------------------------------------------------- ranks ----
@@ -180,6 +206,10 @@ WORKLOADS = {
     "square_g": "square_4096_T32768_K64_gaussian",
     "square_rp": "square_4096_T32768_K64_rademacher_packed",
     "sweep": "sweep_12x4_sites_T65536_K32_gaussian",
+    "sweep_qkv": "sweep_site_qkv_512to1536_T65536_K32_gaussian_gamma0.9",
+    "sweep_o": "sweep_site_o_512to512_T65536_K32_gaussian",
+    "sweep_up": "sweep_site_up_512to2048_T65536_K32_gaussian",
+    "sweep_down": "sweep_site_down_2048to512_T65536_K32_gaussian",
     "forward_g": "forward_mlp_up_512to2048_T16384_8draws+clean_gaussian",
     "forward_r": "forward_mlp_up_512to2048_T16384_8draws+clean_rademacher",
     "forward_rp": "forward_mlp_up_512to2048_T16384_8draws+clean_rademacher_packed",
@@ -188,12 +218,25 @@ FORWARD_KIND = {"forward_g": 1, "forward_r": 0, "forward_rp": 3}
 FORWARD_METRIC = "Dust jittered-forward token-draws/s at 1 GB300 (y = XW^T once, y + sigma a per draw)"
 
 
+SWEEP_KINDS = ("qkv", "o", "up", "down")  # order of a layer's sites in the sweep
+
+
 def workload_sites(name):
     import workloads as wl
     if name == "sweep":
         return wl.sweep_sites()
+    if name.startswith("sweep_"):
+        return [wl.sweep_sites()[SWEEP_KINDS.index(name[len("sweep_"):])]]
     return [{"mlp_up": wl.MLP_UP, "toy": wl.TOY, "qkv": wl.QKV_DECAY, "square_r": wl.SQUARE_R,
              "square_g": wl.SQUARE_G, "square_rp": wl.SQUARE_RP}[name]]
+
+
+def site_kind(w):
+    """The sweep shape a site belongs to ("qkv", "o", "up", "down"), or None."""
+    for k in SWEEP_KINDS:
+        if w.name.endswith("_" + k) and w.name.startswith("sweep_"):
+            return k
+    return None
 
 
 def make_inputs_fast(w, dev, site):
@@ -212,28 +255,87 @@ def make_inputs_fast(w, dev, site):
 
 # ---------------------------------------------------------- roofline -----
 
-def roofline_for(stage, ms_per_step, sites, peaks, antithetic=False):
+# Per-SM, per-clock unit counts from public tables: used only when no pipe
+# rates were measured (the CPU tests, or --no-pipe-probe).
+DERIVED_PER_CLK_SM = {"xu": 16.0, "alu": 64.0, "issue": 128.0, "fma": 256.0}
+DERIVED_SM, DERIVED_MHZ = 152, 2070.0
+
+
+def measure_pipe_peaks(dust, dev, stream, target_ms=20.0, reps=5):
+    """Rates of the XU, ALU, FMA and issue pipes on this device from the
+    library's probe kernels (dust_pipe_probe), timed with CUDA events on
+    `stream`, with the SM clock sampled meanwhile. Returns per-clock, per-SM
+    rates so that a roofline can be scaled to the clock of another region."""
+    import torch
+    sink = torch.empty(dust.dust_pipe_probe_threads(), dtype=torch.float32, device=dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    pipes = {"xu": dust.PIPE_XU, "alu": dust.PIPE_ALU, "fma": dust.PIPE_FMA,
+             "issue": dust.PIPE_ISSUE}
+    rate = {}
+
+    def timed(pipe, steps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        ops = dust.dust_pipe_probe(pipe, steps, sink, stream)
+        b.record(stream)
+        b.synchronize()
+        return ops, a.elapsed_time(b)
+
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        for name, pipe in pipes.items():
+            timed(pipe, 64)
+            ops, ms = timed(pipe, 512)
+            steps = int(max(64, min(1 << 24, 512 * target_ms / max(ms, 1e-3))))
+            runs = [timed(pipe, steps) for _ in range(reps)]
+            rate[name] = statistics.median(o / (m * 1e-3) for o, m in runs)
+    cs = clk.summary()
+    mhz = cs["sm_mhz"] or cs["sm_max_mhz"] or DERIVED_MHZ
+    return {"sm_count": sms, "probe_sm_mhz": mhz, "probe_clock_samples": cs["samples"],
+            "rate_per_s": rate,
+            "per_clk_per_sm": {k: v / (sms * mhz * 1e6) for k, v in rate.items()}}
+
+
+def pipe_peak(peaks, pipe, clock_mhz=None):
+    """(ops/s, source) for `pipe`: the measured per-clock, per-SM rate times
+    the SM count times the SM clock of the timed region (the probe's own
+    clock when none was sampled); derived from unit counts when no probe
+    ran."""
+    m = peaks.get("pipes")
+    if m:
+        mhz = clock_mhz or m["probe_sm_mhz"]
+        v = m["per_clk_per_sm"][pipe] * m["sm_count"] * mhz * 1e6
+        return v, ("measured: dust_pipe_probe %s rate %.3g ops/clk/SM at %.0f MHz on %d SMs, "
+                   "scaled to %.0f MHz (of measured)"
+                   % (pipe, m["per_clk_per_sm"][pipe], m["probe_sm_mhz"], m["sm_count"], mhz))
+    v = DERIVED_PER_CLK_SM[pipe] * DERIVED_SM * DERIVED_MHZ * 1e6
+    return v, ("derived: %g ops/clk/SM x %d SMs x %.0f MHz (no probe run)"
+               % (DERIVED_PER_CLK_SM[pipe], DERIVED_SM, DERIVED_MHZ))
+
+
+def roofline_for(stage, ms_per_step, sites, peaks, antithetic=False, clock_mhz=None):
     """Roofline of the dominant kernel family, from its CUDA-event time per
     step and the algorithmic work of one step (summed over the step's sites):
       weight / fused (Gaussian): 2 transcendental (XU) ops per element-draw
         (Box-Muller's log, sqrt, sin, cos per channel pair) -> bound "alu"
-        against the XU pipe: 16 ops/clk/SM x 152 SMs x 2.07 GHz;
+        against the measured XU rate (lg2/sqrt/sin/cos.approx);
       weight / fused (Rademacher): 4 integer-ALU-pipe ops per element-draw (the
         key xor, fmix32's xor-shift by 13 (shift + xor) and the sign merge into
         the reward; its two multiplies issue on the FMA pipe) -> bound "alu"
-        against the ALU pipe: 64 ops/clk/SM x 152 SMs x 2.07 GHz;
+        against the measured ALU rate (shr + xor);
       weight (packed signs): bound by instruction issue (ncu: issue slots 92 %
         busy, ALU 65 %, FMA 56 %): per element-draw 3 issued instructions (the
         shift that brings the channel's bit to the sign position, the masked
         xor into the reward, the add) plus the word's ~8 (key xor, two
         multiplies, two xor-shifts) shared by 32 channels -> 3.25 lane
-        instructions per element-draw against 4 warp instructions per clock per
-        SM: 128 lanes x 152 SMs x 2.07 GHz;
-      gemm_tc: 2 T d_in d_out FLOP -> bound "tensor" (measured bf16 peak);
-      gemm_simt: same FLOP on FFMA -> "alu", 256 FLOP/clk/SM x 152 x 2.07 GHz.
+        instructions per element-draw against the measured issue rate;
+      gemm_tc: 2 T d_in d_out FLOP -> bound "tensor" against the measured
+        burst bf16 peak (the contraction runs for microseconds to a few
+        milliseconds at a time, inside steps far shorter than the seconds-long
+        loop behind the sustained figure, which is reported beside it);
+      gemm_simt: same FLOP on FFMA -> "alu" against the measured FMA rate.
     With antithetic pairs the weighting kernel evaluates each base draw's
     noise once (K / 2 noise draws per token); the fused kernel still K."""
-    sm, clk = 152, 2.07e9
     s = ms_per_step / 1000.0
     el = float(sum(w.element_draws for w in sites))
     if antithetic and stage == "weight":
@@ -241,29 +343,29 @@ def roofline_for(stage, ms_per_step, sites, peaks, antithetic=False):
     fl = float(sum(w.gemm_flops for w in sites))
     if stage in ("weight", "fused"):
         if sites[0].kind == 1:
-            ops, peak = 2.0 * el, 16 * sm * clk
+            ops, pipe = 2.0 * el, "xu"
         elif sites[0].kind == 3:
-            ops, peak = 3.25 * el, 128 * sm * clk
+            ops, pipe = 3.25 * el, "issue"
         else:
-            ops, peak = 4.0 * el, 64 * sm * clk
+            ops, pipe = 4.0 * el, "alu"
+        peak, src = pipe_peak(peaks, pipe, clock_mhz)
         ach = ops / s
-        return {"bound": "alu", "achieved": ach / 1e9, "peak": peak / 1e9, "unit": "Gop/s",
-                "frac": ach / peak, "traffic": None, "kernel": stage,
-                "algorithmic_per_step": ops,
-                "peak_source": "derived: unit counts x 152 SMs x 2.07 GHz max SM clock"}
+        return {"bound": "alu", "pipe": pipe, "achieved": ach / 1e9, "peak": peak / 1e9,
+                "unit": "Gop/s", "frac": ach / peak, "traffic": None, "kernel": stage,
+                "algorithmic_per_step": ops, "peak_source": src}
     if stage == "gemm_tc":
-        peak = peaks.get("bf16_tflops_sustained", 1694.3) * 1e12
+        peak = peaks.get("bf16_tflops", 1898.2) * 1e12
+        sus = peaks.get("bf16_tflops_sustained", 1694.3) * 1e12
         ach = fl / s
         return {"bound": "tensor", "achieved": ach / 1e12, "peak": peak / 1e12,
-                "unit": "TFLOP/s", "frac": ach / peak, "traffic": None, "kernel": stage,
-                "algorithmic_per_step": fl,
-                "peak_source": "MEASURED_PEAKS.json bf16_tflops_sustained (of measured)"}
-    peak = 256 * sm * clk
+                "unit": "TFLOP/s", "frac": ach / peak, "frac_of_sustained": ach / sus,
+                "traffic": None, "kernel": stage, "algorithmic_per_step": fl,
+                "peak_source": "MEASURED_PEAKS.json bf16_tflops, burst (of measured)"}
+    peak, src = pipe_peak(peaks, "fma", clock_mhz)
     ach = fl / s
-    return {"bound": "alu", "achieved": ach / 1e12, "peak": peak / 1e12, "unit": "TFLOP/s",
-            "frac": ach / peak, "traffic": None, "kernel": stage,
-            "algorithmic_per_step": fl,
-            "peak_source": "derived: 128 FFMA lanes x 2 FLOP x 152 SMs x 2.07 GHz"}
+    return {"bound": "alu", "pipe": "fma", "achieved": ach / 1e12, "peak": peak / 1e12,
+            "unit": "TFLOP/s", "frac": ach / peak, "traffic": None, "kernel": stage,
+            "algorithmic_per_step": fl, "peak_source": src}
 
 
 def load_peaks():
@@ -276,13 +378,13 @@ def load_peaks():
                 "fallback": True}
 
 
-def forward_roofline(ms, T, d_in, d_out, K, clean, kind, peaks):
+def forward_roofline(ms, T, d_in, d_out, K, clean, kind, peaks, clock_mhz=None):
     """Roofline of one jittered forward launch (k_forward):
       algorithmic bytes = 2 (T d_in + d_out d_in + (clean + K) T d_out): X and
         W read once, every output slice written once (bf16);
       Gaussian: 2 XU ops per element-draw (K T d_out), as for the weighting
-        kernel -> bound "alu" against 16 XU ops/clk/SM x 152 SMs x 2.07 GHz
-        when that fraction is the larger one;
+        kernel -> bound "alu" against the measured XU rate when that fraction
+        is the larger one;
       signs: bound "hbm" against the measured copy bandwidth."""
     s = ms / 1000.0
     byts = 2.0 * (T * d_in + d_out * d_in + (clean + K) * T * d_out)
@@ -292,13 +394,13 @@ def forward_roofline(ms, T, d_in, d_out, K, clean, kind, peaks):
            "algorithmic_per_step": byts,
            "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)"}
     if kind == 1:
-        ops, peak = 2.0 * K * T * d_out, 16 * 152 * 2.07e9
+        ops = 2.0 * K * T * d_out
+        peak, src = pipe_peak(peaks, "xu", clock_mhz)
         if ops / s / peak > out["frac"]:
-            out = {"bound": "alu", "achieved": ops / s / 1e9, "peak": peak / 1e9,
+            out = {"bound": "alu", "pipe": "xu", "achieved": ops / s / 1e9, "peak": peak / 1e9,
                    "unit": "Gop/s", "frac": ops / s / peak, "traffic": None,
                    "kernel": "forward", "algorithmic_per_step": ops,
-                   "hbm_frac": byts / s / hbm,
-                   "peak_source": "derived: 16 XU ops/clk/SM x 152 SMs x 2.07 GHz"}
+                   "hbm_frac": byts / s / hbm, "peak_source": src}
     return out
 
 
@@ -325,20 +427,32 @@ def kernel_source_hash(kernel):
     return h.hexdigest()[:16]
 
 
-def traffic_from_profiles(kernel, entry=None):
-    """DRAM bytes (read + write) per launch from a committed ncu capture, if
-    the kernel's sources are unchanged since the capture (else None).  `entry`
-    names a capture of one workload of the kernel (default: the kernel)."""
+def traffic_from_profiles(kernel, workload):
+    """DRAM bytes (read + write) per launch of `kernel` on `workload` from a
+    committed ncu capture (profiles/traffic.json, key "kernel:workload"), if
+    the kernel's sources are unchanged since the capture (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
     except (OSError, ValueError):
         return None
-    e = d.get(entry or kernel)
+    e = d.get("%s:%s" % (kernel, workload))
     if not e or e.get("source_hash") != kernel_source_hash(kernel):
         return None
     return e.get("dram_bytes_per_launch")
+
+
+def traffic_for(kernel, workload, sites):
+    """Per-launch DRAM traffic of `kernel` over a step: for the sweep, the
+    mean over its launches of the four site shapes' captured traffic (None
+    unless all four are current)."""
+    if workload != "sweep":
+        return traffic_from_profiles(kernel, workload)
+    per = {k: traffic_from_profiles(kernel, "sweep_" + k) for k in SWEEP_KINDS}
+    if any(v is None for v in per.values()):
+        return None
+    return sum(per[site_kind(w)] for w in sites) / len(sites)
 
 
 # ------------------------------------------------------------- cpu leg ----
@@ -383,7 +497,76 @@ def cpu_oracle_rate(sites, target_s):
             "kind": "oracle", "sample": "; ".join(desc) + "; %.1f s" % tot_t}
 
 
+def stage_fractions(prof, prof_steps, sites, peaks, anti, clock_mhz):
+    """The metric's named fractions over a step: the contraction against the
+    tensor peak (burst; sustained beside it), the noise/weighting stage
+    against HBM (its bytes: the loss changes or rewards read, g written) and
+    against its binding pipe."""
+    out = {}
+    if "gemm_tc" in prof:
+        g = roofline_for("gemm_tc", prof["gemm_tc"]["total_ms"] / prof_steps, sites, peaks)
+        out["gemm_tc_tensor_frac"] = g["frac"]
+        out["gemm_tc_tensor_frac_of_sustained"] = g["frac_of_sustained"]
+        if "reduce" in prof:
+            ms = (prof["gemm_tc"]["total_ms"] + prof["reduce"]["total_ms"]) / prof_steps
+            out["gemm_tc_with_reduce_tensor_frac"] = roofline_for("gemm_tc", ms, sites,
+                                                                  peaks)["frac"]
+    if "weight" in prof:
+        byts = float(sum(4 * w.K * w.T + (2 if w.x_dtype == "bf16" else 4) * w.T * w.d_out
+                         for w in sites))
+        ms_w = prof["weight"]["total_ms"] / prof_steps
+        out["weight_hbm_frac"] = byts / (ms_w / 1000.0) / (peaks.get("hbm_gbs", 6800.0) * 1e9)
+        r = roofline_for("weight", ms_w, sites, peaks, anti, clock_mhz)
+        out["weight_%s_frac" % r["pipe"]] = r["frac"]
+    return out
+
+
+def site_kind_breakdown(dust, bundles, flags, stream, flush, peaks, anti, clock_mhz, reps=5):
+    """Per distinct site shape of a multi-site step: one site of that shape
+    run `reps` times with per-kernel events; its kernels' times, their share
+    of the site's profiled time, and the stage fractions."""
+    import torch
+    groups = {}
+    for b in bundles:
+        w = b["w"]
+        groups.setdefault((w.d_in, w.d_out, w.gamma), []).append(b)
+    out = {}
+    for (d_in, d_out, gamma), bs in groups.items():
+        b = bs[0]
+        w = b["w"]
+        dust.dust_profile_enable(True)
+        dust.dust_profile_read()
+        for _ in range(reps):
+            flush.zero_()
+            dust.dust_estimate_gW(b["X"], b["delta"], w.d_out, b["so"], w.seed, w.kind, 0,
+                                  w.sigma, w.gamma, 1.0, flags, gW=b["gW"], workspace=b["ws"],
+                                  stream=stream)
+        torch.cuda.synchronize()
+        prof = {k: {"launches": v[0], "total_ms": v[1]} for k, v in
+                dust.dust_profile_read().items()}
+        dust.dust_profile_enable(False)
+        tot = sum(v["total_ms"] for v in prof.values()) / reps
+        out[site_kind(w) or "%dx%d" % (d_in, d_out)] = {
+            "d_in": d_in, "d_out": d_out, "gamma": gamma, "sites": len(bs),
+            "us_per_site": {k: 1000.0 * v["total_ms"] / reps for k, v in prof.items()},
+            "profiled_us_per_site": 1000.0 * tot,
+            "stage_fractions": stage_fractions(prof, reps, [w], peaks, anti, clock_mhz)}
+    return out
+
+
+def reference_sample_tokens(step_s_per_token, steps, warmup, budget_s=150.0, cap=1024):
+    """Tokens per site per reference step: one whole sequence (up to `cap`)
+    when the run fits `budget_s`, fewer (a multiple of 16, at least 16) when
+    it would not."""
+    n = budget_s / max(1e-9, step_s_per_token * (steps + warmup))
+    return int(max(16, min(cap, (int(n) // 16) * 16)))
+
+
 def run_reference(args):
+    """The reference arm: the fp64 CPU oracle, as it stands, on the host cores,
+    on a bounded sample of the same workload per step (for the sweep: the
+    first tokens of one sequence of each of its four site shapes, all draws
+    and all channels; a single layer: the first tokens of one sequence)."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
@@ -391,37 +574,61 @@ def run_reference(args):
     import oracle
     import workloads as wl
 
-    w = wl.MLP_UP
-    X = wl.to_bf16_exact(wl.make_X(w))
-    dp = wl.make_dplant(w)
-    eps = wl.make_eps(w)
-    # One step = the oracle's whole path on one sequence of the workload.
-    T = w.seq_len
-    so = np.array([0, T], np.int32)
-    delta = oracle.planted_delta(dp[:T], w.seed, w.kind, 0, w.K, np.float32(w.sigma),
-                                 w.curvature, eps[:, :T]).astype(np.float32)
+    sites = workload_sites(args.workload)
+    reps = {}
+    for w in sites:  # one representative per distinct shape
+        reps.setdefault((w.d_in, w.d_out, w.gamma), w)
+    reps = list(reps.values())
+    rng = np.random.default_rng(7)
 
-    def step():
-        oracle.estimate_gW(X[:T], delta, w.d_out, so, w.seed, w.kind, 0, np.float32(w.sigma),
-                           np.float32(w.gamma), 1.0, oracle.CENTER)
+    def inputs(w, T):
+        X = rng.standard_normal((T, w.d_in), dtype=np.float32)
+        if w.x_dtype == "bf16":
+            X = wl.to_bf16_exact(X)
+        dp = rng.standard_normal((T, w.d_out), dtype=np.float32)
+        eps = (w.eps_std * rng.standard_normal((w.K, T))).astype(np.float32)
+        delta = oracle.planted_delta(dp, w.seed, w.kind, 0, w.K, np.float32(w.sigma),
+                                     w.curvature, eps).astype(np.float32)
+        return X, delta, np.array([0, T], np.int32)
 
+    def step_fn(T):
+        data = [(w, inputs(w, T)) for w in reps]
+
+        def step():
+            for w, (X, delta, so) in data:
+                oracle.estimate_gW(X, delta, w.d_out, so, w.seed, w.kind, 0,
+                                   np.float32(w.sigma), np.float32(w.gamma), 1.0, oracle.CENTER)
+        return step
+
+    # size the sample from one 16-token step
+    probe = step_fn(16)
+    t0 = time.perf_counter()
+    probe()
+    per_token = (time.perf_counter() - t0) / 16
+    T = reference_sample_tokens(per_token, args.steps, args.warmup,
+                                cap=min(w.seq_len for w in reps))
+    step = step_fn(T)
     for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         step()
     dt = time.perf_counter() - t0
-    value = w.K * T * args.steps / dt
+    units = sum(w.K * T for w in reps)
+    value = units * args.steps / dt
     cores = oracle.num_threads()
+    sample = ("per step: the first %d tokens of one sequence of each of %d site shape(s) (%s), "
+              "all draws and channels" % (T, len(reps), ", ".join(
+                  "%d->%d gamma %g" % (w.d_in, w.d_out, w.gamma) for w in reps)))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": WORKLOADS["mlp_up"], "sample_tokens_per_step": T,
-                                        "d_in": w.d_in, "d_out": w.d_out, "K": w.K},
+        "data": "synthetic",
+        "config": {"workload": WORKLOADS[args.workload], "sample_tokens_per_site": T,
+                   "site_shapes": len(reps), "token_draws_per_step": units},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": "one %d-token sequence per step, all draws and channels"
-                                   % T},
+                         "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -464,12 +671,16 @@ def run_gb300(args):
     sites = workload_sites(args.workload)
     flags = dust.CENTER | (args.flags or 0)
     stream = torch.cuda.current_stream()
+    peaks = load_peaks()
+    if not args.no_pipe_probe:
+        peaks["pipes"] = measure_pipe_peaks(dust, dev, stream)
+    fast = args.workload.startswith("sweep")
     bundles = []
     for i, w in enumerate(sites):
-        if len(sites) == 1:
-            X, delta, so = make_inputs(w, dev)
-        else:
+        if fast:
             X, delta, so = make_inputs_fast(w, dev, i)
+        else:
+            X, delta, so = make_inputs(w, dev)
         xd = dust.BF16 if X.dtype == torch.bfloat16 else dust.F32
         ws = torch.empty(dust.dust_estimate_gW_workspace(w.T, w.d_in, w.d_out, w.K, xd, flags),
                          dtype=torch.uint8, device=dev)
@@ -509,6 +720,8 @@ def run_gb300(args):
     barrier()
     ms_total = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
     value, ms_per_step = aggregate(units, ms_total, args.steps, world, max_over_ranks)
+    clock_summary = clocks.summary()
+    clock_mhz = clock_summary.get("sm_mhz")
 
     # ---- profiled pass for per-kernel times: the same steps, as many as the
     # library's profile buffer holds (one step's launch count measured first)
@@ -527,30 +740,24 @@ def run_gb300(args):
     dust.dust_profile_enable(False)
     launches_per_step = sum(v["launches"] for v in prof.values()) / prof_steps
     top = max(prof.items(), key=lambda kv: kv[1]["total_ms"])
-    peaks = load_peaks()
     anti = bool(flags & dust.ANTITHETIC)
-    roof = roofline_for(top[0], top[1]["total_ms"] / prof_steps, sites, peaks, anti)
+    roof = roofline_for(top[0], top[1]["total_ms"] / prof_steps, sites, peaks, anti, clock_mhz)
     roof["launches_per_step"] = top[1]["launches"] / prof_steps
-    roof["traffic"] = traffic_from_profiles(top[0]) if len(sites) == 1 else None
+    roof["traffic"] = traffic_for(top[0], args.workload, sites)
     tot_ms = sum(x["total_ms"] for x in prof.values())
     breakdown = {k: {"launches": v["launches"],
                      "ms_per_launch": v["total_ms"] / v["launches"],
                      "share": v["total_ms"] / tot_ms}
                  for k, v in prof.items()}
-    # The metric's two named fractions: the contraction against the tensor
-    # peak, the noise/weighting stage against HBM (its bytes: the loss changes
-    # or rewards read, g written).
-    stage_fracs = {}
-    if "gemm_tc" in prof:
-        g = roofline_for("gemm_tc", prof["gemm_tc"]["total_ms"] / prof_steps, sites, peaks)
-        stage_fracs["gemm_tc_tensor_frac"] = g["frac"]
-    if "weight" in prof:
-        byts = float(sum(4 * w.K * w.T + (2 if w.x_dtype == "bf16" else 4) * w.T * w.d_out
-                         for w in sites))
-        s_w = prof["weight"]["total_ms"] / prof_steps / 1000.0
-        stage_fracs["weight_hbm_frac"] = byts / s_w / (peaks.get("hbm_gbs", 6800.0) * 1e9)
+    stage_fracs = stage_fractions(prof, prof_steps, sites, peaks, anti, clock_mhz)
+    per_kind = None
+    if len(sites) > 1:
+        per_kind = site_kind_breakdown(dust, bundles, flags, stream, flush, peaks, anti,
+                                       clock_mhz)
 
-    # ---- end to end through the host-buffer C ABI entry point
+    # ---- end to end through the host-buffer C ABI entry points: one
+    # dust_estimate_gW_host call for a single layer, one
+    # dust_estimate_gW_host_sites call for the whole sweep
     hosts = []
     for b in bundles:
         hosts.append({"Xh": b["X"].cpu().pin_memory(), "dh": b["delta"].cpu().pin_memory(),
@@ -558,24 +765,34 @@ def run_gb300(args):
                       "gh": torch.empty(tuple(b["gW"].shape), dtype=torch.float32).pin_memory(),
                       "Xs": torch.empty_like(b["X"]), "ds": torch.empty_like(b["delta"]),
                       "ss": torch.empty_like(b["so"]), "gs": torch.empty_like(b["gW"])})
+    host_sites = [{"X_host": h["Xh"], "X_dev": h["Xs"], "delta_host": h["dh"],
+                   "delta_dev": h["ds"], "seq_host": h["sh"], "seq_dev": h["ss"],
+                   "gW_host": h["gh"], "gW_dev": h["gs"], "workspace": b["ws"],
+                   "seed": b["w"].seed, "sigma": b["w"].sigma, "gamma": b["w"].gamma}
+                  for b, h in zip(bundles, hosts)]
 
     def e2e_step():
-        for b, h in zip(bundles, hosts):
+        if len(bundles) > 1:
+            dust.dust_estimate_gW_host_sites(host_sites, sites[0].kind, 0, 1.0, flags,
+                                             stream=stream)
+        else:
+            b, h = bundles[0], hosts[0]
             w = b["w"]
             dust.dust_estimate_gW_host(h["Xh"], h["Xs"], h["dh"], h["ds"], h["sh"], h["ss"],
                                        h["gh"], h["gs"], w.d_out, w.seed, w.kind, 0, w.sigma,
                                        w.gamma, 1.0, flags, workspace=b["ws"], stream=stream)
         stream.synchronize()
 
+    n_e2e = max(3, min(args.e2e_steps, args.steps)) if len(sites) > 1 else args.e2e_steps
     for _ in range(3):
         e2e_step()
     barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(args.e2e_steps):
+    for _ in range(n_e2e):
         e2e_step()
     e2e_s = max_over_ranks(time.perf_counter() - t0)
-    e2e_value = world * units * args.e2e_steps / e2e_s
+    e2e_value = world * units * n_e2e / e2e_s
     h2d = sum(h["Xh"].numel() * h["Xh"].element_size() + h["dh"].numel() * 4 +
               h["sh"].numel() * 4 for h in hosts)
     d2h = sum(h["gh"].numel() * 4 for h in hosts)
@@ -608,11 +825,15 @@ def run_gb300(args):
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+                    "d2h_bytes_per_step": d2h, "steps": n_e2e,
+                    "entry_point": "dust_estimate_gW_host_sites" if len(sites) > 1
+                    else "dust_estimate_gW_host"},
             "gpu_launches": int(round(launches_per_step * args.steps)),
-            "clocks": clocks.summary(),
+            "clocks": clock_summary,
             "breakdown": breakdown,
             "stage_fractions": stage_fracs,
+            "sites_by_shape": per_kind,
+            "pipe_peaks": peaks.get("pipes"),
             "gw_updates_per_s": len(sites) * 1000.0 / ms_per_step,
             "profiled_ms_per_step": tot_ms / prof_steps,
             "profiled_steps": prof_steps,
@@ -757,6 +978,7 @@ def run_forward(args):
     ms_total = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
     value, ms_per_step = aggregate(units, ms_total, args.steps, world, max_over_ranks)
 
+    clock_summary = clocks.summary()
     dust.dust_profile_enable(True)
     dust.dust_profile_read()
     for k in range(args.steps):
@@ -766,7 +988,11 @@ def run_forward(args):
     prof = dust.dust_profile_read()
     dust.dust_profile_enable(False)
     launches, fwd_ms = prof["forward"]
-    roof = forward_roofline(fwd_ms / launches, T, w.d_in, w.d_out, K, 1, kind, load_peaks())
+    peaks = load_peaks()
+    if not args.no_pipe_probe:
+        peaks["pipes"] = measure_pipe_peaks(dust, dev, stream)
+    roof = forward_roofline(fwd_ms / launches, T, w.d_in, w.d_out, K, 1, kind, peaks,
+                            clock_summary.get("sm_mhz"))
     roof["launches_per_step"] = launches / args.steps
     roof["traffic"] = traffic_from_profiles("forward", args.workload)
 
@@ -812,7 +1038,8 @@ def run_forward(args):
                     "h2d_bytes_per_step": (Xh.numel() + Wh.numel()) * 2,
                     "d2h_bytes_per_step": Yh.numel() * 2},
             "gpu_launches": int(launches),
-            "clocks": clocks.summary(),
+            "clocks": clock_summary,
+            "pipe_peaks": peaks.get("pipes"),
         }
         print(json.dumps(line), flush=True)
     if pg is not None:
