@@ -28,6 +28,12 @@ SHAPES = [
     (2000, 256, 3840),     # 5 slices: row blocks of 26, the last 24
     (2000, 256, 2688),     # 7 slices: row blocks of 19, the last 14
     (16384, 256, 256),     # 64 slices: partials
+    # 256-channel tiles (two accumulators), where every token slice keeps at
+    # least 4096 tokens: 4 slices through partials; 5 slices with ragged
+    # channels, inputs and tokens; one slice
+    (16384, 1024, 2048),
+    (24600, 520, 2056),
+    (4096, 2048, 4096),
 ]
 
 
@@ -71,4 +77,8 @@ def test_contract_tensor_core_deterministic():
     a = dust.dust_contract(g, X)
     b = dust.dust_contract(g, X)
     assert torch.equal(a, b)
+    # 256-channel tiles, 4 token slices through fp32 partials
+    g2 = torch.randn((16384, 2048), generator=gen).to(torch.bfloat16).to(dev)
+    X2 = torch.randn((16384, 1024), generator=gen).to(torch.bfloat16).to(dev)
+    assert torch.equal(dust.dust_contract(g2, X2), dust.dust_contract(g2, X2))
     assert dust.dust_last_error() == dust.OK

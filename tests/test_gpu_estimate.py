@@ -295,6 +295,31 @@ def test_estimate_gW_full_size_sampled(w):
     assert rel_fro(got[chan, col], want) <= tol
 
 
+@pytest.mark.slow
+@pytest.mark.parametrize("w", [wl.MLP_UP, wl.sweep_sites()[0]], ids=["mlp_up", "sweep_qkv"])
+def test_fused_full_size_sampled(w):
+    """The fused path (g tiles made in shared memory, never in HBM) at full
+    size against the oracle: the up-projection the bench measures (16,384
+    tokens, K 8, gamma 0) and the sweep's QKV site (65,536 tokens, K 32,
+    gamma 0.9, through the scan's chunk carries), 64 sampled GW entries."""
+    flags = dust.CENTER | dust.FORCE_FUSED
+    assert dust.dust_estimate_gW_path(w.T, w.d_in, w.d_out, w.K, dust.BF16,
+                                      flags) == dust.PATH_FUSED_TC
+    X, delta, so = _inputs(w, planted=w.element_draws <= 1_000_000_000)
+    got = _run(w, X, delta, so, flags).double().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    rng = np.random.default_rng(5)
+    n = 64
+    chan = rng.integers(0, w.d_out, n)
+    col = rng.integers(0, w.d_in, n)
+    chan[:2] = [0, w.d_out - 1]
+    col[:2] = [0, w.d_in - 1]
+    r = oracle.credit(delta, so, np.float32(w.gamma), oracle.CENTER)
+    want = oracle.gW_entries(X, r, w.d_out, chan, col, w.seed, w.kind, 0, np.float32(w.sigma),
+                             1.0, oracle.CENTER)
+    assert rel_fro(got[chan, col], want) <= 1e-2
+
+
 # ------------------------------------------------- fused vs unfused paths --
 
 FUSED_SHAPES = [

@@ -100,14 +100,15 @@ __global__ void __launch_bounds__(256) k_reduce(const float* __restrict__ part, 
         float4* g4 = reinterpret_cast<float4*>(gW);
         for (int64_t q = tid; q < n4; q += stride) {
             float4 v = p4[q];
-            // Up to 8 slices' loads in flight at once; the sum stays in slice order.
-            for (int64_t s0 = 1; s0 < S; s0 += 8) {
-                float4 w[8];
+            // Up to 16 slices' loads in flight at once (slice counts up to 17
+            // in one round); the sum stays in slice order.
+            for (int64_t s0 = 1; s0 < S; s0 += 16) {
+                float4 w[16];
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
+                for (int j = 0; j < 16; ++j)
                     if (s0 + j < S) w[j] = p4[(s0 + j) * n4 + q];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
+                for (int j = 0; j < 16; ++j) {
                     if (s0 + j >= S) break;
                     v.x += w[j].x;
                     v.y += w[j].y;
@@ -170,11 +171,14 @@ cudaError_t run(const void* g, const void* X, int64_t T, int64_t d_in, int64_t d
 cudaError_t launch_reduce(const float* partials, int64_t S, int64_t n, float scale,
                           bool accumulate, float* gW, cudaStream_t s) {
     if (n == 0) return cudaSuccess;
-    int64_t rg = (n + 255) / 256;
-    if (rg > 152 * 16) rg = 152 * 16;
-    ProfScope ps(kStageReduce, s);
     const int vec4 = ((n & 3) == 0) && (reinterpret_cast<uintptr_t>(gW) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(partials) % 16 == 0);
+    // One thread per output (per float4 when vectorised), at most 16 CTAs
+    // of 256 threads per SM.
+    const int64_t units = vec4 ? n / 4 : n;
+    int64_t rg = (units + 255) / 256;
+    if (rg > 152 * 16) rg = 152 * 16;
+    ProfScope ps(kStageReduce, s);
     return launch_pdl(k_reduce, dim3(static_cast<unsigned>(rg)), dim3(256), 0, s, partials, S, n,
                       scale, accumulate ? 1 : 0, gW, vec4);
 }

@@ -10,11 +10,17 @@
 // and commits each stage back to the loader; four warps drain TMEM through
 // the idle stage buffers, so that GW is stored along its rows.
 //
-// Tile of one CTA: 128 channels x 256 inputs x one slice of the tokens. When
-// the output tiles alone cannot fill the GPU, the tokens are cut into S
-// fixed slices whose fp32 partials are summed in slice order, so the result
-// does not depend on scheduling: inside a thread-block cluster of the S CTAs
-// when all clusters fit at once, else by a reduction kernel.
+// Tile of one CTA: 128 x MT channels x 256 inputs x one slice of the tokens,
+// MT = 1 or 2 accumulators of 128 rows (MT = 2 uses all 512 TMEM columns and
+// a 3-stage ring of 64 KB stages). The larger tile moves a third fewer
+// operand bytes from L2 into shared memory per FLOP and loads shared memory
+// less per MMA (measured: 4096^2 contraction 781 -> 623 us, qkv 1024 x 3072
+// 104 -> 77 us); it is used where every token slice stays long (see
+// tc_tile_rows). When the output tiles alone cannot fill the GPU, the tokens
+// are cut into S fixed slices whose fp32 partials are summed in slice order,
+// so the result does not depend on scheduling: inside a thread-block cluster
+// of the S CTAs (MT = 1) when all clusters fit at once, else by a reduction
+// kernel.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -27,17 +33,11 @@ namespace dust {
 
 namespace {
 
-#ifndef DUST_GEMM_MT
-#define DUST_GEMM_MT 1       // 128-row accumulators per CTA (1 or 2)
-#endif
 #ifndef DUST_GEMM_BN
 #define DUST_GEMM_BN 256     // inputs per CTA tile (64..256)
 #endif
 #ifndef DUST_GEMM_BK
 #define DUST_GEMM_BK 64      // tokens per stage
-#endif
-#ifndef DUST_GEMM_STAGES
-#define DUST_GEMM_STAGES 4
 #endif
 #ifndef DUST_GEMM_CLUSTER_REDUCE
 #define DUST_GEMM_CLUSTER_REDUCE 1  // reduce the token slices in a cluster (else partials)
@@ -45,25 +45,37 @@ namespace {
 #ifndef DUST_GEMM_PULL
 #define DUST_GEMM_PULL 1  // slices pulled by the summing CTA (else pushed to it)
 #endif
+// The larger tile (two accumulators) where every token slice keeps at least
+// this many tokens (0: never).
+#ifndef DUST_GEMM_MT2_MIN_SLICE
+#define DUST_GEMM_MT2_MIN_SLICE 4096
+#endif
 constexpr bool kClusterReduce = DUST_GEMM_CLUSTER_REDUCE != 0;
 constexpr bool kPull = DUST_GEMM_PULL != 0;
-constexpr int kMT = DUST_GEMM_MT;
-constexpr int kBM = 128 * kMT, kBN = DUST_GEMM_BN, kBK = DUST_GEMM_BK, kStages = DUST_GEMM_STAGES;
+constexpr int kBN = DUST_GEMM_BN, kBK = DUST_GEMM_BK;
 constexpr int kBoxBytes = 64 * kBK * 2;                 // one 64-wide bf16 box of kBK rows
-constexpr int kABytes = (kBM / 64) * kBoxBytes;
-constexpr int kBBytes = (kBN / 64) * kBoxBytes;
-constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
 constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
-constexpr uint32_t kTmemCols = (kMT * kBN <= 256) ? 256u : 512u;
 constexpr uint32_t kIdesc = tc::idesc_bf16_mn(128, kBN);
-static_assert(kMT * kBN <= 512, "accumulators must fit the 512 TMEM columns");
 static_assert(kBK % 16 == 0 && kBN % 64 == 0, "tile shape");
-static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
+// Shape of the kernel with MT accumulators of 128 rows.
+template <int MT>
+struct Cfg {
+    static constexpr int kBM = 128 * MT;                       // channels per tile
+    static constexpr int kStages = MT == 1 ? 4 : 3;            // stages in flight
+    static constexpr int kABytes = (kBM / 64) * kBoxBytes;
+    static constexpr int kBBytes = (kBN / 64) * kBoxBytes;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
+    static constexpr uint32_t kTmemCols = (MT * kBN <= 256) ? 256u : 512u;
+    static_assert(MT * kBN <= 512, "accumulators must fit the 512 TMEM columns");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+};
+
+template <int MT>
 struct Ctl {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
+    uint64_t full[Cfg<MT>::kStages];
+    uint64_t empty[Cfg<MT>::kStages];
     uint64_t done;
     uint64_t never;  // no thread ever arrives here (test hook for the bounded waits)
     uint32_t tmem;
@@ -106,8 +118,11 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, f
 
 constexpr int kRowPad = kBN + 4;  // floats per slot row (16-byte pad: conflict-free stores)
 constexpr int kMaxClusterSlices = 8;  // portable cluster size
+constexpr int kReduceBytes = Cfg<1>::kStages * Cfg<1>::kStageBytes;  // stage buffers, MT = 1
 // S slots of ceil(128 / S) rows each; the most rows over S = 2..8 is 133 (S = 7).
-static_assert(133 * kRowPad * 4 <= kStages * kStageBytes, "slots fit in the stage buffers");
+static_assert(133 * kRowPad * 4 <= kReduceBytes, "slots fit in the stage buffers");
+// The epilogue stages 128 accumulator rows at a time through the stage buffers.
+static_assert(128 * kRowPad * 4 <= Cfg<2>::kStages * Cfg<2>::kStageBytes, "rows fit (MT = 2)");
 
 __device__ void cluster_reduce(unsigned char* smem, uint32_t tmem, bool ok, int64_t m0,
                                int64_t n0, int64_t d_in, int64_t d_out, float* __restrict__ gW,
@@ -176,7 +191,7 @@ __device__ __forceinline__ void st_shared_v4f(uint32_t addr, float a, float b, f
                  : "memory");
 }
 
-static_assert(128 * kRowPad * 4 <= kStages * kStageBytes, "a whole tile fits in the stage buffers");
+static_assert(128 * kRowPad * 4 <= kReduceBytes, "a whole tile fits in the stage buffers");
 
 // The same reduction with each CTA's whole fp32 tile staged in its own shared
 // memory (one row per lane, local stores) and the row blocks pulled: CTA d
@@ -242,14 +257,19 @@ __device__ void cluster_reduce_pull(unsigned char* smem, uint32_t tmem, bool ok,
     cluster_sync_all();  // no CTA leaves while another still reads its tile
 }
 
+template <int MT>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               int64_t d_in, int64_t d_out, int64_t T, int64_t slice, float* __restrict__ out,
               float scale, int mode, unsigned int* __restrict__ status, int stall) {
+    using C = Cfg<MT>;
+    constexpr int kBM = C::kBM, kStages = C::kStages, kABytes = C::kABytes;
+    constexpr int kStageBytes = C::kStageBytes;
+    constexpr uint32_t kTmemCols = C::kTmemCols;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    Ctl* ctl = reinterpret_cast<Ctl*>(smem + kStages * kStageBytes);
+    Ctl<MT>* ctl = reinterpret_cast<Ctl<MT>*>(smem + kStages * kStageBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kBN;
@@ -326,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < kBK / 16; ++kk) {
                 const uint64_t bd = tc::sdesc_sw128(b + kk * 2048, kBoxBytes, 1024);
 #pragma unroll
-                for (int mt = 0; mt < kMT; ++mt) {
+                for (int mt = 0; mt < MT; ++mt) {
                     const uint64_t ad =
                         tc::sdesc_sw128(a + 2 * mt * kBoxBytes + kk * 2048, kBoxBytes, 1024);
                     tc::mma_bf16(tmem + mt * kBN, ad, bd, kIdesc, (it | kk) != 0 ? 1u : 0u);
@@ -350,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float* rows = reinterpret_cast<float*>(smem) + q * 32 * kRowPad;
             const uint32_t rows_s = tc::smem_u32(rows) + 4u * static_cast<uint32_t>(lane * kRowPad);
 #pragma unroll 1
-            for (int mt = 0; mt < kMT; ++mt) {
+            for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll 1
                 for (int c = 0; c < kBN / 32; ++c) {
                     float v[32];
@@ -398,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mbar_wait(&ctl->full[it % kStages], (it / kStages) & 1);
         atomicExch(status, 5u /* DUST_ERR_TIMEOUT */);
     }
-    if (mode >= 3) {
+    if (MT == 1 && mode >= 3) {
         __syncthreads();
         if (kPull)
             cluster_reduce_pull(smem, tmem, !*abort_flag && n_k > 0, m0, n0, d_in, d_out, out,
@@ -416,17 +436,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 
-// Token slices per output tile: enough CTAs to give every SM one tile slice
-// (S = 152 / tiles), each slice at least 4 k-steps. More slices than that
-// measured slower even where they would fill the GPU better (qkv 1024 x 3072,
-// 96 tiles: 3 slices in 2 waves 131 us against 102 us for 1 slice): the
-// CTAs then share one tile feed.
-int64_t tc_slices(int64_t T, int64_t d_in, int64_t d_out) {
-    const int64_t tiles = ((d_out + kBM - 1) / kBM) * ((d_in + kBN - 1) / kBN);
+// Token slices per output tile for tiles of `bm` channels: enough CTAs to
+// give every SM one tile slice (S = 152 / tiles), each slice at least 4
+// k-steps. More slices than that measured slower even where they would fill
+// the GPU better (qkv 1024 x 3072, 96 tiles: 3 slices in 2 waves 131 us
+// against 102 us for 1 slice): the CTAs then share one tile feed.
+int64_t slices_for(int64_t T, int64_t d_in, int64_t d_out, int64_t bm) {
+    const int64_t tiles = ((d_out + bm - 1) / bm) * ((d_in + kBN - 1) / kBN);
     int64_t S = 152 / tiles;
     const int64_t max_s = (T + 4 * kBK - 1) / (4 * kBK);  // at least 4 k-steps per slice
     if (S > max_s) S = max_s;
     return S < 1 ? 1 : S;
+}
+
+// Channels per tile: 256 (two accumulators) when every token slice of the
+// larger tile keeps at least DUST_GEMM_MT2_MIN_SLICE tokens and there are at
+// least 8 such tiles, else 128. Measured (contraction alone, us, 128 -> 256
+// rows): 4096^2 over 32,768 tokens 781 -> 623; 1024 x 3072 over 16,384
+// 104 -> 77; the sweep's 512 -> 2048 and 2048 -> 512 over 65,536 112 -> 101,
+// 512 -> 1536 90 -> 86; but 512 -> 512 over 65,536 (4 larger tiles) 49.5 ->
+// 50.5 and 512 -> 2048 over 16,384 (slices of 1,820 tokens) 42.6 -> 44:
+// there the slices' partials and their reduction outweigh the faster feed.
+int tile_mt(int64_t T, int64_t d_in, int64_t d_out) {
+    if (DUST_GEMM_MT2_MIN_SLICE <= 0) return 1;
+    const int64_t tiles2 = ((d_out + 255) / 256) * ((d_in + kBN - 1) / kBN);
+    if (tiles2 < 8) return 1;
+    const int64_t S = slices_for(T, d_in, d_out, 256);
+    return (T / S >= DUST_GEMM_MT2_MIN_SLICE) ? 2 : 1;
+}
+
+int64_t tc_slices(int64_t T, int64_t d_in, int64_t d_out) {
+    return slices_for(T, d_in, d_out, 128 * tile_mt(T, d_in, d_out));
 }
 
 }  // namespace
@@ -474,9 +514,6 @@ size_t tc_gemm_workspace_bytes(int64_t T, int64_t d_in, int64_t d_out) {
     return S > 1 ? sizeof(float) * static_cast<size_t>(S * d_out * d_in) : 0;
 }
 
-int64_t tc_gemm_tiles(int64_t d_in, int64_t d_out) {
-    return ((d_out + kBM - 1) / kBM) * ((d_in + kBN - 1) / kBN);
-}
 
 namespace {
 
@@ -495,7 +532,7 @@ bool cluster_fits(int S, int64_t tiles) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(1, 1, static_cast<unsigned>(S));
         cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.dynamicSmemBytes = Cfg<1>::kSmemBytes;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 1;
@@ -504,9 +541,9 @@ bool cluster_fits(int S, int64_t tiles) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (ensure_smem_limit(reinterpret_cast<const void*>(k_gemm_tc), kSmemBytes) !=
-                cudaSuccess ||
-            cudaOccupancyMaxActiveClusters(&n, k_gemm_tc, &cfg) != cudaSuccess)
+        if (ensure_smem_limit(reinterpret_cast<const void*>(k_gemm_tc<1>),
+                              Cfg<1>::kSmemBytes) != cudaSuccess ||
+            cudaOccupancyMaxActiveClusters(&n, k_gemm_tc<1>, &cfg) != cudaSuccess)
             n = 0;
         (void)cudaGetLastError();
         max_active[dev][S] = n;
@@ -514,34 +551,31 @@ bool cluster_fits(int S, int64_t tiles) {
     return tiles <= max_active[dev][S];
 }
 
-}  // namespace
-
-cudaError_t launch_tc_gemm(const void* g, const void* X, int64_t T, int64_t d_in, int64_t d_out,
-                           float scale, bool accumulate, float* gW, float* partials,
-                           cudaStream_t s) {
-    CUtensorMap ta, tb;
-    if (!make_tmap_bf16(&ta, g, T, d_out, kBK) || !make_tmap_bf16(&tb, X, T, d_in, kBK))
-        return cudaErrorInvalidValue;
+template <int MT>
+cudaError_t launch_mt(const CUtensorMap& ta, const CUtensorMap& tb, int64_t T, int64_t d_in,
+                      int64_t d_out, float scale, bool accumulate, float* gW, float* partials,
+                      cudaStream_t s) {
+    using C = Cfg<MT>;
     const cudaError_t attr_err =
-        ensure_smem_limit(reinterpret_cast<const void*>(k_gemm_tc), kSmemBytes);
+        ensure_smem_limit(reinterpret_cast<const void*>(k_gemm_tc<MT>), C::kSmemBytes);
     if (attr_err != cudaSuccess) return attr_err;
     unsigned int* st = status_word();
     if (!st) return cudaErrorUnknown;
-    const int64_t S = tc_slices(T, d_in, d_out);
+    const int64_t S = slices_for(T, d_in, d_out, C::kBM);
     int64_t slice = (T + S - 1) / S;
     slice = (slice + kBK - 1) / kBK * kBK;
     const int64_t S_used = (T + slice - 1) / slice;
     dim3 grid(static_cast<unsigned>((d_in + kBN - 1) / kBN),
-              static_cast<unsigned>((d_out + kBM - 1) / kBM), static_cast<unsigned>(S_used));
+              static_cast<unsigned>((d_out + C::kBM - 1) / C::kBM), static_cast<unsigned>(S_used));
     cudaError_t e;
     const int stall = take_stall_injection() ? 1 : 0;
-    if (kClusterReduce && kMT == 1 && S_used >= 2 && S_used <= kMaxClusterSlices &&
+    if (kClusterReduce && MT == 1 && S_used >= 2 && S_used <= kMaxClusterSlices &&
         cluster_fits(static_cast<int>(S_used), static_cast<int64_t>(grid.x) * grid.y)) {
         // The slices of a tile reduce through distributed shared memory.
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = grid;
         cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.dynamicSmemBytes = C::kSmemBytes;
         cfg.stream = s;
         cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -554,7 +588,7 @@ cudaError_t launch_tc_gemm(const void* g, const void* X, int64_t T, int64_t d_in
         cfg.numAttrs = 2;
         {
             ProfScope ps(kStageGemmTc, s);
-            e = cudaLaunchKernelEx(&cfg, k_gemm_tc, ta, tb, d_in, d_out, T, slice, gW, scale,
+            e = cudaLaunchKernelEx(&cfg, k_gemm_tc<MT>, ta, tb, d_in, d_out, T, slice, gW, scale,
                                    accumulate ? 4 : 3, st, stall);
         }
         if (e == cudaSuccess) return e;
@@ -563,11 +597,24 @@ cudaError_t launch_tc_gemm(const void* g, const void* X, int64_t T, int64_t d_in
     const int mode = (S_used > 1) ? 0 : (accumulate ? 2 : 1);
     {
         ProfScope ps(kStageGemmTc, s);
-        e = launch_pdl(k_gemm_tc, grid, dim3(kThreads), kSmemBytes, s, ta, tb, d_in, d_out, T,
-                       slice, S_used > 1 ? partials : gW, scale, mode, st, stall);
+        e = launch_pdl(k_gemm_tc<MT>, grid, dim3(kThreads), C::kSmemBytes, s, ta, tb, d_in,
+                       d_out, T, slice, S_used > 1 ? partials : gW, scale, mode, st, stall);
     }
     if (e != cudaSuccess || S_used == 1) return e;
     return launch_reduce(partials, S_used, d_out * d_in, scale, accumulate, gW, s);
+}
+
+}  // namespace
+
+cudaError_t launch_tc_gemm(const void* g, const void* X, int64_t T, int64_t d_in, int64_t d_out,
+                           float scale, bool accumulate, float* gW, float* partials,
+                           cudaStream_t s) {
+    CUtensorMap ta, tb;
+    if (!make_tmap_bf16(&ta, g, T, d_out, kBK) || !make_tmap_bf16(&tb, X, T, d_in, kBK))
+        return cudaErrorInvalidValue;
+    if (tile_mt(T, d_in, d_out) == 2)
+        return launch_mt<2>(ta, tb, T, d_in, d_out, scale, accumulate, gW, partials, s);
+    return launch_mt<1>(ta, tb, T, d_in, d_out, scale, accumulate, gW, partials, s);
 }
 
 }  // namespace dust
