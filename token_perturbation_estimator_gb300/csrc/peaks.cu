@@ -75,10 +75,10 @@ __device__ __forceinline__ uint32_t alu_step(uint32_t h) {
     asm volatile("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(y) : "r"(a), "r"(b), "r"(h));
     return y;
 }
-// Majority of three values: one three-input logic op.
-__device__ __forceinline__ uint32_t maj3(uint32_t a, uint32_t b, uint32_t c) {
+// (a & b) ^ 0x5BD1E995: one logic op of two registers and an immediate.
+__device__ __forceinline__ uint32_t and_xor(uint32_t a, uint32_t b) {
     uint32_t y;
-    asm volatile("lop3.b32 %0, %1, %2, %3, 0xE8;" : "=r"(y) : "r"(a), "r"(b), "r"(c));
+    asm volatile("lop3.b32 %0, %1, %2, 0x5BD1E995, 0x6A;" : "=r"(y) : "r"(a), "r"(b));
     return y;
 }
 
@@ -157,8 +157,8 @@ __global__ void __launch_bounds__(kThreads) k_pipe_probe(float* __restrict__ sin
         }
         for (int64_t k = 0; k < steps; k += kUnroll) {
             // Per step: 3 FMAs on each fp32 chain and one lop3 on each integer
-            // chain (the majority of it and two others, updated in place):
-            // 4 kChains instructions.
+            // chain (it and the next chain, and-ed, xor-ed with a constant,
+            // updated in place): 4 kChains instructions.
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
 #pragma unroll
@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(kThreads) k_pipe_probe(float* __restrict__ sin
                     a[j] = fma_f(a[j], 0.999f, 0.0001f);
                     a[j] = fma_f(a[j], 1.001f, -0.0001f);
                     a[j] = fma_f(a[j], 0.999f, 0.0001f);
-                    h[j] = maj3(h[j], h[(j + 1) % kChains], h[(j + 3) % kChains]);
+                    h[j] = and_xor(h[j], h[(j + 1) % kChains]);
                 }
             }
         }
