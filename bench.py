@@ -788,11 +788,26 @@ def run_gb300(args):
         e2e_step()
     barrier()
     torch.cuda.synchronize()
+    e2e_times = []
     t0 = time.perf_counter()
     for _ in range(n_e2e):
+        a = time.perf_counter()
         e2e_step()
+        e2e_times.append(time.perf_counter() - a)
     e2e_s = max_over_ranks(time.perf_counter() - t0)
     e2e_value = world * units * n_e2e / e2e_s
+    # The host link's rate for this step's inputs: every X copied host -> device
+    # on one stream with nothing else running (the bound the inputs put on e2e).
+    link = torch.cuda.Stream()
+    la, lb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    la.record(link)
+    with torch.cuda.stream(link):
+        for h in hosts:
+            h["Xs"].copy_(h["Xh"], non_blocking=True)
+    lb.record(link)
+    lb.synchronize()
+    x_bytes = sum(h["Xh"].numel() * h["Xh"].element_size() for h in hosts)
+    link_gbs = x_bytes / (la.elapsed_time(lb) * 1e-3) / 1e9
     h2d = sum(h["Xh"].numel() * h["Xh"].element_size() + h["dh"].numel() * 4 +
               h["sh"].numel() * 4 for h in hosts)
     d2h = sum(h["gh"].numel() * 4 for h in hosts)
@@ -826,6 +841,10 @@ def run_gb300(args):
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": n_e2e,
+                    "ms_per_step_min_median_max": [1000.0 * min(e2e_times),
+                                                   1000.0 * statistics.median(e2e_times),
+                                                   1000.0 * max(e2e_times)],
+                    "x_h2d_link_gbs": link_gbs,
                     "entry_point": "dust_estimate_gW_host_sites" if len(sites) > 1
                     else "dust_estimate_gW_host"},
             "gpu_launches": int(round(launches_per_step * args.steps)),

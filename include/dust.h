@@ -410,8 +410,12 @@ dust_status dust_estimate_gW_host(const void* X_host, void* X_dev, dust_dtype x_
  * (any site's X_dev, delta_dev, seq_dev, gW_dev or workspace): checked on the
  * host, DUST_ERR_INVALID_ARG otherwise. Every argument of every site is
  * checked before anything is enqueued. At most 4096 sites (DUST_ERR_RANGE).
- * gW_host follows dust_estimate_gW_host's rule (written in place over the
- * host link when page-locked and device-mapped, else through gW_dev).
+ * Results: every site but the last writes gW_dev, which an internal return
+ * stream copies to gW_host while later sites compute (gW_dev of those sites
+ * is therefore also read out of stream order and falls under the overlap
+ * rule); the last site follows dust_estimate_gW_host's rule (gW_host written
+ * in place over the host link when page-locked and device-mapped, else
+ * through gW_dev and a copy on `stream`).
  */
 typedef struct {
     const void* X_host;              /* host [T][d_in], x_dtype; page-locked for overlap */

@@ -517,9 +517,10 @@ struct CopyLane {
     std::mutex mu;
     bool ready = false;
     cudaError_t err = cudaSuccess;
-    cudaStream_t copy = nullptr;
-    cudaEvent_t fork = nullptr;
-    std::vector<cudaEvent_t> ev;  // per site: loss changes copied, X copied
+    cudaStream_t copy = nullptr;  // host -> device inputs
+    cudaStream_t ret = nullptr;   // device -> host results of all but the last site
+    cudaEvent_t fork = nullptr, ret_done = nullptr;
+    std::vector<cudaEvent_t> ev;  // per site: loss changes copied, X copied, ĜW ready
 };
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxHostSites = 4096;
@@ -715,7 +716,8 @@ dust_status estimate_host_sites(const dust_host_site* sites, int64_t n, dust_dty
             add(q.X_dev, esz * static_cast<size_t>(q.T * q.d_in), i, true);
             add(q.delta_dev, sizeof(float) * static_cast<size_t>(q.K * q.T), i, i > 0);
             add(q.seq_dev, sizeof(int32_t) * static_cast<size_t>(q.n_seq + 1), i, i > 0);
-            add(q.gW_dev, sizeof(float) * static_cast<size_t>(q.d_out * q.d_in), i, false);
+            // read by the return stream while later sites compute
+            add(q.gW_dev, sizeof(float) * static_cast<size_t>(q.d_out * q.d_in), i, i < n - 1);
             add(q.workspace, q.ws_bytes, i, false);
         }
         for (size_t a = 0; a < rs.size(); ++a) {
@@ -726,16 +728,20 @@ dust_status estimate_host_sites(const dust_host_site* sites, int64_t n, dust_dty
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    // Per site: the device address ĜW goes to. A page-locked, device-mapped
-    // gW_host is written (and, accumulating, read) by the kernels in place,
-    // over the host link, instead of through gW_dev and a copy back.
+    // Per site: the device address ĜW goes to. For the last site (the only
+    // one of a single-site call) a page-locked, device-mapped gW_host is
+    // written (and, accumulating, read) by the kernels in place, over the host
+    // link, instead of through gW_dev and a copy back. Earlier sites write
+    // gW_dev, which a return stream copies back while later sites compute
+    // (in place, each site's writes would hold its contraction, and with it
+    // every later kernel on `stream`, until they crossed the link).
     std::vector<float*> target(static_cast<size_t>(n));
     std::vector<char> direct(static_cast<size_t>(n), 0);
     for (int64_t i = 0; i < n; ++i) {
         const dust_host_site& q = sites[i];
         target[i] = q.gW_dev;
 #if DUST_HOST_DIRECT_GW
-        if (q.d_out * q.d_in > 0) {
+        if (i == n - 1 && q.d_out * q.d_in > 0) {
             cudaPointerAttributes pa;
             if (cudaPointerGetAttributes(&pa, q.gW_host) == cudaSuccess &&
                 pa.type == cudaMemoryTypeHost && pa.devicePointer &&
@@ -766,16 +772,18 @@ dust_status estimate_host_sites(const dust_host_site* sites, int64_t n, dust_dty
     };
     if (n > 0 && (!small_copies(sites[0], s) || !gw_in(0))) return DUST_ERR_CUDA;
 
-    // The copy lane: its stream and two events per site, created on first
-    // use and kept for the life of the process. The lock covers the whole
-    // enqueue sequence, so the events are re-recorded only after every wait
-    // on them has been enqueued.
+    // The copy lane: its input and return streams and three events per site,
+    // created on first use and kept for the life of the process. The lock
+    // covers the whole enqueue sequence, so the events are re-recorded only
+    // after every wait on them has been enqueued. Per site i: ev[3i] its loss
+    // changes and offsets copied, ev[3i+1] its X copied, ev[3i+2] its ĜW
+    // computed into gW_dev (sites before the last).
     bool any_x = false;
     for (int64_t i = 0; i < n; ++i)
         if (sites[i].T * sites[i].d_in > 0 && sites[i].d_out * sites[i].d_in > 0) any_x = true;
     CopyLane* lane = nullptr;
     std::unique_lock<std::mutex> lock;
-    if (any_x) {
+    if (any_x || n > 1) {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
             return DUST_ERR_CUDA;
@@ -784,30 +792,35 @@ dust_status estimate_host_sites(const dust_host_site* sites, int64_t n, dust_dty
         if (!lane->ready) {
             lane->err = cudaStreamCreateWithFlags(&lane->copy, cudaStreamNonBlocking);
             if (lane->err == cudaSuccess)
+                lane->err = cudaStreamCreateWithFlags(&lane->ret, cudaStreamNonBlocking);
+            if (lane->err == cudaSuccess)
                 lane->err = cudaEventCreateWithFlags(&lane->fork, cudaEventDisableTiming);
+            if (lane->err == cudaSuccess)
+                lane->err = cudaEventCreateWithFlags(&lane->ret_done, cudaEventDisableTiming);
             lane->ready = true;
         }
         if (lane->err != cudaSuccess) return DUST_ERR_CUDA;
-        while (lane->ev.size() < static_cast<size_t>(2 * n)) {
+        while (lane->ev.size() < static_cast<size_t>(3 * n)) {
             cudaEvent_t e = nullptr;
             if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess)
                 return DUST_ERR_CUDA;
             lane->ev.push_back(e);
         }
         if (cudaEventRecord(lane->fork, s) != cudaSuccess ||
-            cudaStreamWaitEvent(lane->copy, lane->fork, 0) != cudaSuccess)
+            cudaStreamWaitEvent(lane->copy, lane->fork, 0) != cudaSuccess ||
+            cudaStreamWaitEvent(lane->ret, lane->fork, 0) != cudaSuccess)
             return DUST_ERR_CUDA;
         for (int64_t i = 0; i < n; ++i) {
             const dust_host_site& q = sites[i];
             if (i > 0 && (!small_copies(q, lane->copy) ||
-                          cudaEventRecord(lane->ev[2 * i], lane->copy) != cudaSuccess))
+                          cudaEventRecord(lane->ev[3 * i], lane->copy) != cudaSuccess))
                 return DUST_ERR_CUDA;
             const size_t x_bytes = esz * static_cast<size_t>(q.T * q.d_in);
             if (x_bytes && q.d_out * q.d_in > 0 &&
                 cudaMemcpyAsync(q.X_dev, q.X_host, x_bytes, cudaMemcpyHostToDevice,
                                 lane->copy) != cudaSuccess)
                 return DUST_ERR_CUDA;
-            if (cudaEventRecord(lane->ev[2 * i + 1], lane->copy) != cudaSuccess)
+            if (cudaEventRecord(lane->ev[3 * i + 1], lane->copy) != cudaSuccess)
                 return DUST_ERR_CUDA;
         }
     }
@@ -815,16 +828,10 @@ dust_status estimate_host_sites(const dust_host_site* sites, int64_t n, dust_dty
     for (int64_t i = 0; i < n && result == DUST_OK; ++i) {
         const dust_host_site& q = sites[i];
         if (i > 0) {
-            if (lane) {
-                if (cudaStreamWaitEvent(s, lane->ev[2 * i], 0) != cudaSuccess) {
-                    result = DUST_ERR_CUDA;
-                    break;
-                }
-            } else if (!small_copies(q, s)) {
-                result = DUST_ERR_CUDA;
-                break;
-            }
-            if (!gw_in(i)) {
+            // the inputs came over the copy stream (or, with no lane, go now)
+            const bool ok = lane ? cudaStreamWaitEvent(s, lane->ev[3 * i], 0) == cudaSuccess
+                                 : small_copies(q, s);
+            if (!ok || !gw_in(i)) {
                 result = DUST_ERR_CUDA;
                 break;
             }
@@ -832,16 +839,28 @@ dust_status estimate_host_sites(const dust_host_site* sites, int64_t n, dust_dty
         result = estimate(q.X_dev, x_dtype, q.T, q.d_in, q.delta_dev, q.K, q.d_out, q.seq_dev,
                           q.n_seq, q.seed, kind, draw_begin, q.sigma, q.gamma, scale, flags,
                           target[i], q.workspace, q.ws_bytes, stream,
-                          lane ? lane->ev[2 * i + 1] : nullptr);
+                          lane ? lane->ev[3 * i + 1] : nullptr);
         const size_t gw_bytes = sizeof(float) * static_cast<size_t>(q.d_out * q.d_in);
-        if (result == DUST_OK && gw_bytes && !direct[i] &&
-            cudaMemcpyAsync(q.gW_host, q.gW_dev, gw_bytes, cudaMemcpyDeviceToHost, s) !=
-                cudaSuccess)
+        if (result != DUST_OK || !gw_bytes || direct[i]) continue;
+        if (i < n - 1) {
+            // copied back on the return stream while later sites compute
+            if (cudaEventRecord(lane->ev[3 * i + 2], s) != cudaSuccess ||
+                cudaStreamWaitEvent(lane->ret, lane->ev[3 * i + 2], 0) != cudaSuccess ||
+                cudaMemcpyAsync(q.gW_host, q.gW_dev, gw_bytes, cudaMemcpyDeviceToHost,
+                                lane->ret) != cudaSuccess)
+                result = DUST_ERR_CUDA;
+        } else if (cudaMemcpyAsync(q.gW_host, q.gW_dev, gw_bytes, cudaMemcpyDeviceToHost, s) !=
+                   cudaSuccess) {
             result = DUST_ERR_CUDA;
+        }
     }
     // However the sequence ended, `stream` waits for every copy of the call.
-    if (lane && n > 0 && cudaStreamWaitEvent(s, lane->ev[2 * n - 1], 0) != cudaSuccess)
-        return DUST_ERR_CUDA;
+    if (lane && n > 0) {
+        if (cudaStreamWaitEvent(s, lane->ev[3 * n - 2], 0) != cudaSuccess ||
+            cudaEventRecord(lane->ret_done, lane->ret) != cudaSuccess ||
+            cudaStreamWaitEvent(s, lane->ret_done, 0) != cudaSuccess)
+            return DUST_ERR_CUDA;
+    }
     return result;
 }
 
