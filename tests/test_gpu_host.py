@@ -154,3 +154,37 @@ def test_host_sites_reject_overlapping_staging():
     with pytest.raises(dust.DustError) as e:
         dust.dust_estimate_gW_host_sites([a, b], dust.GAUSSIAN, 0)
     assert e.value.status == dust.ERR_INVALID_ARG
+
+
+def test_host_sites_accumulate_and_empty_site():
+    """Accumulating into existing host gradients (each site's GW_host is read
+    before and written after), with an empty site (no tokens) in the middle,
+    which leaves its accumulated gradient unchanged."""
+    import torch
+    dev = cuda()
+    shapes = [(2048, 256, 512, 8, 0.9), (0, 256, 512, 8, 0.0), (3000, 128, 1024, 16, 0.0)]
+    sites, wants = [], []
+    for i, (T, d_in, d_out, K, gamma) in enumerate(shapes):
+        if T:
+            X, delta, so = _case(30 + i, T, d_in, d_out, K)
+        else:
+            X = torch.empty((0, d_in), dtype=torch.bfloat16)
+            delta = torch.empty((K, 0), dtype=torch.float32)
+            so = torch.zeros(1, dtype=torch.int32)
+        base = torch.randn((d_out, d_in))
+        if T:
+            wants.append(dust.dust_estimate_gW(X.to(dev), delta.to(dev), d_out, so.to(dev),
+                                               200 + i, dust.GAUSSIAN, 0, 1e-3, gamma, 1.0,
+                                               dust.CENTER | dust.ACCUMULATE,
+                                               gW=base.clone().to(dev)).cpu())
+        else:
+            wants.append(base.clone())
+        q = _site(X, delta, so, d_out, 200 + i, gamma, dev)
+        q["gW_host"].copy_(base)
+        sites.append(q)
+    dust.dust_estimate_gW_host_sites(sites, dust.GAUSSIAN, 0, 1.0,
+                                     dust.CENTER | dust.ACCUMULATE)
+    torch.cuda.synchronize()
+    assert dust.dust_last_error() == dust.OK
+    for i, (q, want) in enumerate(zip(sites, wants)):
+        assert torch.equal(q["gW_host"], want), i

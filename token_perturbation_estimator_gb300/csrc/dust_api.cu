@@ -712,12 +712,13 @@ dust_status estimate_host_sites(const dust_host_site* sites, int64_t n, dust_dty
         };
         for (int64_t i = 0; i < n; ++i) {
             const dust_host_site& q = sites[i];
-            if (q.T == 0 || q.d_out * q.d_in == 0) continue;
+            if (q.d_out * q.d_in == 0) continue;
+            // read by the return stream while later sites compute
+            add(q.gW_dev, sizeof(float) * static_cast<size_t>(q.d_out * q.d_in), i, i < n - 1);
+            if (q.T == 0) continue;
             add(q.X_dev, esz * static_cast<size_t>(q.T * q.d_in), i, true);
             add(q.delta_dev, sizeof(float) * static_cast<size_t>(q.K * q.T), i, i > 0);
             add(q.seq_dev, sizeof(int32_t) * static_cast<size_t>(q.n_seq + 1), i, i > 0);
-            // read by the return stream while later sites compute
-            add(q.gW_dev, sizeof(float) * static_cast<size_t>(q.d_out * q.d_in), i, i < n - 1);
             add(q.workspace, q.ws_bytes, i, false);
         }
         for (size_t a = 0; a < rs.size(); ++a) {
