@@ -273,7 +273,8 @@ dust_status dust_credit_scan(const float* delta, int64_t K, int64_t T,
  * GPU that loads it until the process exits; it calls no cudaMalloc or
  * cudaFree. The caller still passes delta, seq_offsets and r (same meaning,
  * layout and results as dust_credit_scan). A call needing more scratch than
- * the capacity (about 4 T + 8 K ceil(T/256) bytes) returns DUST_ERR_RANGE.
+ * the capacity (4 T + 8 (K + 1) ceil(T/256) bytes, each of its four parts
+ * rounded up to 256) returns DUST_ERR_RANGE.
  * The first call on a device looks up the array's device address with that
  * device current; make it before any stream capture. All calls share the
  * array: calls whose GPU work overlaps (several streams or host threads on
