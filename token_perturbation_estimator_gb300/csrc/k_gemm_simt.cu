@@ -87,44 +87,70 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const TG* __restrict__ g,
     }
 }
 
-__global__ void __launch_bounds__(256) k_reduce(const float* __restrict__ part, int64_t S,
-                                                int64_t n, float scale, int accumulate,
-                                                float* __restrict__ gW, int vec4) {
+// gW[q] = scale * sum_{s<S} partials[s][q] (+ gW[q]), the sum in slice
+// order. Vectorised form: each thread sums U float4 outputs per round, with
+// the loads of SB slices of all U outputs issued before any sum, so that a
+// thread keeps about 8 loads in flight however few slices there are (the
+// reduction is bound by L2 latency: with one output per thread a 3-slice
+// reduction over 3072 x 1024 outputs ran as 10 waves of one round trip each),
+// at 3 CTAs per SM.
+template <int U, int SB>
+__global__ void __launch_bounds__(256, 3) k_reduce_v4(const float4* __restrict__ p4, int64_t S,
+                                                   int64_t n4, float scale, int accumulate,
+                                                   float4* __restrict__ g4) {
     pdl_wait();
     pdl_trigger();
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t threads = (int64_t)gridDim.x * blockDim.x;
     const int64_t tid = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-    if (vec4) {
-        const int64_t n4 = n >> 2;
-        const float4* p4 = reinterpret_cast<const float4*>(part);
-        float4* g4 = reinterpret_cast<float4*>(gW);
-        for (int64_t q = tid; q < n4; q += stride) {
-            float4 v = p4[q];
-            // Up to 16 slices' loads in flight at once (slice counts up to 17
-            // in one round); the sum stays in slice order.
-            for (int64_t s0 = 1; s0 < S; s0 += 16) {
-                float4 w[16];
+    for (int64_t base = tid; base < n4; base += U * threads) {
+        float4 v[U];
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    if (s0 + j < S) w[j] = p4[(s0 + j) * n4 + q];
+        for (int u = 0; u < U; ++u) {
+            const int64_t q = base + u * threads;
+            v[u] = q < n4 ? p4[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        for (int64_t s0 = 1; s0 < S; s0 += SB) {
+            float4 w[U][SB];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
+            for (int u = 0; u < U; ++u) {
+                const int64_t q = base + u * threads;
+#pragma unroll
+                for (int j = 0; j < SB; ++j)
+                    if (s0 + j < S && q < n4) w[u][j] = p4[(s0 + j) * n4 + q];
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+#pragma unroll
+                for (int j = 0; j < SB; ++j) {
                     if (s0 + j >= S) break;
-                    v.x += w[j].x;
-                    v.y += w[j].y;
-                    v.z += w[j].z;
-                    v.w += w[j].w;
+                    v[u].x += w[u][j].x;
+                    v[u].y += w[u][j].y;
+                    v[u].z += w[u][j].z;
+                    v[u].w += w[u][j].w;
                 }
             }
-            float4 o = make_float4(scale * v.x, scale * v.y, scale * v.z, scale * v.w);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t q = base + u * threads;
+            if (q >= n4) break;
+            float4 o = make_float4(scale * v[u].x, scale * v[u].y, scale * v[u].z, scale * v[u].w);
             if (accumulate) {
                 const float4 a = g4[q];
                 o = make_float4(a.x + o.x, a.y + o.y, a.z + o.z, a.w + o.w);
             }
             g4[q] = o;
         }
-        return;
     }
+}
+
+__global__ void __launch_bounds__(256) k_reduce(const float* __restrict__ part, int64_t S,
+                                                int64_t n, float scale, int accumulate,
+                                                float* __restrict__ gW) {
+    pdl_wait();
+    pdl_trigger();
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t tid = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
     for (int64_t q = tid; q < n; q += stride) {
         float v = 0.0f;
         for (int64_t s = 0; s < S; ++s) v += part[s * n + q];
@@ -173,14 +199,28 @@ cudaError_t launch_reduce(const float* partials, int64_t S, int64_t n, float sca
     if (n == 0) return cudaSuccess;
     const int vec4 = ((n & 3) == 0) && (reinterpret_cast<uintptr_t>(gW) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(partials) % 16 == 0);
-    // One thread per output (per float4 when vectorised), at most 16 CTAs
-    // of 256 threads per SM.
-    const int64_t units = vec4 ? n / 4 : n;
-    int64_t rg = (units + 255) / 256;
-    if (rg > 152 * 16) rg = 152 * 16;
     ProfScope ps(kStageReduce, s);
-    return launch_pdl(k_reduce, dim3(static_cast<unsigned>(rg)), dim3(256), 0, s, partials, S, n,
-                      scale, accumulate ? 1 : 0, gW, vec4);
+    if (!vec4) {
+        int64_t rg = (n + 255) / 256;
+        if (rg > 152 * 16) rg = 152 * 16;
+        return launch_pdl(k_reduce, dim3(static_cast<unsigned>(rg)), dim3(256), 0, s, partials,
+                          S, n, scale, accumulate ? 1 : 0, gW);
+    }
+    // Outputs per thread and slices per batch: about 8 loads in flight per
+    // thread; one CTA of 256 threads per U x 256 outputs, at most 8 per SM.
+    const int64_t n4 = n / 4;
+    const float4* p4 = reinterpret_cast<const float4*>(partials);
+    float4* g4 = reinterpret_cast<float4*>(gW);
+    const int acc = accumulate ? 1 : 0;
+    auto go = [&](auto kernel, int U) {
+        int64_t rg = (n4 + 256 * U - 1) / (256 * U);
+        if (rg > 152 * 8) rg = 152 * 8;
+        return launch_pdl(kernel, dim3(static_cast<unsigned>(rg)), dim3(256), 0, s, p4, S, n4,
+                          scale, acc, g4);
+    };
+    if (S <= 3) return go(k_reduce_v4<4, 2>, 4);
+    if (S <= 5) return go(k_reduce_v4<2, 4>, 2);
+    return go(k_reduce_v4<1, 8>, 1);
 }
 
 size_t simt_gemm_workspace_bytes(int64_t T, int64_t d_in, int64_t d_out) {

@@ -19,8 +19,8 @@
 // tc_tile_rows). When the output tiles alone cannot fill the GPU, the tokens
 // are cut into S fixed slices whose fp32 partials are summed in slice order,
 // so the result does not depend on scheduling: inside a thread-block cluster
-// of the S CTAs (MT = 1) when all clusters fit at once, else by a reduction
-// kernel.
+// of the S CTAs when all clusters fit at once (one 128-row accumulator at a
+// time), else by a reduction kernel.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -191,13 +191,17 @@ __device__ __forceinline__ void st_shared_v4f(uint32_t addr, float a, float b, f
                  : "memory");
 }
 
-static_assert(128 * kRowPad * 4 <= kReduceBytes, "a whole tile fits in the stage buffers");
+static_assert(128 * kRowPad * 4 <= kReduceBytes &&
+                  128 * kRowPad * 4 <= Cfg<2>::kStages * Cfg<2>::kStageBytes,
+              "a 128-row accumulator fits in the stage buffers");
 
 // The same reduction with each CTA's whole fp32 tile staged in its own shared
 // memory (one row per lane, local stores) and the row blocks pulled: CTA d
 // reads its rows from every CTA of the cluster, in slice order, with loads
 // that run along the rows. A third cluster barrier keeps every tile in place
 // until all its readers are done.
+// One 128-row accumulator at a time: with MT = 2 the kernel calls it for the
+// TMEM columns of each accumulator (tmem + 256 mt) and its rows (m0 + 128 mt).
 __device__ void cluster_reduce_pull(unsigned char* smem, uint32_t tmem, bool ok, int64_t m0,
                                     int64_t n0, int64_t d_in, int64_t d_out,
                                     float* __restrict__ gW, float scale, bool accumulate) {
@@ -418,14 +422,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mbar_wait(&ctl->full[it % kStages], (it / kStages) & 1);
         atomicExch(status, 5u /* DUST_ERR_TIMEOUT */);
     }
-    if (MT == 1 && mode >= 3) {
+    if (mode >= 3) {
         __syncthreads();
-        if (kPull)
-            cluster_reduce_pull(smem, tmem, !*abort_flag && n_k > 0, m0, n0, d_in, d_out, out,
-                                scale, mode == 4);
-        else
+        if (kPull || MT > 1) {
+#pragma unroll 1
+            for (int mt = 0; mt < MT; ++mt)
+                cluster_reduce_pull(smem, tmem + mt * kBN, !*abort_flag && n_k > 0, m0 + 128 * mt,
+                                    n0, d_in, d_out, out, scale, mode == 4);
+        } else {
             cluster_reduce(smem, tmem, !*abort_flag && n_k > 0, m0, n0, d_in, d_out, out, scale,
                            mode == 4);
+        }
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -522,6 +529,7 @@ namespace {
 // SM counts leaves SMs unused and can push a few clusters into a second
 // wave; the fp32 partials then win (measured on the 48-site sweep: 6-CTA
 // clusters 5.1 ms of contraction against 4.3 ms with partials).
+template <int MT>
 bool cluster_fits(int S, int64_t tiles) {
     constexpr int kMaxDev = 64;
     static int max_active[kMaxDev][kMaxClusterSlices + 1] = {};
@@ -532,7 +540,7 @@ bool cluster_fits(int S, int64_t tiles) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(1, 1, static_cast<unsigned>(S));
         cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = Cfg<1>::kSmemBytes;
+        cfg.dynamicSmemBytes = Cfg<MT>::kSmemBytes;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 1;
@@ -541,9 +549,9 @@ bool cluster_fits(int S, int64_t tiles) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (ensure_smem_limit(reinterpret_cast<const void*>(k_gemm_tc<1>),
-                              Cfg<1>::kSmemBytes) != cudaSuccess ||
-            cudaOccupancyMaxActiveClusters(&n, k_gemm_tc<1>, &cfg) != cudaSuccess)
+        if (ensure_smem_limit(reinterpret_cast<const void*>(k_gemm_tc<MT>),
+                              Cfg<MT>::kSmemBytes) != cudaSuccess ||
+            cudaOccupancyMaxActiveClusters(&n, k_gemm_tc<MT>, &cfg) != cudaSuccess)
             n = 0;
         (void)cudaGetLastError();
         max_active[dev][S] = n;
@@ -569,8 +577,8 @@ cudaError_t launch_mt(const CUtensorMap& ta, const CUtensorMap& tb, int64_t T, i
               static_cast<unsigned>((d_out + C::kBM - 1) / C::kBM), static_cast<unsigned>(S_used));
     cudaError_t e;
     const int stall = take_stall_injection() ? 1 : 0;
-    if (kClusterReduce && MT == 1 && S_used >= 2 && S_used <= kMaxClusterSlices &&
-        cluster_fits(static_cast<int>(S_used), static_cast<int64_t>(grid.x) * grid.y)) {
+    if (kClusterReduce && S_used >= 2 && S_used <= kMaxClusterSlices &&
+        cluster_fits<MT>(static_cast<int>(S_used), static_cast<int64_t>(grid.x) * grid.y)) {
         // The slices of a tile reduce through distributed shared memory.
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = grid;
