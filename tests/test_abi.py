@@ -248,3 +248,27 @@ def test_pipe_probe_rejects_bad_arguments(L):
                              NULL) == dust.ERR_INVALID_ARG
     assert L.dust_pipe_probe(dust.PIPE_XU, 100, None, sink, NULL) == dust.ERR_INVALID_ARG
     assert L.dust_pipe_probe(dust.PIPE_XU, 100, C.byref(ops), NULL, NULL) == dust.ERR_INVALID_ARG
+
+
+def test_host_sites_overlap_check_scales_to_many_sites(L):
+    """4096 sites (the most one call takes) with one overlap between the first
+    and the last: found before anything is enqueued, without a quadratic
+    search over the call's buffers."""
+    import time
+    T, d_in, d_out, K = 256, 64, 64, 4
+    ws = C.c_size_t(0)
+    assert L.dust_estimate_gW_workspace(C.byref(ws), T, d_in, d_out, K, dust.BF16,
+                                        dust.CENTER) == dust.OK
+    n = 4096
+    arr = (dust.HostSite * n)()
+    for i in range(n):
+        base = (1 << 40) + i * (1 << 24)  # 16 MiB apart, 256-aligned
+        arr[i] = dust.HostSite(0x1000, base, T, d_in, d_out, 0x2000, base + (1 << 20), K,
+                               0x3000, base + (2 << 20), 1, i, 1e-3, 0.0, 0x4000,
+                               base + (3 << 20), base + (4 << 20), ws.value)
+    arr[n - 1].X_dev = arr[0].workspace + 256
+    t0 = time.perf_counter()
+    st = L.dust_estimate_gW_host_sites(C.cast(arr, C.c_void_p), n, dust.BF16, dust.GAUSSIAN, 0,
+                                       1.0, dust.CENTER, NULL)
+    assert st == dust.ERR_INVALID_ARG
+    assert time.perf_counter() - t0 < 2.0

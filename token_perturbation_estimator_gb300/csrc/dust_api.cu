@@ -2,6 +2,7 @@
 // Everything is enqueued on the caller's stream (dust_estimate_gW_host also
 // copies X on an internal stream and joins back); nothing here allocates
 // device memory or synchronises, except dust_last_error.
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -667,7 +668,6 @@ struct Range {
     bool async;  // written by the copy stream, out of `stream`'s order
 };
 
-bool overlap(const Range& a, const Range& b) { return a.lo < b.hi && b.lo < a.hi; }
 
 // The estimator for several sites from host buffers (see dust.h). Inputs go
 // host -> device over an internal copy stream that runs ahead of the compute
@@ -721,10 +721,15 @@ dust_status estimate_host_sites(const dust_host_site* sites, int64_t n, dust_dty
             add(q.seq_dev, sizeof(int32_t) * static_cast<size_t>(q.n_seq + 1), i, i > 0);
             add(q.workspace, q.ws_bytes, i, false);
         }
-        for (size_t a = 0; a < rs.size(); ++a) {
-            if (!rs[a].async) continue;
-            for (size_t b = 0; b < rs.size(); ++b)
-                if (b != a && overlap(rs[a], rs[b])) return DUST_ERR_INVALID_ARG;
+        // Sorted by start, a range overlaps an earlier one exactly when it
+        // starts before the largest end seen so far; an asynchronous range
+        // may overlap nothing, any other range no asynchronous one.
+        std::sort(rs.begin(), rs.end(), [](const Range& a, const Range& b) { return a.lo < b.lo; });
+        uintptr_t end_all = 0, end_async = 0;
+        for (const Range& r : rs) {
+            if (r.lo < (r.async ? end_all : end_async)) return DUST_ERR_INVALID_ARG;
+            end_all = r.hi > end_all ? r.hi : end_all;
+            if (r.async) end_async = r.hi > end_async ? r.hi : end_async;
         }
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -38,9 +38,13 @@ namespace {
 #define DUST_WEIGHT_CPT 16
 #endif
 // Resident CTAs per SM that the register allocation must allow, per noise
-// kind (Gaussian: 40 registers; Rademacher: 64).
+// kind (narrow Gaussian lanes: 48 registers; Rademacher: 64). The narrow
+// Gaussian lanes now serve only channel counts that are not a multiple of
+// 1024 (the sweep's 512- and 1536-channel sites): there 5 CTAs per SM
+// measured 0.65 % faster than 6 on the 1536-channel site with the scan's
+// rewards (1439 -> 1430 us) and the same on the 512-channel sites.
 #ifndef DUST_WEIGHT_MINB_G
-#define DUST_WEIGHT_MINB_G 6
+#define DUST_WEIGHT_MINB_G 5
 #endif
 #ifndef DUST_WEIGHT_MINB_R
 #define DUST_WEIGHT_MINB_R 4
