@@ -118,15 +118,31 @@ __global__ void __launch_bounds__(256) k_scan_local(const float* __restrict__ de
     } else {
         s_m[tid] = decay_of(t, T, so, n_seq, gamma);
     }
-    // Loads are issued in batches of independent registers before they are
-    // used, so a thread waits for one memory latency per batch rather than one
-    // per draw. The sum's order: each batch of 8 draws summed in draw order,
-    // then the batch sums in order (the weighting kernel's direct path, which
-    // centres without a scan, sums in the same order, so both give the same
-    // bits).
+    // The first draw group's loss changes (all of them when K <= 32) are
+    // loaded once, every load in flight together, and serve both the mean
+    // and the scan. Later draws' loads are issued in batches of independent
+    // registers, so a thread waits for one memory latency per batch rather
+    // than one per draw. The sum's order: each batch of 8 draws summed in
+    // draw order, then the batch sums in order (the weighting kernel's direct
+    // path, which centres without a scan, sums in the same order, so both
+    // give the same bits).
+    const int gn0 = static_cast<int>(K < kDrawGroup ? K : kDrawGroup);
+    float v0[kDrawGroup];
+#pragma unroll
+    for (int k = 0; k < kDrawGroup; ++k) v0[k] = (k < gn0 && t < T) ? delta[k * T + t] : 0.0f;
     float mean = 0.0f;
     if (center && K > 1 && t < T) {
-        for (int64_t i0 = 0; i0 < K; i0 += 8) {
+#pragma unroll
+        for (int b = 0; b < kDrawGroup / 8; ++b) {
+            if (8 * b < K) {
+                float part = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (8 * b + j < K) part += v0[8 * b + j];
+                mean += part;
+            }
+        }
+        for (int64_t i0 = kDrawGroup; i0 < K; i0 += 8) {
             float v[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) v[j] = (i0 + j < K) ? delta[(i0 + j) * T + t] : 0.0f;
@@ -155,14 +171,18 @@ __global__ void __launch_bounds__(256) k_scan_local(const float* __restrict__ de
         // of the group in flight at once.
         {
             float v[kDrawGroup];
+            if (g0 == 0) {
 #pragma unroll
-            for (int k = 0; k < kDrawGroup; ++k)
-                v[k] = (k < gn && t < T) ? delta[(g0 + k) * T + t] : 0.0f;
-            // While the first group's loads are in flight, warp 0 multiplies
-            // out the chunk's decay products in fp64 (a chain of about 20
-            // dependent double-precision steps): the suffix over the lanes
-            // after each lane, P for the lane's 8 tokens, and the chunk
-            // product B as an fp32 pair.
+                for (int k = 0; k < kDrawGroup; ++k) v[k] = v0[k];
+            } else {
+#pragma unroll
+                for (int k = 0; k < kDrawGroup; ++k)
+                    v[k] = (k < gn && t < T) ? delta[(g0 + k) * T + t] : 0.0f;
+            }
+            // In the first group warp 0 multiplies out the chunk's decay
+            // products in fp64 (a chain of about 20 dependent double-precision
+            // steps): the suffix over the lanes after each lane, P for the
+            // lane's 8 tokens, and the chunk product B as an fp32 pair.
             if (g0 == 0 && warp == 0) {
                 double Bl_d = 1.0;
 #pragma unroll
