@@ -689,13 +689,28 @@ def run_gb300(args):
                         "path": dust.dust_estimate_gW_path(w.T, w.d_in, w.d_out, w.K, xd, flags)})
     units = sum(w.token_draws for w in sites)
     flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)  # 256 MB > L2
+    multi = len(bundles) > 1
+    if multi:
+        assert len({w.kind for w in sites}) == 1, "one noise kind per multi-site call"
+        site_arr = dust.SiteArray([{"X": b["X"], "delta": b["delta"], "seq_offsets": b["so"],
+                                    "gW": b["gW"], "workspace": b["ws"], "seed": b["w"].seed,
+                                    "sigma": b["w"].sigma, "gamma": b["w"].gamma}
+                                   for b in bundles])
 
-    def step():
+    def step_sequential():
+        # one dust_estimate_gW per site on one stream: each kernel runs alone
         for b in bundles:
             w = b["w"]
             dust.dust_estimate_gW(b["X"], b["delta"], w.d_out, b["so"], w.seed, w.kind, 0,
                                   w.sigma, w.gamma, 1.0, flags, gW=b["gW"], workspace=b["ws"],
                                   stream=stream)
+
+    def step():
+        # the whole model's sites in one call (the library's compute lanes)
+        if multi:
+            dust.dust_estimate_gW_sites(site_arr, sites[0].kind, 0, 1.0, flags, stream=stream)
+        else:
+            step_sequential()
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -723,18 +738,42 @@ def run_gb300(args):
     clock_summary = clocks.summary()
     clock_mhz = clock_summary.get("sm_mhz")
 
-    # ---- profiled pass for per-kernel times: the same steps, as many as the
-    # library's profile buffer holds (one step's launch count measured first)
+    # ---- the same sites one after another on one stream (no overlap between
+    # sites): the reference point for the multi-site call's lanes
+    seq_ms = None
+    if multi:
+        n_seq = max(1, min(args.steps, 5))
+        for _ in range(2):
+            flush.zero_()
+            step_sequential()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(n_seq):
+            flush.zero_()
+            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            step_sequential()
+            b_.record(stream)
+            b_.synchronize()
+            ts.append(a.elapsed_time(b_))
+        seq_ms = statistics.median(ts)
+
+    # ---- profiled pass for per-kernel times: the sites one after another on
+    # one stream, so that each kernel's events time it alone (in the timed
+    # multi-site step kernels of different sites overlap, and a kernel's
+    # bracketing events would include the time it shares the SMs); as many
+    # steps as the library's profile buffer holds (one step's launch count
+    # measured first)
     dust.dust_profile_enable(True)
     dust.dust_profile_read()
     flush.zero_()
-    step()
+    step_sequential()
     torch.cuda.synchronize()
     per_step = sum(v[0] for v in dust.dust_profile_read().values())
     prof_steps = max(1, min(args.steps, 60000 // max(1, per_step)))
     for k in range(prof_steps):
         flush.zero_()
-        step()
+        step_sequential()
     torch.cuda.synchronize()
     prof = {k: {"launches": v[0], "total_ms": v[1]} for k, v in dust.dust_profile_read().items()}
     dust.dust_profile_enable(False)
@@ -744,6 +783,9 @@ def run_gb300(args):
     roof = roofline_for(top[0], top[1]["total_ms"] / prof_steps, sites, peaks, anti, clock_mhz)
     roof["launches_per_step"] = top[1]["launches"] / prof_steps
     roof["traffic"] = traffic_for(top[0], args.workload, sites)
+    # the same kernel family's work against the whole timed step (for the
+    # multi-site call: with the sites' overlap)
+    roof["frac_of_step"] = roof["frac"] * (top[1]["total_ms"] / prof_steps) / ms_per_step
     tot_ms = sum(x["total_ms"] for x in prof.values())
     breakdown = {k: {"launches": v["launches"],
                      "ms_per_launch": v["total_ms"] / v["launches"],
@@ -856,6 +898,9 @@ def run_gb300(args):
             "gw_updates_per_s": len(sites) * 1000.0 / ms_per_step,
             "profiled_ms_per_step": tot_ms / prof_steps,
             "profiled_steps": prof_steps,
+            "profile_mode": "sites one after another on one stream" if multi else "the step",
+            "sites_call": {"entry_point": "dust_estimate_gW_sites", "lanes": dust.dust_estimate_gW_sites_lanes(),
+                           "sequential_ms_per_step": seq_ms} if multi else None,
         }
         print(json.dumps(line), flush=True)
     if pg is not None:

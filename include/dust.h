@@ -366,6 +366,52 @@ int32_t dust_estimate_gW_path(int64_t T, int64_t d_in, int64_t d_out, int64_t K,
                               dust_dtype x_dtype, uint32_t flags);
 
 /*
+ * dust_estimate_gW_sites — dust_estimate_gW for several layers ("sites") in
+ * one stream-ordered pass, as in the page's section "What the released code
+ * actually does" (one update covers every linear layer): sites[i] is computed
+ * exactly as dust_estimate_gW would compute it with that site's arguments and
+ * the shared x_dtype, kind, draw_begin, scale and flags, and the results are
+ * bit-identical to such calls made one after another. What differs is the
+ * order on the device: the sites run on internal compute lanes of the current
+ * device (streams created on first use, never destroyed), site i on lane
+ * i mod L, which start after everything enqueued on `stream` before this call
+ * and which `stream` waits for at its end (on error paths too). So one site's
+ * contraction (tensor cores) overlaps the next sites' weighting
+ * (transcendental and integer pipes). The same delta or seq_offsets may serve
+ * several sites (Dust's loss changes are one per token and draw for the whole
+ * model).
+ *
+ * Because sites run concurrently, what a site writes (its gW, and its
+ * workspace) must not overlap any buffer of another site (X, delta,
+ * seq_offsets, gW or workspace): checked on the host, DUST_ERR_INVALID_ARG
+ * otherwise. Every argument of every site is checked before anything is
+ * enqueued. At most 4096 sites (DUST_ERR_RANGE). Graph replay as for
+ * dust_estimate_gW: from the second call with identical arguments (the whole
+ * site array included), the call is captured once into a CUDA graph, lanes
+ * and all, and later calls launch that graph on `stream`. Concurrent calls
+ * on one device are serialised on the host while they enqueue.
+ */
+typedef struct {
+    const void* X;                   /* device [T][d_in], x_dtype */
+    int64_t T, d_in, d_out;
+    const float* delta;              /* device f32 [K][T] loss changes */
+    int64_t K;
+    const int32_t* seq_offsets;      /* device i32 [n_seq + 1] */
+    int64_t n_seq;
+    uint64_t seed;                   /* this site's noise seed */
+    float sigma, gamma;
+    float* gW;                       /* device f32 [d_out][d_in] */
+    void* workspace;                 /* device, dust_estimate_gW_workspace bytes */
+    size_t ws_bytes;
+} dust_site;
+
+dust_status dust_estimate_gW_sites(const dust_site* sites, int64_t n_sites, dust_dtype x_dtype,
+                                   dust_noise_kind kind, int64_t draw_begin, float scale,
+                                   uint32_t flags, void* stream);
+/* The number L of compute lanes per device (fixed when the library is built). */
+int32_t dust_estimate_gW_sites_lanes(void);
+
+/*
  * dust_estimate_gW_host — the same computation from HOST buffers: copies
  * X_host -> X_dev, delta_host -> delta_dev and seq_offsets_host -> seq_dev,
  * runs dust_estimate_gW, and copies gW_dev -> gW_host. With DUST_ACCUMULATE,
@@ -396,21 +442,25 @@ dust_status dust_estimate_gW_host(const void* X_host, void* X_dev, dust_dtype x_
  * sites[i] is computed exactly as dust_estimate_gW_host would compute it with
  * that site's arguments and the shared x_dtype, kind, draw_begin, scale and
  * flags, and the results are bit-identical to such calls made one after
- * another. What differs is the copying: the inputs of later sites travel
- * host -> device while earlier sites compute. Site 0's loss changes and
+ * another. What differs is the copying and the order on the device: the
+ * inputs of later sites travel host -> device while earlier sites compute,
+ * and with more than one site the sites compute on the compute lanes of
+ * dust_estimate_gW_sites (site i on lane i mod L). Site 0's loss changes and
  * offsets are copied on `stream`; then, on the internal copy stream and after
  * everything enqueued on `stream` before this call, X of site 0 and, for each
  * later site, its loss changes, offsets and X, in site order. Each site's
  * kernels wait for its own loss changes before they start and for its X
- * before the contraction. Every copy of the call has completed when the
- * call's work on `stream` has (also on error paths).
+ * before the contraction. Every copy and every kernel of the call has
+ * completed when the call's work on `stream` has (also on error paths).
  *
  * Because the copy stream writes a site's staging buffers (X_dev of every
  * site; delta_dev and seq_dev of sites after the first) while earlier sites
  * compute, those buffers must not overlap any device buffer of the call
- * (any site's X_dev, delta_dev, seq_dev, gW_dev or workspace): checked on the
- * host, DUST_ERR_INVALID_ARG otherwise. Every argument of every site is
- * checked before anything is enqueued. At most 4096 sites (DUST_ERR_RANGE).
+ * (any site's X_dev, delta_dev, seq_dev, gW_dev or workspace); and because
+ * sites compute concurrently, a site's workspace and gW_dev must not overlap
+ * a buffer of another site. Checked on the host, DUST_ERR_INVALID_ARG
+ * otherwise. Every argument of every site is checked before anything is
+ * enqueued. At most 4096 sites (DUST_ERR_RANGE).
  * Results: every site but the last writes gW_dev, which an internal return
  * stream copies to gW_host while later sites compute (gW_dev of those sites
  * is therefore also read out of stream order and falls under the overlap

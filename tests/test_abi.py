@@ -17,6 +17,20 @@ def L():
     return dust.lib()
 
 
+def _has_gpu():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+# Tests that pass fake device addresses: each call is meant to fail its host
+# checks, but should a check ever let one through, no kernel may be launched
+# on a made-up pointer, so they run only where there is no GPU.
+fake_addresses = pytest.mark.skipif(_has_gpu(), reason="fake device addresses: CPU only")
+
+
 def test_exports_every_declared_function(L):
     names = dust.header_functions()
     assert "dust_estimate_gW" in names and "dust_noise" in names and "dust_jitter_apply" in names
@@ -63,6 +77,7 @@ def _est(L, **kw):
                               a["wsb"], NULL)
 
 
+@fake_addresses
 def test_estimate_rejects_bad_arguments(L):
     fake = C.c_void_p(1 << 20)
     assert _est(L) == dust.ERR_INVALID_ARG                      # null gW
@@ -86,6 +101,7 @@ def test_estimate_rejects_bad_arguments(L):
     assert _est(L, d_out=0) == dust.OK
 
 
+@fake_addresses
 def test_noise_and_jitter_reject_bad_arguments(L):
     fake = C.c_void_p(1 << 20)
     assert L.dust_noise(fake, dust.F32, 0, dust.RAW_WORDS, 0, 1, 4, 4, 0, NULL) == dust.ERR_INVALID_ARG
@@ -100,6 +116,7 @@ def test_noise_and_jitter_reject_bad_arguments(L):
     assert L.dust_jitter_apply(fake, dust.U32, 4, 4, 4, 0, dust.GAUSSIAN, 0, 1.0, 0, NULL) == dust.ERR_INVALID_ARG
 
 
+@fake_addresses
 def test_scan_and_weighting_reject_bad_arguments(L):
     fake = C.c_void_p(1 << 20)
     assert L.dust_credit_scan(fake, 4, 8, fake, 1, 1.5, 1, fake, fake, 1 << 20, NULL) == dust.ERR_INVALID_ARG
@@ -110,6 +127,7 @@ def test_scan_and_weighting_reject_bad_arguments(L):
     assert L.dust_error_estimate(fake, 4, 8, 8, 0, dust.GAUSSIAN, 0, 1.0, 0, fake, dust.U32, NULL) == dust.ERR_INVALID_ARG
 
 
+@fake_addresses
 def test_packed_signs_accepted_where_values_are(L):
     """DUST_NOISE_RADEMACHER_PACKED is a value kind like the other two: it is
     refused as a word stream and as a U32 output, and unknown kinds (4) are
@@ -131,6 +149,7 @@ def test_packed_signs_accepted_where_values_are(L):
         dust.ERR_INVALID_ARG
 
 
+@fake_addresses
 def test_scatter_and_embedding_estimator_validation(L):
     fake = C.c_void_p(1 << 20)
     n = C.c_size_t(0)
@@ -156,6 +175,7 @@ def test_scatter_and_embedding_estimator_validation(L):
                               1 << 30, NULL) == dust.ERR_INVALID_ARG
 
 
+@fake_addresses
 def test_forward_jitter_validation(L):
     """Argument checks of dust_forward_jitter that return before any launch."""
     fake = C.c_void_p(1 << 20)
@@ -204,6 +224,7 @@ def test_binding_rejects_wrong_dtype_and_shape():
                  (torch.float32, torch.bfloat16), shape=(8, 4))
 
 
+@fake_addresses
 def test_host_sites_validation_without_a_device(L):
     """Argument errors of the multi-site host entry point are found on the
     host before anything is enqueued: staging that overlaps another buffer,
@@ -238,6 +259,7 @@ def test_host_sites_validation_without_a_device(L):
     assert call(arr2, 5000) == dust.ERR_RANGE
 
 
+@fake_addresses
 def test_pipe_probe_rejects_bad_arguments(L):
     ops = C.c_double(0.0)
     sink = C.c_void_p(1 << 32)
@@ -250,6 +272,7 @@ def test_pipe_probe_rejects_bad_arguments(L):
     assert L.dust_pipe_probe(dust.PIPE_XU, 100, C.byref(ops), NULL, NULL) == dust.ERR_INVALID_ARG
 
 
+@fake_addresses
 def test_host_sites_overlap_check_scales_to_many_sites(L):
     """4096 sites (the most one call takes) with one overlap between the first
     and the last: found before anything is enqueued, without a quadratic
@@ -270,5 +293,105 @@ def test_host_sites_overlap_check_scales_to_many_sites(L):
     t0 = time.perf_counter()
     st = L.dust_estimate_gW_host_sites(C.cast(arr, C.c_void_p), n, dust.BF16, dust.GAUSSIAN, 0,
                                        1.0, dust.CENTER, NULL)
+    assert st == dust.ERR_INVALID_ARG
+    assert time.perf_counter() - t0 < 2.0
+
+
+def test_site_struct_matches_the_header():
+    # dust_site is 13 eight-byte fields with no padding (its bytes key graphs)
+    assert C.sizeof(dust.Site) == 13 * 8
+    assert C.sizeof(dust.HostSite) == 17 * 8
+
+
+@fake_addresses
+def test_sites_validation_without_a_device(L):
+    """Argument errors of the multi-site device entry point are found on the
+    host before anything is enqueued: what a site writes (gW, workspace)
+    overlapping any buffer of another site, too many sites, a bad site
+    argument, a null site array. (Sharing read-only inputs between sites is
+    accepted; that is checked on the GPU, with real buffers.)"""
+    T, d_in, d_out, K = 1024, 256, 512, 8
+    ws = C.c_size_t(0)
+    assert L.dust_estimate_gW_workspace(C.byref(ws), T, d_in, d_out, K, dust.BF16,
+                                        dust.CENTER) == dust.OK
+
+    def site(base, seed):
+        # fake, 256-aligned, disjoint device addresses from `base`
+        return dust.Site(base, T, d_in, d_out, base + (1 << 24), K, base + (2 << 24), 4, seed,
+                         1e-3, 0.0, base + (3 << 24), base + (4 << 24), ws.value)
+
+    call = lambda a, n: L.dust_estimate_gW_sites(C.cast(a, C.c_void_p), n, dust.BF16,
+                                                  dust.GAUSSIAN, 0, 1.0, dust.CENTER, NULL)
+    arr = (dust.Site * 3)(site(1 << 32, 1), site(2 << 32, 2), site(3 << 32, 3))
+    arr[2].workspace = arr[0].workspace  # two sites writing one workspace
+    assert call(arr, 3) == dust.ERR_INVALID_ARG
+    arr[2].workspace = (3 << 32) + (4 << 24)
+    arr[1].gW = arr[2].X + 1024  # a site's result over another site's input
+    assert call(arr, 3) == dust.ERR_INVALID_ARG
+    arr[1].gW = (2 << 32) + (3 << 24)
+    arr[0].X = arr[2].gW + 1024  # an input inside another site's result
+    assert call(arr, 3) == dust.ERR_INVALID_ARG
+    arr[0].X = 1 << 32
+    arr[2].delta = arr[1].workspace + 4096  # an input inside another site's workspace
+    assert call(arr, 3) == dust.ERR_INVALID_ARG
+    one = (dust.Site * 1)(site(1 << 32, 1))
+    one[0].ws_bytes = 16
+    assert call(one, 1) == dust.ERR_WORKSPACE
+    one[0].ws_bytes = ws.value
+    one[0].gamma = 2.0
+    assert call(one, 1) == dust.ERR_INVALID_ARG
+    assert call(one, 0) == dust.OK  # nothing to do
+    assert call(one, -1) == dust.ERR_INVALID_ARG
+    assert call(one, 5000) == dust.ERR_RANGE
+    assert L.dust_estimate_gW_sites(NULL, 2, dust.BF16, dust.GAUSSIAN, 0, 1.0, dust.CENTER,
+                                    NULL) == dust.ERR_INVALID_ARG
+
+
+@fake_addresses
+def test_host_sites_reject_a_shared_workspace(L):
+    """With several sites the host entry point computes them on concurrent
+    lanes, so two sites may no longer share a workspace (or write into each
+    other's buffers)."""
+    T, d_in, d_out, K = 1024, 256, 512, 8
+    ws = C.c_size_t(0)
+    assert L.dust_estimate_gW_workspace(C.byref(ws), T, d_in, d_out, K, dust.BF16,
+                                        dust.CENTER) == dust.OK
+
+    def site(base, seed):
+        return dust.HostSite(0x1000, base, T, d_in, d_out, 0x2000, base + (1 << 24), K,
+                             0x3000, base + (2 << 24), 4, seed, 1e-3, 0.0, 0x4000,
+                             base + (3 << 24), base + (4 << 24), ws.value)
+
+    arr = (dust.HostSite * 2)(site(1 << 32, 1), site(2 << 32, 2))
+    arr[1].workspace = arr[0].workspace
+    call = lambda a, n: L.dust_estimate_gW_host_sites(C.cast(a, C.c_void_p), n, dust.BF16,
+                                                       dust.GAUSSIAN, 0, 1.0, dust.CENTER, NULL)
+    assert call(arr, 2) == dust.ERR_INVALID_ARG
+    arr[1].workspace = (2 << 32) + (4 << 24)
+    arr[1].gW_dev = arr[0].workspace + 512  # the last site's result (not copied out of order)
+    assert call(arr, 2) == dust.ERR_INVALID_ARG
+
+
+@fake_addresses
+def test_sites_overlap_check_scales_to_many_sites(L):
+    """4096 device sites sharing one delta and one offset array, with one
+    conflict between the first and the last: found on the host in well under
+    a second (sorted sweep, not a search over pairs)."""
+    import time
+    T, d_in, d_out, K = 256, 64, 64, 4
+    ws = C.c_size_t(0)
+    assert L.dust_estimate_gW_workspace(C.byref(ws), T, d_in, d_out, K, dust.BF16,
+                                        dust.CENTER) == dust.OK
+    n = 4096
+    arr = (dust.Site * n)()
+    delta, so = 1 << 39, (1 << 39) + (1 << 20)  # shared by every site
+    for i in range(n):
+        base = (1 << 40) + i * (1 << 24)
+        arr[i] = dust.Site(base, T, d_in, d_out, delta, K, so, 1, i, 1e-3, 0.0,
+                           base + (3 << 20), base + (4 << 20), ws.value)
+    arr[n - 1].gW = arr[0].X + 256
+    t0 = time.perf_counter()
+    st = L.dust_estimate_gW_sites(C.cast(arr, C.c_void_p), n, dust.BF16, dust.GAUSSIAN, 0, 1.0,
+                                  dust.CENTER, NULL)
     assert st == dust.ERR_INVALID_ARG
     assert time.perf_counter() - t0 < 2.0

@@ -64,6 +64,8 @@ def _signatures():
                                         i32, i64, f32, f32, f32, u32, P, P, P, SZ, P]),
         "dust_last_error": (i32, [P]),
         "dust_estimate_gW_host_sites": (i32, [P, i64, i32, i32, i64, f32, u32, P]),
+        "dust_estimate_gW_sites": (i32, [P, i64, i32, i32, i64, f32, u32, P]),
+        "dust_estimate_gW_sites_lanes": (i32, []),
         "dust_credit_scan_noalloc_capacity": (SZ, []),
         "dust_credit_scan_noalloc": (i32, [P, i64, i64, P, i64, f32, u32, P, P]),
         "dust_forward_jitter": (i32, [P, P, i64, i64, i64, u64, i32, i64, i64, f32, u32, i32,
@@ -421,6 +423,68 @@ def dust_pipe_probe_threads():
     if n < 0:
         raise DustError(-n, "dust_pipe_probe_threads")
     return n
+
+
+class Site(C.Structure):
+    """dust_site of include/dust.h: one layer of a multi-site device call."""
+    _fields_ = [("X", C.c_void_p), ("T", C.c_int64), ("d_in", C.c_int64),
+                ("d_out", C.c_int64), ("delta", C.c_void_p), ("K", C.c_int64),
+                ("seq_offsets", C.c_void_p), ("n_seq", C.c_int64), ("seed", C.c_uint64),
+                ("sigma", C.c_float), ("gamma", C.c_float), ("gW", C.c_void_p),
+                ("workspace", C.c_void_p), ("ws_bytes", C.c_size_t)]
+
+
+class SiteArray:
+    """The marshalled site array of a dust_estimate_gW_sites call, built once
+    from a list of dicts (see dust_estimate_gW_sites) and reusable while the
+    tensors it points to live (it keeps references to them)."""
+
+    def __init__(self, sites):
+        import torch
+        self.sites = list(sites)
+        self.arr = (Site * max(1, len(self.sites)))()
+        self.x_dtype = None
+        for i, q in enumerate(self.sites):
+            X, delta, so, gW, ws = q["X"], q["delta"], q["seq_offsets"], q["gW"], q["workspace"]
+            _need_cuda(X, delta, so, gW, ws)
+            _expect(X, "X", (torch.float32, torch.bfloat16), dim=2)
+            T, d_in = X.shape
+            _expect(delta, "delta", (torch.float32,), dim=2)
+            K = delta.shape[0]
+            _expect(delta, "delta", (torch.float32,), shape=(K, T))
+            _expect(so, "seq_offsets", (torch.int32,), dim=1)
+            _expect(gW, "gW", (torch.float32,), dim=2)
+            d_out = gW.shape[0]
+            _expect(gW, "gW", (torch.float32,), shape=(d_out, d_in))
+            _expect(ws, "workspace", (torch.uint8,), dim=1)
+            code = _dtype_code(X)
+            if self.x_dtype is None:
+                self.x_dtype = code
+            elif code != self.x_dtype:
+                raise ValueError("every site's X must have the same dtype")
+            self.arr[i] = Site(_ptr(X), T, d_in, d_out, _ptr(delta), K, _ptr(so), so.numel() - 1,
+                               int(q["seed"]), float(q["sigma"]), float(q["gamma"]), _ptr(gW),
+                               _ptr(ws), ws.numel())
+
+
+def dust_estimate_gW_sites(sites, kind, draw_begin, scale=1.0, flags=CENTER, stream=None):
+    """Several layers on device buffers in one pass on the library's compute
+    lanes (one site's contraction overlaps later sites' weighting).
+    `sites`: a SiteArray, or a list of dicts with the CUDA tensors X [T, d_in]
+    (bf16 or f32, one dtype for all), delta f32 [K, T], seq_offsets i32
+    [n_seq+1], gW f32 [d_out, d_in] (written), a uint8 `workspace` of at least
+    dust_estimate_gW_workspace bytes, and the scalars seed, sigma, gamma.
+    Returns the gW tensors."""
+    a = sites if isinstance(sites, SiteArray) else SiteArray(sites)
+    _check(lib().dust_estimate_gW_sites(C.cast(a.arr, C.c_void_p), len(a.sites),
+                                        BF16 if a.x_dtype is None else a.x_dtype, kind,
+                                        draw_begin, float(scale), flags, _stream(stream)),
+           "dust_estimate_gW_sites")
+    return [q["gW"] for q in a.sites]
+
+
+def dust_estimate_gW_sites_lanes():
+    return int(lib().dust_estimate_gW_sites_lanes())
 
 
 class HostSite(C.Structure):

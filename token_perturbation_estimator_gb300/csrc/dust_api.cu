@@ -457,12 +457,14 @@ dust_status estimate_check(const void* X, dust_dtype x_dtype, int64_t T, int64_t
 // The whole estimator on `stream`. When x_ready is given, X is still being
 // copied on another stream: the stream waits for that event just before the
 // first kernel that reads X (the contraction), so the scan and the weighting
-// overlap the copy.
+// overlap the copy. `lean`: the contraction build that shares an SM with
+// weighting CTAs (for sites running concurrently on the compute lanes).
 dust_status estimate(const void* X, dust_dtype x_dtype, int64_t T, int64_t d_in,
                      const float* delta, int64_t K, int64_t d_out, const int32_t* seq_offsets,
                      int64_t n_seq, uint64_t seed, dust_noise_kind kind, int64_t draw_begin,
                      float sigma, float gamma, float scale, uint32_t flags, float* gW,
-                     void* workspace, size_t ws_bytes, void* stream, cudaEvent_t x_ready) {
+                     void* workspace, size_t ws_bytes, void* stream, cudaEvent_t x_ready,
+                     bool lean = false) {
     const dust_status st =
         estimate_check(X, x_dtype, T, d_in, delta, K, d_out, seq_offsets, n_seq, kind,
                        draw_begin, sigma, gamma, scale, flags, gW, workspace, ws_bytes);
@@ -503,7 +505,7 @@ dust_status estimate(const void* X, dust_dtype x_dtype, int64_t T, int64_t d_in,
     if (e != cudaSuccess) return DUST_ERR_CUDA;
     if (x_ready && cudaStreamWaitEvent(s, x_ready, 0) != cudaSuccess) return DUST_ERR_CUDA;
     if (L.path == DUST_PATH_UNFUSED_TC && tc_gemm_supported(g, X, d_in, d_out))
-        e = launch_tc_gemm(g, X, T, d_in, d_out, scale, acc, gW, part, s);
+        e = launch_tc_gemm(g, X, T, d_in, d_out, scale, acc, gW, part, s, lean);
     else
         e = launch_simt_gemm(g, L.g_bf16, X, x_dtype == DUST_BF16, T, d_in, d_out, scale, acc,
                              gW, part, s);
@@ -524,8 +526,113 @@ struct CopyLane {
     std::vector<cudaEvent_t> ev;  // per site: loss changes copied, X copied, ĜW ready
 };
 constexpr int kMaxDevices = 64;
-constexpr int64_t kMaxHostSites = 4096;
+constexpr int64_t kMaxSites = 4096;
 CopyLane g_lanes[kMaxDevices];
+
+// Compute lanes of the multi-site entry points: streams of one device on
+// which whole sites run, site i on lane i mod kSiteLanes, so that one site's
+// contraction overlaps later sites' weighting. Created on first use and kept
+// for the life of the process; the lock covers a call's whole enqueue
+// sequence, so the fork and join events are re-recorded only after every
+// wait on them has been enqueued. Measured on the 48-site sweep (a GB300):
+// 55.9 ms per pass on one stream, 55.3 on two lanes, 55.0 on three (54.5
+// with the shared-memory carveout that lets a contraction CTA sit beside
+// the weighting CTAs).
+#ifndef DUST_SITE_LANES
+#define DUST_SITE_LANES 3
+#endif
+constexpr int kSiteLanes = DUST_SITE_LANES;
+static_assert(kSiteLanes >= 1, "at least one lane");
+
+struct SiteLanes {
+    std::mutex mu;
+    bool ready = false;
+    cudaError_t err = cudaSuccess;
+    cudaStream_t lane[kSiteLanes] = {};
+    cudaEvent_t fork = nullptr;
+    cudaEvent_t join[kSiteLanes] = {};
+};
+SiteLanes g_site_lanes[kMaxDevices];
+
+// The current device's lanes, locked into `lock` (created on first use);
+// nullptr if they could not be made.
+SiteLanes* site_lanes(std::unique_lock<std::mutex>& lock) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    SiteLanes* L = &g_site_lanes[dev];
+    lock = std::unique_lock<std::mutex>(L->mu);
+    if (!L->ready) {
+        for (int l = 0; l < kSiteLanes && L->err == cudaSuccess; ++l) {
+            L->err = cudaStreamCreateWithFlags(&L->lane[l], cudaStreamNonBlocking);
+            if (L->err == cudaSuccess)
+                L->err = cudaEventCreateWithFlags(&L->join[l], cudaEventDisableTiming);
+        }
+        if (L->err == cudaSuccess)
+            L->err = cudaEventCreateWithFlags(&L->fork, cudaEventDisableTiming);
+        L->ready = true;
+    }
+    return L->err == cudaSuccess ? L : nullptr;
+}
+
+// Lanes 0 .. used-1 start after the work enqueued on `s` so far.
+bool fork_lanes(SiteLanes* L, int used, cudaStream_t s) {
+    if (cudaEventRecord(L->fork, s) != cudaSuccess) return false;
+    for (int l = 0; l < used; ++l)
+        if (cudaStreamWaitEvent(L->lane[l], L->fork, 0) != cudaSuccess) return false;
+    return true;
+}
+
+// `s` waits for everything enqueued on lanes 0 .. used-1.
+bool join_lanes(SiteLanes* L, int used, cudaStream_t s) {
+    for (int l = 0; l < used; ++l)
+        if (cudaEventRecord(L->join[l], L->lane[l]) != cudaSuccess ||
+            cudaStreamWaitEvent(s, L->join[l], 0) != cudaSuccess)
+            return false;
+    return true;
+}
+
+// One device buffer of a multi-site call.
+struct SiteRange {
+    uintptr_t lo, hi;
+    int64_t site;
+    bool written;
+};
+
+// The two largest range ends seen so far that belong to two different sites.
+struct EndsBySite {
+    uintptr_t hi1 = 0, hi2 = 0;
+    int64_t site1 = -1, site2 = -1;
+    void add(uintptr_t hi, int64_t site) {
+        if (site == site1) {
+            if (hi > hi1) hi1 = hi;
+        } else if (hi > hi1) {
+            hi2 = hi1;
+            site2 = site1;
+            hi1 = hi;
+            site1 = site;
+        } else if (hi > hi2) {
+            hi2 = hi;
+            site2 = site;
+        }
+    }
+    // the largest end among sites other than `site`
+    uintptr_t other(int64_t site) const { return site == site1 ? hi2 : hi1; }
+};
+
+// True when no written range overlaps a range of another site. Sorted by
+// start, a range overlaps an earlier one exactly when it starts before that
+// one's end; it conflicts with one of another site when either is written.
+bool sites_disjoint(std::vector<SiteRange>& rs) {
+    std::sort(rs.begin(), rs.end(),
+              [](const SiteRange& a, const SiteRange& b) { return a.lo < b.lo; });
+    EndsBySite all, written;
+    for (const SiteRange& r : rs) {
+        if (r.lo < (r.written ? all : written).other(r.site)) return false;
+        all.add(r.hi, r.site);
+        if (r.written) written.add(r.hi, r.site);
+    }
+    return true;
+}
 
 #ifndef DUST_HOST_DIRECT_GW
 #define DUST_HOST_DIRECT_GW 1
@@ -575,9 +682,122 @@ dust_status enqueue_host(const void* ctx, cudaStream_t s) {
                          a.scale, a.flags, a.gW_host, a.gW, a.workspace, a.ws_bytes, s);
 }
 
+static_assert(sizeof(dust_site) == 13 * 8, "dust_site has no padding (its bytes key graphs)");
+
+// Several sites on the compute lanes (see dust.h): every check first, then
+// site i on lane i mod kSiteLanes between a fork from and a join into `s`.
+dust_status estimate_sites(const dust_site* sites, int64_t n, dust_dtype x_dtype,
+                           dust_noise_kind kind, int64_t draw_begin, float scale, uint32_t flags,
+                           cudaStream_t s) {
+    if (n < 0 || (n > 0 && !sites)) return DUST_ERR_INVALID_ARG;
+    if (n > kMaxSites) return DUST_ERR_RANGE;
+    for (int64_t i = 0; i < n; ++i) {
+        const dust_site& q = sites[i];
+        const dust_status st =
+            estimate_check(q.X, x_dtype, q.T, q.d_in, q.delta, q.K, q.d_out, q.seq_offsets,
+                           q.n_seq, kind, draw_begin, q.sigma, q.gamma, scale, flags, q.gW,
+                           q.workspace, q.ws_bytes);
+        if (st != DUST_OK) return st;
+    }
+    if (n > 1) {
+        const size_t esz = (x_dtype == DUST_BF16) ? 2 : 4;
+        std::vector<SiteRange> rs;
+        rs.reserve(static_cast<size_t>(5 * n));
+        auto add = [&](const void* p, size_t bytes, int64_t site, bool written) {
+            if (p && bytes) {
+                const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+                rs.push_back(SiteRange{lo, lo + bytes, site, written});
+            }
+        };
+        for (int64_t i = 0; i < n; ++i) {
+            const dust_site& q = sites[i];
+            if (q.d_out * q.d_in == 0) continue;  // nothing read or written
+            add(q.gW, sizeof(float) * static_cast<size_t>(q.d_out * q.d_in), i, true);
+            if (q.T == 0) continue;  // gW zeroed (or left), nothing else touched
+            add(q.X, esz * static_cast<size_t>(q.T * q.d_in), i, false);
+            add(q.delta, sizeof(float) * static_cast<size_t>(q.K * q.T), i, false);
+            add(q.seq_offsets, sizeof(int32_t) * static_cast<size_t>(q.n_seq + 1), i, false);
+            add(q.workspace, q.ws_bytes, i, true);
+        }
+        if (!sites_disjoint(rs)) return DUST_ERR_INVALID_ARG;
+    }
+    auto one = [&](const dust_site& q, cudaStream_t cs, bool lean) {
+        return estimate(q.X, x_dtype, q.T, q.d_in, q.delta, q.K, q.d_out, q.seq_offsets,
+                        q.n_seq, q.seed, kind, draw_begin, q.sigma, q.gamma, scale, flags, q.gW,
+                        q.workspace, q.ws_bytes, cs, nullptr, lean);
+    };
+    if (n == 0) return DUST_OK;
+    if (n == 1) return one(sites[0], s, false);
+    std::unique_lock<std::mutex> lock;
+    SiteLanes* L = site_lanes(lock);
+    if (!L) return DUST_ERR_CUDA;
+    const int used = n < kSiteLanes ? static_cast<int>(n) : kSiteLanes;
+    if (!fork_lanes(L, used, s)) return DUST_ERR_CUDA;
+    dust_status result = DUST_OK;
+    for (int64_t i = 0; i < n && result == DUST_OK; ++i)
+        result = one(sites[i], L->lane[i % kSiteLanes], kSiteLanes > 1);
+    // However the sequence ended, `s` waits for what the lanes were given.
+    if (!join_lanes(L, used, s)) return DUST_ERR_CUDA;
+    return result;
+}
+
+// A multi-site call: its shared arguments and its site array (the graph key
+// is both, byte for byte).
+struct SitesCall {
+    const dust_site* sites;
+    int64_t n;
+    int32_t x_dtype, kind;
+    int64_t draw_begin;
+    float scale;
+    uint32_t flags;
+};
+
+dust_status enqueue_sites(const void* ctx, cudaStream_t s) {
+    const SitesCall& c = *static_cast<const SitesCall*>(ctx);
+    return estimate_sites(c.sites, c.n, static_cast<dust_dtype>(c.x_dtype),
+                          static_cast<dust_noise_kind>(c.kind), c.draw_begin, c.scale, c.flags,
+                          s);
+}
+
 }  // namespace
 
 extern "C" {
+
+dust_status dust_estimate_gW_sites(const dust_site* sites, int64_t n_sites, dust_dtype x_dtype,
+                                   dust_noise_kind kind, int64_t draw_begin, float scale,
+                                   uint32_t flags, void* stream) {
+    SitesCall c;
+    c.sites = sites;
+    c.n = n_sites;
+    c.x_dtype = x_dtype;
+    c.kind = kind;
+    c.draw_begin = draw_begin;
+    c.scale = scale;
+    c.flags = flags;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (n_sites < 2 || n_sites > kMaxSites || !sites) return enqueue_sites(&c, s);
+    // key: entry tag and shared arguments, then the site array
+    struct Head {
+        int32_t entry, x_dtype, kind;
+        uint32_t flags;
+        int64_t n, draw_begin;
+        float scale, pad;
+    } h;
+    std::memset(&h, 0, sizeof(h));
+    h.entry = 2;
+    h.x_dtype = x_dtype;
+    h.kind = kind;
+    h.flags = flags;
+    h.n = n_sites;
+    h.draw_begin = draw_begin;
+    h.scale = scale;
+    std::vector<unsigned char> key(sizeof(h) + sizeof(dust_site) * static_cast<size_t>(n_sites));
+    std::memcpy(key.data(), &h, sizeof(h));
+    std::memcpy(key.data() + sizeof(h), sites, sizeof(dust_site) * static_cast<size_t>(n_sites));
+    return graph_call(key.data(), key.size(), s, enqueue_sites, &c);
+}
+
+int32_t dust_estimate_gW_sites_lanes(void) { return kSiteLanes; }
 
 dust_status dust_estimate_gW(const void* X, dust_dtype x_dtype, int64_t T, int64_t d_in,
                              const float* delta, int64_t K, int64_t d_out,
@@ -682,7 +902,7 @@ dust_status estimate_host_sites(const dust_host_site* sites, int64_t n, dust_dty
                                 dust_noise_kind kind, int64_t draw_begin, float scale,
                                 uint32_t flags, void* stream) {
     if (n < 0 || (n > 0 && !sites)) return DUST_ERR_INVALID_ARG;
-    if (n > kMaxHostSites) return DUST_ERR_RANGE;
+    if (n > kMaxSites) return DUST_ERR_RANGE;
     const size_t esz = (x_dtype == DUST_BF16) ? 2 : 4;
     // Every check before anything is enqueued.
     for (int64_t i = 0; i < n; ++i) {
@@ -699,28 +919,35 @@ dust_status estimate_host_sites(const dust_host_site* sites, int64_t n, dust_dty
                             q.workspace, q.ws_bytes);
         if (st != DUST_OK) return st;
     }
-    // Buffers that the copy stream writes while `stream` computes must not
-    // overlap any other device buffer of the call.
+    // Buffers that the copy stream writes while the sites compute must not
+    // overlap any other device buffer of the call; what a site's kernels
+    // write (its workspace and gW_dev) must not overlap a buffer of another
+    // site, whose kernels run on another lane.
     if (n > 1) {
         std::vector<Range> rs;
+        std::vector<SiteRange> sr;
         rs.reserve(static_cast<size_t>(5 * n));
-        auto add = [&](const void* p, size_t bytes, int64_t site, bool async) {
+        sr.reserve(static_cast<size_t>(5 * n));
+        auto add = [&](const void* p, size_t bytes, int64_t site, bool async, bool written) {
             if (p && bytes) {
                 const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
                 rs.push_back(Range{lo, lo + bytes, site, async});
+                sr.push_back(SiteRange{lo, lo + bytes, site, written});
             }
         };
         for (int64_t i = 0; i < n; ++i) {
             const dust_host_site& q = sites[i];
             if (q.d_out * q.d_in == 0) continue;
             // read by the return stream while later sites compute
-            add(q.gW_dev, sizeof(float) * static_cast<size_t>(q.d_out * q.d_in), i, i < n - 1);
+            add(q.gW_dev, sizeof(float) * static_cast<size_t>(q.d_out * q.d_in), i, i < n - 1,
+                true);
             if (q.T == 0) continue;
-            add(q.X_dev, esz * static_cast<size_t>(q.T * q.d_in), i, true);
-            add(q.delta_dev, sizeof(float) * static_cast<size_t>(q.K * q.T), i, i > 0);
-            add(q.seq_dev, sizeof(int32_t) * static_cast<size_t>(q.n_seq + 1), i, i > 0);
-            add(q.workspace, q.ws_bytes, i, false);
+            add(q.X_dev, esz * static_cast<size_t>(q.T * q.d_in), i, true, false);
+            add(q.delta_dev, sizeof(float) * static_cast<size_t>(q.K * q.T), i, i > 0, false);
+            add(q.seq_dev, sizeof(int32_t) * static_cast<size_t>(q.n_seq + 1), i, i > 0, false);
+            add(q.workspace, q.ws_bytes, i, false, true);
         }
+        if (!sites_disjoint(sr)) return DUST_ERR_INVALID_ARG;
         // Sorted by start, a range overlaps an earlier one exactly when it
         // starts before the largest end seen so far; an asynchronous range
         // may overlap nothing, any other range no asynchronous one.
@@ -769,14 +996,14 @@ dust_status estimate_host_sites(const dust_host_site* sites, int64_t n, dust_dty
                                sizeof(int32_t) * static_cast<size_t>(q.n_seq + 1),
                                cudaMemcpyHostToDevice, cs) == cudaSuccess;
     };
-    auto gw_in = [&](int64_t i) {
+    auto gw_in = [&](int64_t i, cudaStream_t cs) {
         const dust_host_site& q = sites[i];
         const size_t gw_bytes = sizeof(float) * static_cast<size_t>(q.d_out * q.d_in);
         if (!(flags & DUST_ACCUMULATE) || !gw_bytes || direct[i]) return true;
-        return cudaMemcpyAsync(q.gW_dev, q.gW_host, gw_bytes, cudaMemcpyHostToDevice, s) ==
+        return cudaMemcpyAsync(q.gW_dev, q.gW_host, gw_bytes, cudaMemcpyHostToDevice, cs) ==
                cudaSuccess;
     };
-    if (n > 0 && (!small_copies(sites[0], s) || !gw_in(0))) return DUST_ERR_CUDA;
+    if (n > 0 && (!small_copies(sites[0], s) || !gw_in(0, s))) return DUST_ERR_CUDA;
 
     // The copy lane: its input and return streams and three events per site,
     // created on first use and kept for the life of the process. The lock
@@ -789,6 +1016,11 @@ dust_status estimate_host_sites(const dust_host_site* sites, int64_t n, dust_dty
         if (sites[i].T * sites[i].d_in > 0 && sites[i].d_out * sites[i].d_in > 0) any_x = true;
     CopyLane* lane = nullptr;
     std::unique_lock<std::mutex> lock;
+    // With several sites the compute runs on the compute lanes (as for
+    // dust_estimate_gW_sites), site i on lane i mod kSiteLanes.
+    SiteLanes* lanes = nullptr;
+    std::unique_lock<std::mutex> lanes_lock;
+    int used = 0;
     if (any_x || n > 1) {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
@@ -812,10 +1044,16 @@ dust_status estimate_host_sites(const dust_host_site* sites, int64_t n, dust_dty
                 return DUST_ERR_CUDA;
             lane->ev.push_back(e);
         }
+        if (n > 1) {
+            lanes = site_lanes(lanes_lock);
+            if (!lanes) return DUST_ERR_CUDA;
+            used = n < kSiteLanes ? static_cast<int>(n) : kSiteLanes;
+        }
         if (cudaEventRecord(lane->fork, s) != cudaSuccess ||
             cudaStreamWaitEvent(lane->copy, lane->fork, 0) != cudaSuccess ||
             cudaStreamWaitEvent(lane->ret, lane->fork, 0) != cudaSuccess)
             return DUST_ERR_CUDA;
+        if (lanes && !fork_lanes(lanes, used, s)) return DUST_ERR_CUDA;
         for (int64_t i = 0; i < n; ++i) {
             const dust_host_site& q = sites[i];
             if (i > 0 && (!small_copies(q, lane->copy) ||
@@ -833,34 +1071,37 @@ dust_status estimate_host_sites(const dust_host_site* sites, int64_t n, dust_dty
     dust_status result = DUST_OK;
     for (int64_t i = 0; i < n && result == DUST_OK; ++i) {
         const dust_host_site& q = sites[i];
+        cudaStream_t cs = lanes ? lanes->lane[i % kSiteLanes] : s;
         if (i > 0) {
             // the inputs came over the copy stream (or, with no lane, go now)
-            const bool ok = lane ? cudaStreamWaitEvent(s, lane->ev[3 * i], 0) == cudaSuccess
-                                 : small_copies(q, s);
-            if (!ok || !gw_in(i)) {
+            const bool ok = lane ? cudaStreamWaitEvent(cs, lane->ev[3 * i], 0) == cudaSuccess
+                                 : small_copies(q, cs);
+            if (!ok || !gw_in(i, cs)) {
                 result = DUST_ERR_CUDA;
                 break;
             }
         }
         result = estimate(q.X_dev, x_dtype, q.T, q.d_in, q.delta_dev, q.K, q.d_out, q.seq_dev,
                           q.n_seq, q.seed, kind, draw_begin, q.sigma, q.gamma, scale, flags,
-                          target[i], q.workspace, q.ws_bytes, stream,
-                          lane ? lane->ev[3 * i + 1] : nullptr);
+                          target[i], q.workspace, q.ws_bytes, cs,
+                          lane ? lane->ev[3 * i + 1] : nullptr, lanes && kSiteLanes > 1);
         const size_t gw_bytes = sizeof(float) * static_cast<size_t>(q.d_out * q.d_in);
         if (result != DUST_OK || !gw_bytes || direct[i]) continue;
         if (i < n - 1) {
             // copied back on the return stream while later sites compute
-            if (cudaEventRecord(lane->ev[3 * i + 2], s) != cudaSuccess ||
+            if (cudaEventRecord(lane->ev[3 * i + 2], cs) != cudaSuccess ||
                 cudaStreamWaitEvent(lane->ret, lane->ev[3 * i + 2], 0) != cudaSuccess ||
                 cudaMemcpyAsync(q.gW_host, q.gW_dev, gw_bytes, cudaMemcpyDeviceToHost,
                                 lane->ret) != cudaSuccess)
                 result = DUST_ERR_CUDA;
-        } else if (cudaMemcpyAsync(q.gW_host, q.gW_dev, gw_bytes, cudaMemcpyDeviceToHost, s) !=
+        } else if (cudaMemcpyAsync(q.gW_host, q.gW_dev, gw_bytes, cudaMemcpyDeviceToHost, cs) !=
                    cudaSuccess) {
             result = DUST_ERR_CUDA;
         }
     }
-    // However the sequence ended, `stream` waits for every copy of the call.
+    // However the sequence ended, `stream` waits for the compute lanes and
+    // for every copy of the call.
+    if (lanes && !join_lanes(lanes, used, s)) return DUST_ERR_CUDA;
     if (lane && n > 0) {
         if (cudaStreamWaitEvent(s, lane->ev[3 * n - 2], 0) != cudaSuccess ||
             cudaEventRecord(lane->ret_done, lane->ret) != cudaSuccess ||

@@ -19,6 +19,14 @@ unsigned int* status_word();
 // per (kernel, device), under a lock, for processes that use several GPUs.
 cudaError_t ensure_smem_limit(const void* kernel, int bytes);
 
+// Asks for the largest shared-memory carveout for `kernel` on the current
+// device (set once per (kernel, device)). The estimator's small-footprint
+// kernels (scan, weighting, slice reduction) then leave SMs configured so
+// that a contraction CTA (about 193 KB of shared memory) can become resident
+// beside them: under the default preference an SM running them keeps most of
+// its unified memory as L1, and the contraction waits for the SM to drain.
+cudaError_t ensure_shared_carveout(const void* kernel);
+
 // Kernel families timed by dust_profile_read.
 enum Stage {
     kStageScanLocal, kStageScanCarry, kStageScanFixup, kStageWeight, kStageGemmSimt,
@@ -95,6 +103,16 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// launch_pdl for the estimator's small-footprint kernels: with the largest
+// shared-memory carveout (ensure_shared_carveout).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_shared(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args&&... args) {
+    const cudaError_t e = ensure_shared_carveout(reinterpret_cast<const void*>(kernel));
+    if (e != cudaSuccess) return e;
+    return launch_pdl(kernel, grid, block, smem, s, static_cast<Args&&>(args)...);
+}
+
 // Token chunk of the credit scan (one CTA, 32 lanes x 8 tokens).
 constexpr int kScanChunk = 256;
 
@@ -156,12 +174,14 @@ cudaError_t launch_simt_gemm(const void* g, int g_bf16, const void* X, int x_bf1
 cudaError_t launch_reduce(const float* partials, int64_t S, int64_t n, float scale,
                           bool accumulate, float* gW, cudaStream_t s);
 
-// Tensor-core contraction (tcgen05, bf16 g and X, fp32 accumulate).
+// Tensor-core contraction (tcgen05, bf16 g and X, fp32 accumulate). `lean`
+// takes the build capped at 80 registers a thread, which fits on an SM
+// beside four weighting CTAs (for sites that run concurrently).
 bool tc_gemm_supported(const void* g, const void* X, int64_t d_in, int64_t d_out);
 size_t tc_gemm_workspace_bytes(int64_t T, int64_t d_in, int64_t d_out);
 cudaError_t launch_tc_gemm(const void* g, const void* X, int64_t T, int64_t d_in, int64_t d_out,
                            float scale, bool accumulate, float* gW, float* partials,
-                           cudaStream_t s);
+                           cudaStream_t s, bool lean = false);
 
 // Bytes of per-call synchronisation words (the scan's ticket) at the head of
 // a workspace; zeroed by one cudaMemsetAsync per call.

@@ -203,7 +203,7 @@ cudaError_t launch_reduce(const float* partials, int64_t S, int64_t n, float sca
     if (!vec4) {
         int64_t rg = (n + 255) / 256;
         if (rg > 152 * 16) rg = 152 * 16;
-        return launch_pdl(k_reduce, dim3(static_cast<unsigned>(rg)), dim3(256), 0, s, partials,
+        return launch_pdl_shared(k_reduce, dim3(static_cast<unsigned>(rg)), dim3(256), 0, s, partials,
                           S, n, scale, accumulate ? 1 : 0, gW);
     }
     // Outputs per thread and slices per batch: about 8 loads in flight per
@@ -215,7 +215,7 @@ cudaError_t launch_reduce(const float* partials, int64_t S, int64_t n, float sca
     auto go = [&](auto kernel, int U) {
         int64_t rg = (n4 + 256 * U - 1) / (256 * U);
         if (rg > 152 * 8) rg = 152 * 8;
-        return launch_pdl(kernel, dim3(static_cast<unsigned>(rg)), dim3(256), 0, s, p4, S, n4,
+        return launch_pdl_shared(kernel, dim3(static_cast<unsigned>(rg)), dim3(256), 0, s, p4, S, n4,
                           scale, acc, g4);
     };
     if (S <= 3) return go(k_reduce_v4<4, 2>, 4);

@@ -261,8 +261,15 @@ __device__ void cluster_reduce_pull(unsigned char* smem, uint32_t tmem, bool ok,
     cluster_sync_all();  // no CTA leaves while another still reads its tile
 }
 
-template <int MT>
-__global__ void __launch_bounds__(kThreads, 1)
+// LEAN: at most 80 registers a thread (the launch bound asks for four CTAs
+// per SM), for the multi-site lanes, where a contraction CTA shares its SM
+// with four weighting CTAs of a later site (4 x 12,288 + 192 x 80 registers
+// fit the SM's 65,536; the unbounded 109-register build needs two weighting
+// CTAs to leave first). Alone it runs a little slower (a few spilled
+// registers): measured on the 48-site sweep, one stream 55.91 -> 55.98 ms,
+// three lanes 54.5 -> 54.1 ms. Same instructions otherwise, same results.
+template <int MT, bool LEAN>
+__global__ void __launch_bounds__(kThreads, LEAN ? 4 : 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               int64_t d_in, int64_t d_out, int64_t T, int64_t slice, float* __restrict__ out,
               float scale, int mode, unsigned int* __restrict__ status, int stall) {
@@ -529,7 +536,7 @@ namespace {
 // SM counts leaves SMs unused and can push a few clusters into a second
 // wave; the fp32 partials then win (measured on the 48-site sweep: 6-CTA
 // clusters 5.1 ms of contraction against 4.3 ms with partials).
-template <int MT>
+template <int MT, bool LEAN>
 bool cluster_fits(int S, int64_t tiles) {
     constexpr int kMaxDev = 64;
     static int max_active[kMaxDev][kMaxClusterSlices + 1] = {};
@@ -549,9 +556,9 @@ bool cluster_fits(int S, int64_t tiles) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (ensure_smem_limit(reinterpret_cast<const void*>(k_gemm_tc<MT>),
+        if (ensure_smem_limit(reinterpret_cast<const void*>(k_gemm_tc<MT, LEAN>),
                               Cfg<MT>::kSmemBytes) != cudaSuccess ||
-            cudaOccupancyMaxActiveClusters(&n, k_gemm_tc<MT>, &cfg) != cudaSuccess)
+            cudaOccupancyMaxActiveClusters(&n, k_gemm_tc<MT, LEAN>, &cfg) != cudaSuccess)
             n = 0;
         (void)cudaGetLastError();
         max_active[dev][S] = n;
@@ -559,13 +566,13 @@ bool cluster_fits(int S, int64_t tiles) {
     return tiles <= max_active[dev][S];
 }
 
-template <int MT>
+template <int MT, bool LEAN>
 cudaError_t launch_mt(const CUtensorMap& ta, const CUtensorMap& tb, int64_t T, int64_t d_in,
                       int64_t d_out, float scale, bool accumulate, float* gW, float* partials,
                       cudaStream_t s) {
     using C = Cfg<MT>;
     const cudaError_t attr_err =
-        ensure_smem_limit(reinterpret_cast<const void*>(k_gemm_tc<MT>), C::kSmemBytes);
+        ensure_smem_limit(reinterpret_cast<const void*>(k_gemm_tc<MT, LEAN>), C::kSmemBytes);
     if (attr_err != cudaSuccess) return attr_err;
     unsigned int* st = status_word();
     if (!st) return cudaErrorUnknown;
@@ -578,7 +585,8 @@ cudaError_t launch_mt(const CUtensorMap& ta, const CUtensorMap& tb, int64_t T, i
     cudaError_t e;
     const int stall = take_stall_injection() ? 1 : 0;
     if (kClusterReduce && S_used >= 2 && S_used <= kMaxClusterSlices &&
-        cluster_fits<MT>(static_cast<int>(S_used), static_cast<int64_t>(grid.x) * grid.y)) {
+        cluster_fits<MT, LEAN>(static_cast<int>(S_used),
+                               static_cast<int64_t>(grid.x) * grid.y)) {
         // The slices of a tile reduce through distributed shared memory.
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = grid;
@@ -596,8 +604,8 @@ cudaError_t launch_mt(const CUtensorMap& ta, const CUtensorMap& tb, int64_t T, i
         cfg.numAttrs = 2;
         {
             ProfScope ps(kStageGemmTc, s);
-            e = cudaLaunchKernelEx(&cfg, k_gemm_tc<MT>, ta, tb, d_in, d_out, T, slice, gW, scale,
-                                   accumulate ? 4 : 3, st, stall);
+            e = cudaLaunchKernelEx(&cfg, k_gemm_tc<MT, LEAN>, ta, tb, d_in, d_out, T, slice, gW,
+                                   scale, accumulate ? 4 : 3, st, stall);
         }
         if (e == cudaSuccess) return e;
         (void)cudaGetLastError();  // clusters refused: fall back to partials + reduction
@@ -605,7 +613,7 @@ cudaError_t launch_mt(const CUtensorMap& ta, const CUtensorMap& tb, int64_t T, i
     const int mode = (S_used > 1) ? 0 : (accumulate ? 2 : 1);
     {
         ProfScope ps(kStageGemmTc, s);
-        e = launch_pdl(k_gemm_tc<MT>, grid, dim3(kThreads), C::kSmemBytes, s, ta, tb, d_in,
+        e = launch_pdl(k_gemm_tc<MT, LEAN>, grid, dim3(kThreads), C::kSmemBytes, s, ta, tb, d_in,
                        d_out, T, slice, S_used > 1 ? partials : gW, scale, mode, st, stall);
     }
     if (e != cudaSuccess || S_used == 1) return e;
@@ -616,13 +624,17 @@ cudaError_t launch_mt(const CUtensorMap& ta, const CUtensorMap& tb, int64_t T, i
 
 cudaError_t launch_tc_gemm(const void* g, const void* X, int64_t T, int64_t d_in, int64_t d_out,
                            float scale, bool accumulate, float* gW, float* partials,
-                           cudaStream_t s) {
+                           cudaStream_t s, bool lean) {
     CUtensorMap ta, tb;
     if (!make_tmap_bf16(&ta, g, T, d_out, kBK) || !make_tmap_bf16(&tb, X, T, d_in, kBK))
         return cudaErrorInvalidValue;
-    if (tile_mt(T, d_in, d_out) == 2)
-        return launch_mt<2>(ta, tb, T, d_in, d_out, scale, accumulate, gW, partials, s);
-    return launch_mt<1>(ta, tb, T, d_in, d_out, scale, accumulate, gW, partials, s);
+    const bool mt2 = tile_mt(T, d_in, d_out) == 2;
+    if (lean)
+        return mt2 ? launch_mt<2, true>(ta, tb, T, d_in, d_out, scale, accumulate, gW, partials, s)
+                   : launch_mt<1, true>(ta, tb, T, d_in, d_out, scale, accumulate, gW, partials,
+                                        s);
+    return mt2 ? launch_mt<2, false>(ta, tb, T, d_in, d_out, scale, accumulate, gW, partials, s)
+               : launch_mt<1, false>(ta, tb, T, d_in, d_out, scale, accumulate, gW, partials, s);
 }
 
 }  // namespace dust

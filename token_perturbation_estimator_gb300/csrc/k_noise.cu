@@ -206,6 +206,28 @@ cudaError_t ensure_smem_limit(const void* kernel, int bytes) {
     return cudaSuccess;
 }
 
+cudaError_t ensure_shared_carveout(const void* kernel) {
+    struct Entry {
+        const void* kernel;
+        int dev;
+    };
+    constexpr int kMaxEntries = 256;
+    static Entry done[kMaxEntries];
+    static int n_done = 0;
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < n_done; ++i)
+        if (done[i].kernel == kernel && done[i].dev == dev) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    if (n_done < kMaxEntries) done[n_done++] = Entry{kernel, dev};
+    return cudaSuccess;
+}
+
 cudaError_t launch_zero(float* p, int64_t n, cudaStream_t s) {
     if (n == 0) return cudaSuccess;
     ProfScope ps(kStageZero, s);
