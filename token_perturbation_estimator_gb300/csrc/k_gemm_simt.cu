@@ -203,8 +203,8 @@ cudaError_t launch_reduce(const float* partials, int64_t S, int64_t n, float sca
     if (!vec4) {
         int64_t rg = (n + 255) / 256;
         if (rg > 152 * 16) rg = 152 * 16;
-        return launch_pdl_shared(k_reduce, dim3(static_cast<unsigned>(rg)), dim3(256), 0, s, partials,
-                          S, n, scale, accumulate ? 1 : 0, gW);
+        return launch_pdl_shared(k_reduce, dim3(static_cast<unsigned>(rg)), dim3(256), 0, s,
+                                 partials, S, n, scale, accumulate ? 1 : 0, gW);
     }
     // Outputs per thread and slices per batch: about 8 loads in flight per
     // thread; one CTA of 256 threads per U x 256 outputs, at most 8 per SM.
@@ -215,8 +215,8 @@ cudaError_t launch_reduce(const float* partials, int64_t S, int64_t n, float sca
     auto go = [&](auto kernel, int U) {
         int64_t rg = (n4 + 256 * U - 1) / (256 * U);
         if (rg > 152 * 8) rg = 152 * 8;
-        return launch_pdl_shared(kernel, dim3(static_cast<unsigned>(rg)), dim3(256), 0, s, p4, S, n4,
-                          scale, acc, g4);
+        return launch_pdl_shared(kernel, dim3(static_cast<unsigned>(rg)), dim3(256), 0, s, p4,
+                                 S, n4, scale, acc, g4);
     };
     if (S <= 3) return go(k_reduce_v4<4, 2>, 4);
     if (S <= 5) return go(k_reduce_v4<2, 4>, 2);

@@ -343,9 +343,9 @@ cudaError_t launch_scan(const float* delta, int64_t K, int64_t T, const int32_t*
     cudaError_t e;
     {
     ProfScope ps(kStageScanLocal, s);
-    e = launch_pdl_shared(k_scan_local, dim3(static_cast<unsigned>(b.n_chunks)), dim3(256), 0, s, delta,
-                   K, T, seq_offsets, n_seq, gamma, center ? 1 : 0, b.r, b.P, b.A, b.B, b.carry,
-                   merged ? ticket : nullptr);
+    e = launch_pdl_shared(k_scan_local, dim3(static_cast<unsigned>(b.n_chunks)), dim3(256), 0, s,
+                          delta, K, T, seq_offsets, n_seq, gamma, center ? 1 : 0, b.r, b.P, b.A,
+                          b.B, b.carry, merged ? ticket : nullptr);
     }
     if (e != cudaSuccess || merged) return e;
     const size_t smem = sizeof(float) * static_cast<size_t>(b.n_chunks * (K + 2));
@@ -354,8 +354,8 @@ cudaError_t launch_scan(const float* delta, int64_t K, int64_t T, const int32_t*
         ensure_smem_limit(reinterpret_cast<const void*>(k_carry), static_cast<int>(kCarrySmem));
     if (attr != cudaSuccess) return attr;
     ProfScope ps(kStageScanCarry, s);
-    return launch_pdl_shared(k_carry, dim3(1), dim3(256), staged ? smem : 0, s, b.A, b.B, K, b.n_chunks,
-                      b.carry, staged);
+    return launch_pdl_shared(k_carry, dim3(1), dim3(256), staged ? smem : 0, s, b.A, b.B, K,
+                             b.n_chunks, b.carry, staged);
 }
 
 cudaError_t launch_scan_fixup(const ScanBuffers& b, int64_t K, int64_t T, cudaStream_t s) {
@@ -364,8 +364,8 @@ cudaError_t launch_scan_fixup(const ScanBuffers& b, int64_t K, int64_t T, cudaSt
     int64_t grid = (n + 255) / 256;
     if (grid > 152 * 32) grid = 152 * 32;
     ProfScope ps(kStageScanFixup, s);
-    return launch_pdl_shared(k_fixup, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, b.r, b.P,
-                      b.carry, K, T);
+    return launch_pdl_shared(k_fixup, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, b.r,
+                             b.P, b.carry, K, T);
 }
 
 }  // namespace dust

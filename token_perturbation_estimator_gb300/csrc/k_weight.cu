@@ -346,8 +346,8 @@ cudaError_t launch_kind(const float* r, const ScanBuffers& b, int64_t K, int64_t
     const bool vec_ok = (d_out % 8 == 0) && (reinterpret_cast<uintptr_t>(g) % 16 == 0);
     ProfScope ps(kStageWeight, s);
     auto go = [&](auto kernel, auto* out) {
-        return launch_pdl_shared(kernel, grid, dim3(256), 0, s, r, b.P, b.carry, K, T, d_out, skey,
-                          draw_begin, coef, out, vec_ok, center, keys);
+        return launch_pdl_shared(kernel, grid, dim3(256), 0, s, r, b.P, b.carry, K, T, d_out,
+                                 skey, draw_begin, coef, out, vec_ok, center, keys);
     };
     auto* gb = static_cast<__nv_bfloat16*>(g);
     auto* gf = static_cast<float*>(g);
