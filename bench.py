@@ -869,6 +869,7 @@ def run_gb300(args):
                "noise": {0: "rademacher", 1: "gaussian", 3: "rademacher_packed"}[w0.kind],
                "x_dtype": w0.x_dtype, "paths": sorted({b["path"] for b in bundles}),
                "parallelism": "replicas" if world > 1 else "single",
+               "entry_point": "dust_estimate_gW_sites" if multi else "dust_estimate_gW",
                "l2": "flushed (256 MB write) between timed steps"}
         if len(sites) == 1:
             cfg.update({"d_in": w0.d_in, "d_out": w0.d_out, "T": w0.T, "n_seq": w0.n_seq,
