@@ -457,14 +457,18 @@ dust_status estimate_check(const void* X, dust_dtype x_dtype, int64_t T, int64_t
 // The whole estimator on `stream`. When x_ready is given, X is still being
 // copied on another stream: the stream waits for that event just before the
 // first kernel that reads X (the contraction), so the scan and the weighting
-// overlap the copy. `lean`: the contraction build that shares an SM with
-// weighting CTAs (for sites running concurrently on the compute lanes).
+// overlap the copy. `fit`: the contraction build (launch_tc_gemm), by what
+// shares its SMs (sites running concurrently on the compute lanes). With `cs`
+// given (a lane's contraction stream), the contraction kernel runs there
+// after the weighting (event `cs_in`), and `stream` waits for it (event
+// `cs_out`) before the slice reduction and anything later.
 dust_status estimate(const void* X, dust_dtype x_dtype, int64_t T, int64_t d_in,
                      const float* delta, int64_t K, int64_t d_out, const int32_t* seq_offsets,
                      int64_t n_seq, uint64_t seed, dust_noise_kind kind, int64_t draw_begin,
                      float sigma, float gamma, float scale, uint32_t flags, float* gW,
                      void* workspace, size_t ws_bytes, void* stream, cudaEvent_t x_ready,
-                     bool lean = false) {
+                     int fit = 0, cudaStream_t cs = nullptr, cudaEvent_t cs_in = nullptr,
+                     cudaEvent_t cs_out = nullptr) {
     const dust_status st =
         estimate_check(X, x_dtype, T, d_in, delta, K, d_out, seq_offsets, n_seq, kind,
                        draw_begin, sigma, gamma, scale, flags, gW, workspace, ws_bytes);
@@ -504,8 +508,14 @@ dust_status estimate(const void* X, dust_dtype x_dtype, int64_t T, int64_t d_in,
                       g, L.g_bf16, s, direct ? delta : nullptr, center);
     if (e != cudaSuccess) return DUST_ERR_CUDA;
     if (x_ready && cudaStreamWaitEvent(s, x_ready, 0) != cudaSuccess) return DUST_ERR_CUDA;
+    if (cs && L.path == DUST_PATH_UNFUSED_TC && tc_gemm_supported(g, X, d_in, d_out)) {
+        if (cudaEventRecord(cs_in, s) != cudaSuccess || cudaStreamWaitEvent(cs, cs_in, 0) != cudaSuccess)
+            return DUST_ERR_CUDA;
+        return cuda_status(
+            launch_tc_gemm(g, X, T, d_in, d_out, scale, acc, gW, part, cs, fit, s, cs_out));
+    }
     if (L.path == DUST_PATH_UNFUSED_TC && tc_gemm_supported(g, X, d_in, d_out))
-        e = launch_tc_gemm(g, X, T, d_in, d_out, scale, acc, gW, part, s, lean);
+        e = launch_tc_gemm(g, X, T, d_in, d_out, scale, acc, gW, part, s, fit);
     else
         e = launch_simt_gemm(g, L.g_bf16, X, x_dtype == DUST_BF16, T, d_in, d_out, scale, acc,
                              gW, part, s);
@@ -530,27 +540,40 @@ constexpr int64_t kMaxSites = 4096;
 CopyLane g_lanes[kMaxDevices];
 
 // Compute lanes of the multi-site entry points: streams of one device on
-// which whole sites run, site i on lane i mod kSiteLanes, so that one site's
-// contraction overlaps later sites' weighting. Created on first use and kept
-// for the life of the process; the lock covers a call's whole enqueue
-// sequence, so the fork and join events are re-recorded only after every
-// wait on them has been enqueued. Measured on the 48-site sweep (a GB300):
-// 55.9 ms per pass on one stream, 55.3 on two lanes, 55.0 on three (54.5
-// with the shared-memory carveout that lets a contraction CTA sit beside
-// the weighting CTAs).
+// which whole sites run, site i on lane i mod kSiteLanes, each lane with a
+// contraction stream of the device's highest priority on which its sites'
+// contraction kernels run. The hardware dispatches the CTAs of concurrent
+// grids of equal priority in launch order, so a contraction launched behind
+// another site's weighting would wait for that whole grid to be placed; at
+// the higher priority its CTAs take the room the weighting CTAs leave (the
+// 32-register build: one beside five weighting CTAs) and run beside them.
+// The slice reductions stay on the lanes: at high priority their many
+// short CTAs would take the weighting's places instead. Created on first use
+// and kept for the life of the process; the lock covers a call's whole
+// enqueue sequence, so the events are re-recorded only after every wait on
+// them has been enqueued. Measured on the 48-site sweep (a GB300): 55.9 ms
+// per pass on one stream; 54.2 on three lanes without the contraction
+// streams; 53.4 with them.
 #ifndef DUST_SITE_LANES
 #define DUST_SITE_LANES 3
 #endif
 constexpr int kSiteLanes = DUST_SITE_LANES;
 static_assert(kSiteLanes >= 1, "at least one lane");
+// The contraction build the lanes use (launch_tc_gemm's `fit`).
+#ifndef DUST_SITE_FIT
+#define DUST_SITE_FIT 2
+#endif
+constexpr int kSiteFit = DUST_SITE_FIT;
 
 struct SiteLanes {
     std::mutex mu;
     bool ready = false;
     cudaError_t err = cudaSuccess;
     cudaStream_t lane[kSiteLanes] = {};
+    cudaStream_t gemm[kSiteLanes] = {};  // the lanes' contraction streams
     cudaEvent_t fork = nullptr;
-    cudaEvent_t join[kSiteLanes] = {};
+    cudaEvent_t join[kSiteLanes] = {}, gemm_join[kSiteLanes] = {};
+    cudaEvent_t gemm_in[kSiteLanes] = {}, gemm_out[kSiteLanes] = {};
 };
 SiteLanes g_site_lanes[kMaxDevices];
 
@@ -562,10 +585,16 @@ SiteLanes* site_lanes(std::unique_lock<std::mutex>& lock) {
     SiteLanes* L = &g_site_lanes[dev];
     lock = std::unique_lock<std::mutex>(L->mu);
     if (!L->ready) {
+        int least = 0, greatest = 0;
+        L->err = cudaDeviceGetStreamPriorityRange(&least, &greatest);
         for (int l = 0; l < kSiteLanes && L->err == cudaSuccess; ++l) {
             L->err = cudaStreamCreateWithFlags(&L->lane[l], cudaStreamNonBlocking);
             if (L->err == cudaSuccess)
-                L->err = cudaEventCreateWithFlags(&L->join[l], cudaEventDisableTiming);
+                L->err = cudaStreamCreateWithPriority(&L->gemm[l], cudaStreamNonBlocking, greatest);
+            cudaEvent_t* evs[4] = {&L->join[l], &L->gemm_join[l], &L->gemm_in[l], &L->gemm_out[l]};
+            for (cudaEvent_t* e : evs)
+                if (L->err == cudaSuccess)
+                    L->err = cudaEventCreateWithFlags(e, cudaEventDisableTiming);
         }
         if (L->err == cudaSuccess)
             L->err = cudaEventCreateWithFlags(&L->fork, cudaEventDisableTiming);
@@ -574,19 +603,25 @@ SiteLanes* site_lanes(std::unique_lock<std::mutex>& lock) {
     return L->err == cudaSuccess ? L : nullptr;
 }
 
-// Lanes 0 .. used-1 start after the work enqueued on `s` so far.
+// Lanes 0 .. used-1 and their contraction streams start after the work
+// enqueued on `s` so far.
 bool fork_lanes(SiteLanes* L, int used, cudaStream_t s) {
     if (cudaEventRecord(L->fork, s) != cudaSuccess) return false;
     for (int l = 0; l < used; ++l)
-        if (cudaStreamWaitEvent(L->lane[l], L->fork, 0) != cudaSuccess) return false;
+        if (cudaStreamWaitEvent(L->lane[l], L->fork, 0) != cudaSuccess ||
+            cudaStreamWaitEvent(L->gemm[l], L->fork, 0) != cudaSuccess)
+            return false;
     return true;
 }
 
-// `s` waits for everything enqueued on lanes 0 .. used-1.
+// `s` waits for everything enqueued on lanes 0 .. used-1 and their
+// contraction streams.
 bool join_lanes(SiteLanes* L, int used, cudaStream_t s) {
     for (int l = 0; l < used; ++l)
         if (cudaEventRecord(L->join[l], L->lane[l]) != cudaSuccess ||
-            cudaStreamWaitEvent(s, L->join[l], 0) != cudaSuccess)
+            cudaStreamWaitEvent(s, L->join[l], 0) != cudaSuccess ||
+            cudaEventRecord(L->gemm_join[l], L->gemm[l]) != cudaSuccess ||
+            cudaStreamWaitEvent(s, L->gemm_join[l], 0) != cudaSuccess)
             return false;
     return true;
 }
@@ -721,21 +756,27 @@ dust_status estimate_sites(const dust_site* sites, int64_t n, dust_dtype x_dtype
         }
         if (!sites_disjoint(rs)) return DUST_ERR_INVALID_ARG;
     }
-    auto one = [&](const dust_site& q, cudaStream_t cs, bool lean) {
+    if (n == 0) return DUST_OK;
+    if (n == 1) {
+        const dust_site& q = sites[0];
         return estimate(q.X, x_dtype, q.T, q.d_in, q.delta, q.K, q.d_out, q.seq_offsets,
                         q.n_seq, q.seed, kind, draw_begin, q.sigma, q.gamma, scale, flags, q.gW,
-                        q.workspace, q.ws_bytes, cs, nullptr, lean);
-    };
-    if (n == 0) return DUST_OK;
-    if (n == 1) return one(sites[0], s, false);
+                        q.workspace, q.ws_bytes, s, nullptr);
+    }
     std::unique_lock<std::mutex> lock;
     SiteLanes* L = site_lanes(lock);
     if (!L) return DUST_ERR_CUDA;
     const int used = n < kSiteLanes ? static_cast<int>(n) : kSiteLanes;
     if (!fork_lanes(L, used, s)) return DUST_ERR_CUDA;
     dust_status result = DUST_OK;
-    for (int64_t i = 0; i < n && result == DUST_OK; ++i)
-        result = one(sites[i], L->lane[i % kSiteLanes], kSiteLanes > 1);
+    for (int64_t i = 0; i < n && result == DUST_OK; ++i) {
+        const dust_site& q = sites[i];
+        const int l = static_cast<int>(i % kSiteLanes);
+        result = estimate(q.X, x_dtype, q.T, q.d_in, q.delta, q.K, q.d_out, q.seq_offsets,
+                          q.n_seq, q.seed, kind, draw_begin, q.sigma, q.gamma, scale, flags,
+                          q.gW, q.workspace, q.ws_bytes, L->lane[l], nullptr, kSiteFit,
+                          L->gemm[l], L->gemm_in[l], L->gemm_out[l]);
+    }
     // However the sequence ended, `s` waits for what the lanes were given.
     if (!join_lanes(L, used, s)) return DUST_ERR_CUDA;
     return result;
@@ -1081,10 +1122,13 @@ dust_status estimate_host_sites(const dust_host_site* sites, int64_t n, dust_dty
                 break;
             }
         }
+        const int l = static_cast<int>(i % kSiteLanes);
         result = estimate(q.X_dev, x_dtype, q.T, q.d_in, q.delta_dev, q.K, q.d_out, q.seq_dev,
                           q.n_seq, q.seed, kind, draw_begin, q.sigma, q.gamma, scale, flags,
                           target[i], q.workspace, q.ws_bytes, cs,
-                          lane ? lane->ev[3 * i + 1] : nullptr, lanes && kSiteLanes > 1);
+                          lane ? lane->ev[3 * i + 1] : nullptr, lanes ? kSiteFit : 0,
+                          lanes ? lanes->gemm[l] : nullptr, lanes ? lanes->gemm_in[l] : nullptr,
+                          lanes ? lanes->gemm_out[l] : nullptr);
         const size_t gw_bytes = sizeof(float) * static_cast<size_t>(q.d_out * q.d_in);
         if (result != DUST_OK || !gw_bytes || direct[i]) continue;
         if (i < n - 1) {

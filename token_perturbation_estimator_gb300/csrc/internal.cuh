@@ -174,14 +174,18 @@ cudaError_t launch_simt_gemm(const void* g, int g_bf16, const void* X, int x_bf1
 cudaError_t launch_reduce(const float* partials, int64_t S, int64_t n, float scale,
                           bool accumulate, float* gW, cudaStream_t s);
 
-// Tensor-core contraction (tcgen05, bf16 g and X, fp32 accumulate). `lean`
-// takes the build capped at 80 registers a thread, which fits on an SM
-// beside four weighting CTAs (for sites that run concurrently).
+// Tensor-core contraction (tcgen05, bf16 g and X, fp32 accumulate). `fit`
+// picks the build by what shares its SMs: 0 alone (192 threads), 1 beside
+// four weighting CTAs (192 threads, at most 80 registers), 2 beside five
+// (128 threads, at most 32 registers); for sites that run concurrently.
+// With `back` given, the kernel runs on `s` (a stream of high priority) and
+// `back` then waits for it (through `back_ev`) and runs the slice reduction.
 bool tc_gemm_supported(const void* g, const void* X, int64_t d_in, int64_t d_out);
 size_t tc_gemm_workspace_bytes(int64_t T, int64_t d_in, int64_t d_out);
 cudaError_t launch_tc_gemm(const void* g, const void* X, int64_t T, int64_t d_in, int64_t d_out,
                            float scale, bool accumulate, float* gW, float* partials,
-                           cudaStream_t s, bool lean = false);
+                           cudaStream_t s, int fit = 0, cudaStream_t back = nullptr,
+                           cudaEvent_t back_ev = nullptr);
 
 // Bytes of per-call synchronisation words (the scan's ticket) at the head of
 // a workspace; zeroed by one cudaMemsetAsync per call.

@@ -54,7 +54,15 @@ constexpr bool kClusterReduce = DUST_GEMM_CLUSTER_REDUCE != 0;
 constexpr bool kPull = DUST_GEMM_PULL != 0;
 constexpr int kBN = DUST_GEMM_BN, kBK = DUST_GEMM_BK;
 constexpr int kBoxBytes = 64 * kBK * 2;                 // one 64-wide bf16 box of kBK rows
-constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
+// Builds of the kernel, by what else shares its SM ("fit"):
+//   0: 192 threads (warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue), no
+//      register bound: the kernel alone on the SM;
+//   1: the same at most 80 registers a thread, beside four weighting CTAs;
+//   2: 128 threads at most 32 registers (warp 0 TMA, warp 1 MMA + TMEM, then
+//      all four warps the epilogue), beside five weighting CTAs, which hold
+//      61,440 of the SM's 65,536 registers: the 4,096 left are this CTA's.
+constexpr int threads_of(int fit) { return fit == 2 ? 128 : 192; }
+constexpr int min_ctas_of(int fit) { return fit == 0 ? 1 : fit == 1 ? 4 : 16; }
 constexpr uint32_t kIdesc = tc::idesc_bf16_mn(128, kBN);
 static_assert(kBK % 16 == 0 && kBN % 64 == 0, "tile shape");
 
@@ -191,6 +199,26 @@ __device__ __forceinline__ void st_shared_v4f(uint32_t addr, float a, float b, f
                  : "memory");
 }
 
+// The warp's TMEM lane quarter (32 accumulator rows) at taddr, columns
+// [0, kBN), into shared memory at dst (this lane's row): 32 columns per load,
+// or 8 in the 32-register build.
+template <int FIT>
+__device__ __forceinline__ void stage_rows(uint32_t taddr, uint32_t dst) {
+    constexpr int W = FIT == 2 ? 8 : 32;
+#pragma unroll 1
+    for (int c = 0; c < kBN / W; ++c) {
+        float v[W];
+        if constexpr (W == 32)
+            tc::tmem_ld_32x32(taddr + c * W, v);
+        else
+            tc::tmem_ld_32xN<W>(taddr + c * W, v);
+#pragma unroll
+        for (int u = 0; u < W / 4; ++u)
+            st_shared_v4f(dst + 4u * (c * W + 4 * u), v[4 * u], v[4 * u + 1], v[4 * u + 2],
+                          v[4 * u + 3]);
+    }
+}
+
 static_assert(128 * kRowPad * 4 <= kReduceBytes &&
                   128 * kRowPad * 4 <= Cfg<2>::kStages * Cfg<2>::kStageBytes,
               "a 128-row accumulator fits in the stage buffers");
@@ -202,6 +230,9 @@ static_assert(128 * kRowPad * 4 <= kReduceBytes &&
 // until all its readers are done.
 // One 128-row accumulator at a time: with MT = 2 the kernel calls it for the
 // TMEM columns of each accumulator (tmem + 256 mt) and its rows (m0 + 128 mt).
+// With FIT = 2 every warp stages its quarter, 8 columns at a time, and the
+// slices' loads go one by one (the same sums in the same order).
+template <int FIT>
 __device__ void cluster_reduce_pull(unsigned char* smem, uint32_t tmem, bool ok, int64_t m0,
                                     int64_t n0, int64_t d_in, int64_t d_out,
                                     float* __restrict__ gW, float scale, bool accumulate) {
@@ -213,18 +244,10 @@ __device__ void cluster_reduce_pull(unsigned char* smem, uint32_t tmem, bool ok,
     const int R_me = (128 - r0 < R) ? 128 - r0 : R;
     float* tile = reinterpret_cast<float*>(smem);  // [128][kRowPad]
     cluster_sync_all();  // every CTA's main loop is over: its stage buffers are free
-    if (warp >= 2 && ok) {
+    if ((FIT == 2 || warp >= 2) && ok) {
         const int q = warp & 3;
         const uint32_t dst = tc::smem_u32(tile + (32 * q + lane) * kRowPad);
-#pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
-            float v[32];
-            tc::tmem_ld_32x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + c * 32, v);
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                st_shared_v4f(dst + 4u * (c * 32 + 4 * u), v[4 * u], v[4 * u + 1], v[4 * u + 2],
-                              v[4 * u + 3]);
-        }
+        stage_rows<FIT>(tmem + (static_cast<uint32_t>(32 * q) << 16), dst);
     }
     cluster_sync_all();  // every tile is in place
     const uint32_t base = tc::smem_u32(tile);
@@ -235,19 +258,32 @@ __device__ void cluster_reduce_pull(unsigned char* smem, uint32_t tmem, bool ok,
         const int64_t col = n0 + 4 * c4;
         if (row >= d_out || col >= d_in) continue;
         const uint32_t a = base + 4u * static_cast<uint32_t>((r0 + rr) * kRowPad + 4 * c4);
-        // All S loads issued before the sums, which then run in slice order.
-        float4 w[kMaxClusterSlices];
+        float4 v;
+        if constexpr (FIT == 2) {
+            v = ld_cluster_v4(map_to_rank(a, 0u));
+#pragma unroll 1
+            for (int z = 1; z < S; ++z) {
+                const float4 w = ld_cluster_v4(map_to_rank(a, static_cast<uint32_t>(z)));
+                v.x += w.x;
+                v.y += w.y;
+                v.z += w.z;
+                v.w += w.w;
+            }
+        } else {
+            // All S loads issued before the sums, which then run in slice order.
+            float4 w[kMaxClusterSlices];
 #pragma unroll
-        for (int z = 0; z < kMaxClusterSlices; ++z)
-            if (z < S) w[z] = ld_cluster_v4(map_to_rank(a, static_cast<uint32_t>(z)));
-        float4 v = w[0];
+            for (int z = 0; z < kMaxClusterSlices; ++z)
+                if (z < S) w[z] = ld_cluster_v4(map_to_rank(a, static_cast<uint32_t>(z)));
+            v = w[0];
 #pragma unroll
-        for (int z = 1; z < kMaxClusterSlices; ++z) {
-            if (z < S) {
-                v.x += w[z].x;
-                v.y += w[z].y;
-                v.z += w[z].z;
-                v.w += w[z].w;
+            for (int z = 1; z < kMaxClusterSlices; ++z) {
+                if (z < S) {
+                    v.x += w[z].x;
+                    v.y += w[z].y;
+                    v.z += w[z].z;
+                    v.w += w[z].w;
+                }
             }
         }
         float4 o = make_float4(scale * v.x, scale * v.y, scale * v.z, scale * v.w);
@@ -261,15 +297,11 @@ __device__ void cluster_reduce_pull(unsigned char* smem, uint32_t tmem, bool ok,
     cluster_sync_all();  // no CTA leaves while another still reads its tile
 }
 
-// LEAN: at most 80 registers a thread (the launch bound asks for four CTAs
-// per SM), for the multi-site lanes, where a contraction CTA shares its SM
-// with four weighting CTAs of a later site (4 x 12,288 + 192 x 80 registers
-// fit the SM's 65,536; the unbounded 109-register build needs two weighting
-// CTAs to leave first). Alone it runs a little slower (a few spilled
-// registers): measured on the 48-site sweep, one stream 55.91 -> 55.98 ms,
-// three lanes 54.5 -> 54.1 ms. Same instructions otherwise, same results.
-template <int MT, bool LEAN>
-__global__ void __launch_bounds__(kThreads, LEAN ? 4 : 1)
+// FIT (see threads_of): the builds that share an SM serve the multi-site
+// lanes, where a contraction CTA runs beside weighting CTAs of later sites.
+// Every build issues the same MMAs and sums in the same order: same results.
+template <int MT, int FIT>
+__global__ void __launch_bounds__(threads_of(FIT), min_ctas_of(FIT))
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               int64_t d_in, int64_t d_out, int64_t T, int64_t slice, float* __restrict__ out,
               float scale, int mode, unsigned int* __restrict__ status, int stall) {
@@ -367,7 +399,9 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 4 : 1)
         }
         ctl->consumed = it;
         tc::mma_commit(&ctl->done);
-    } else if (warp >= 2) {
+    }
+    if (FIT == 2) __syncwarp();  // warps 0 and 1 regroup after their roles
+    if (FIT == 2 || warp >= 2) {
         const bool ok = tc::mbar_wait(&ctl->done, 0);
         tc::tc_fence_after();
         if (!ok) *abort_flag = 1;
@@ -382,16 +416,7 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 4 : 1)
             const uint32_t rows_s = tc::smem_u32(rows) + 4u * static_cast<uint32_t>(lane * kRowPad);
 #pragma unroll 1
             for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll 1
-                for (int c = 0; c < kBN / 32; ++c) {
-                    float v[32];
-                    tc::tmem_ld_32x32(
-                        tmem + (static_cast<uint32_t>(32 * q) << 16) + mt * kBN + c * 32, v);
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        st_shared_v4f(rows_s + 4u * (c * 32 + 4 * u), v[4 * u], v[4 * u + 1],
-                                      v[4 * u + 2], v[4 * u + 3]);
-                }
+                stage_rows<FIT>(tmem + (static_cast<uint32_t>(32 * q) << 16) + mt * kBN, rows_s);
                 __syncwarp();
 #pragma unroll 1
                 for (int rr = 0; rr < 32; ++rr) {
@@ -431,10 +456,10 @@ __global__ void __launch_bounds__(kThreads, LEAN ? 4 : 1)
     }
     if (mode >= 3) {
         __syncthreads();
-        if (kPull || MT > 1) {
+        if (kPull || MT > 1 || FIT == 2) {
 #pragma unroll 1
             for (int mt = 0; mt < MT; ++mt)
-                cluster_reduce_pull(smem, tmem + mt * kBN, !*abort_flag && n_k > 0, m0 + 128 * mt,
+                cluster_reduce_pull<FIT>(smem, tmem + mt * kBN, !*abort_flag && n_k > 0, m0 + 128 * mt,
                                     n0, d_in, d_out, out, scale, mode == 4);
         } else {
             cluster_reduce(smem, tmem, !*abort_flag && n_k > 0, m0, n0, d_in, d_out, out, scale,
@@ -536,7 +561,7 @@ namespace {
 // SM counts leaves SMs unused and can push a few clusters into a second
 // wave; the fp32 partials then win (measured on the 48-site sweep: 6-CTA
 // clusters 5.1 ms of contraction against 4.3 ms with partials).
-template <int MT, bool LEAN>
+template <int MT, int FIT>
 bool cluster_fits(int S, int64_t tiles) {
     constexpr int kMaxDev = 64;
     static int max_active[kMaxDev][kMaxClusterSlices + 1] = {};
@@ -546,7 +571,7 @@ bool cluster_fits(int S, int64_t tiles) {
     std::call_once(once[dev][S], [S, dev] {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(1, 1, static_cast<unsigned>(S));
-        cfg.blockDim = dim3(kThreads);
+        cfg.blockDim = dim3(threads_of(FIT));
         cfg.dynamicSmemBytes = Cfg<MT>::kSmemBytes;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -556,9 +581,9 @@ bool cluster_fits(int S, int64_t tiles) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (ensure_smem_limit(reinterpret_cast<const void*>(k_gemm_tc<MT, LEAN>),
+        if (ensure_smem_limit(reinterpret_cast<const void*>(k_gemm_tc<MT, FIT>),
                               Cfg<MT>::kSmemBytes) != cudaSuccess ||
-            cudaOccupancyMaxActiveClusters(&n, k_gemm_tc<MT, LEAN>, &cfg) != cudaSuccess)
+            cudaOccupancyMaxActiveClusters(&n, k_gemm_tc<MT, FIT>, &cfg) != cudaSuccess)
             n = 0;
         (void)cudaGetLastError();
         max_active[dev][S] = n;
@@ -566,13 +591,22 @@ bool cluster_fits(int S, int64_t tiles) {
     return tiles <= max_active[dev][S];
 }
 
-template <int MT, bool LEAN>
+// With `back` given, the contraction kernel ran on a stream of its own: `back`
+// (the caller's stream) waits for it, and the slice reduction, if any, runs on
+// `back` (at that stream's priority, not the contraction's).
+cudaError_t hand_back(cudaStream_t s, cudaStream_t back, cudaEvent_t back_ev) {
+    if (!back) return cudaSuccess;
+    cudaError_t e = cudaEventRecord(back_ev, s);
+    return e != cudaSuccess ? e : cudaStreamWaitEvent(back, back_ev, 0);
+}
+
+template <int MT, int FIT>
 cudaError_t launch_mt(const CUtensorMap& ta, const CUtensorMap& tb, int64_t T, int64_t d_in,
                       int64_t d_out, float scale, bool accumulate, float* gW, float* partials,
-                      cudaStream_t s) {
+                      cudaStream_t s, cudaStream_t back, cudaEvent_t back_ev) {
     using C = Cfg<MT>;
     const cudaError_t attr_err =
-        ensure_smem_limit(reinterpret_cast<const void*>(k_gemm_tc<MT, LEAN>), C::kSmemBytes);
+        ensure_smem_limit(reinterpret_cast<const void*>(k_gemm_tc<MT, FIT>), C::kSmemBytes);
     if (attr_err != cudaSuccess) return attr_err;
     unsigned int* st = status_word();
     if (!st) return cudaErrorUnknown;
@@ -585,12 +619,12 @@ cudaError_t launch_mt(const CUtensorMap& ta, const CUtensorMap& tb, int64_t T, i
     cudaError_t e;
     const int stall = take_stall_injection() ? 1 : 0;
     if (kClusterReduce && S_used >= 2 && S_used <= kMaxClusterSlices &&
-        cluster_fits<MT, LEAN>(static_cast<int>(S_used),
+        cluster_fits<MT, FIT>(static_cast<int>(S_used),
                                static_cast<int64_t>(grid.x) * grid.y)) {
         // The slices of a tile reduce through distributed shared memory.
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = grid;
-        cfg.blockDim = dim3(kThreads);
+        cfg.blockDim = dim3(threads_of(FIT));
         cfg.dynamicSmemBytes = C::kSmemBytes;
         cfg.stream = s;
         cudaLaunchAttribute attr[2];
@@ -604,37 +638,41 @@ cudaError_t launch_mt(const CUtensorMap& ta, const CUtensorMap& tb, int64_t T, i
         cfg.numAttrs = 2;
         {
             ProfScope ps(kStageGemmTc, s);
-            e = cudaLaunchKernelEx(&cfg, k_gemm_tc<MT, LEAN>, ta, tb, d_in, d_out, T, slice, gW,
+            e = cudaLaunchKernelEx(&cfg, k_gemm_tc<MT, FIT>, ta, tb, d_in, d_out, T, slice, gW,
                                    scale, accumulate ? 4 : 3, st, stall);
         }
-        if (e == cudaSuccess) return e;
+        if (e == cudaSuccess) return hand_back(s, back, back_ev);
         (void)cudaGetLastError();  // clusters refused: fall back to partials + reduction
     }
     const int mode = (S_used > 1) ? 0 : (accumulate ? 2 : 1);
     {
         ProfScope ps(kStageGemmTc, s);
-        e = launch_pdl(k_gemm_tc<MT, LEAN>, grid, dim3(kThreads), C::kSmemBytes, s, ta, tb, d_in,
+        e = launch_pdl(k_gemm_tc<MT, FIT>, grid, dim3(threads_of(FIT)), C::kSmemBytes, s, ta, tb,
+                       d_in,
                        d_out, T, slice, S_used > 1 ? partials : gW, scale, mode, st, stall);
     }
+    if (e != cudaSuccess) return e;
+    e = hand_back(s, back, back_ev);
     if (e != cudaSuccess || S_used == 1) return e;
-    return launch_reduce(partials, S_used, d_out * d_in, scale, accumulate, gW, s);
+    return launch_reduce(partials, S_used, d_out * d_in, scale, accumulate, gW, back ? back : s);
 }
 
 }  // namespace
 
 cudaError_t launch_tc_gemm(const void* g, const void* X, int64_t T, int64_t d_in, int64_t d_out,
                            float scale, bool accumulate, float* gW, float* partials,
-                           cudaStream_t s, bool lean) {
+                           cudaStream_t s, int fit, cudaStream_t back, cudaEvent_t back_ev) {
     CUtensorMap ta, tb;
     if (!make_tmap_bf16(&ta, g, T, d_out, kBK) || !make_tmap_bf16(&tb, X, T, d_in, kBK))
         return cudaErrorInvalidValue;
     const bool mt2 = tile_mt(T, d_in, d_out) == 2;
-    if (lean)
-        return mt2 ? launch_mt<2, true>(ta, tb, T, d_in, d_out, scale, accumulate, gW, partials, s)
-                   : launch_mt<1, true>(ta, tb, T, d_in, d_out, scale, accumulate, gW, partials,
-                                        s);
-    return mt2 ? launch_mt<2, false>(ta, tb, T, d_in, d_out, scale, accumulate, gW, partials, s)
-               : launch_mt<1, false>(ta, tb, T, d_in, d_out, scale, accumulate, gW, partials, s);
+    auto go = [&](auto k1, auto k2) {
+        return mt2 ? k2(ta, tb, T, d_in, d_out, scale, accumulate, gW, partials, s, back, back_ev)
+                   : k1(ta, tb, T, d_in, d_out, scale, accumulate, gW, partials, s, back, back_ev);
+    };
+    if (fit == 2) return go(launch_mt<1, 2>, launch_mt<2, 2>);
+    if (fit == 1) return go(launch_mt<1, 1>, launch_mt<2, 1>);
+    return go(launch_mt<1, 0>, launch_mt<2, 0>);
 }
 
 }  // namespace dust
