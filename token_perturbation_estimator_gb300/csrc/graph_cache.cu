@@ -69,7 +69,8 @@ Entry* insert(Cache& c, const void* key, size_t len) {
 }  // namespace
 
 dust_status graph_call(const void* key, size_t key_len, cudaStream_t stream,
-                       dust_status (*enqueue)(const void* ctx, cudaStream_t s), const void* ctx) {
+                       dust_status (*enqueue)(const void* ctx, cudaStream_t s), const void* ctx,
+                       bool node_priority) {
     if (!DUST_GRAPHS || profiling_on() || stall_injection_pending()) return enqueue(ctx, stream);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
@@ -102,7 +103,9 @@ dust_status graph_call(const void* key, size_t key_len, cudaStream_t stream,
             // End the capture whatever happened, so the stream leaves capture mode.
             const cudaError_t end = cudaStreamEndCapture(c.capture, &graph);
             ok = st == DUST_OK && end == cudaSuccess && graph != nullptr &&
-                 cudaGraphInstantiate(&exec, graph, 0) == cudaSuccess;
+                 cudaGraphInstantiateWithFlags(
+                     &exec, graph,
+                     node_priority ? cudaGraphInstantiateFlagUseNodePriority : 0) == cudaSuccess;
         }
         if (graph) cudaGraphDestroy(graph);
         if (!ok) {

@@ -59,9 +59,13 @@ bool profiling_on();
 // later calls with that key launch the graph on `stream`. Graphs read and
 // write the same addresses, so they see the current contents of every
 // buffer. Bypassed while profiling or a test stall is pending; a call that
-// cannot be captured falls back to direct launches for that key.
+// cannot be captured falls back to direct launches for that key. With
+// `node_priority` the graph keeps the priority of the stream each kernel was
+// captured from (for work that spans internal streams of different
+// priority); otherwise every kernel runs at the priority of `stream`.
 dust_status graph_call(const void* key, size_t key_len, cudaStream_t stream,
-                       dust_status (*enqueue)(const void* ctx, cudaStream_t s), const void* ctx);
+                       dust_status (*enqueue)(const void* ctx, cudaStream_t s), const void* ctx,
+                       bool node_priority = false);
 
 // ---- Programmatic dependent launch. The estimator's kernels are launched so
 // that the next kernel on the stream may be scheduled while the previous one
