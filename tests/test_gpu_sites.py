@@ -181,3 +181,49 @@ def test_sites_graph_replay_reads_current_inputs():
     torch.cuda.synchronize()
     for i, (q, want) in enumerate(zip(sites, wants)):
         assert torch.equal(q["gW"].cpu(), want), i
+
+
+@pytest.mark.parametrize("kind", [dust.RADEMACHER, dust.RADEMACHER_PACKED, dust.GAUSSIAN])
+def test_sites_other_noises_antithetic_and_offset(kind):
+    """Sign noises and Gaussians with antithetic pairs and a later draw range
+    (draw_begin 6) and a scale: each site equals dust_estimate_gW's result."""
+    import torch
+    dev = cuda()
+    shapes = [(4096, 512, 1024, 16, 0.9), (4096, 256, 512, 16, 0.0), (2048, 512, 2048, 8, 0.0),
+              (3000, 128, 1024, 16, 0.5)]
+    sites, wants = [], []
+    flags = dust.CENTER | dust.ANTITHETIC
+    for i, (T, d_in, d_out, K, gamma) in enumerate(shapes):
+        X, delta, so = _inputs(110 + i, T, d_in, K, dev)
+        q = _site(X, delta, so, d_out, 900 + i, gamma, dev)
+        wants.append(dust.dust_estimate_gW(X, delta, d_out, so, q["seed"], kind, 6, q["sigma"],
+                                           gamma, 0.25, flags).cpu())
+        sites.append(q)
+    dust.dust_estimate_gW_sites(sites, kind, 6, 0.25, flags)
+    torch.cuda.synchronize()
+    assert dust.dust_last_error() == dust.OK
+    for i, (q, want) in enumerate(zip(sites, wants)):
+        assert torch.equal(q["gW"].cpu(), want), i
+
+
+def test_sites_fp32_inputs():
+    """fp32 X (the CUDA-core contraction, which stays on the lanes): each site
+    equals dust_estimate_gW's result."""
+    import torch
+    dev = cuda()
+    shapes = [(2048, 256, 512, 8, 0.9), (1500, 192, 320, 8, 0.0), (1024, 128, 256, 4, 0.0)]
+    sites, wants = [], []
+    for i, (T, d_in, d_out, K, gamma) in enumerate(shapes):
+        X, delta, so = _inputs(130 + i, T, d_in, K, dev)
+        X = X.float()
+        ws = torch.empty(max(256, dust.dust_estimate_gW_workspace(T, d_in, d_out, K, dust.F32,
+                                                                  dust.CENTER)),
+                         dtype=torch.uint8, device=dev)
+        q = {"X": X, "delta": delta, "seq_offsets": so, "seed": 950 + i, "sigma": 1e-3,
+             "gamma": gamma, "workspace": ws, "gW": torch.empty((d_out, d_in), device=dev)}
+        wants.append(_single(q).cpu())
+        sites.append(q)
+    dust.dust_estimate_gW_sites(sites, dust.GAUSSIAN, 0, 1.0, dust.CENTER)
+    torch.cuda.synchronize()
+    for i, (q, want) in enumerate(zip(sites, wants)):
+        assert torch.equal(q["gW"].cpu(), want), i
