@@ -64,9 +64,10 @@ def parse_args(argv=None):
     p.add_argument("--workload", default="sweep",
                    choices=["sweep", "mlp_up", "toy", "qkv", "square_r", "square_g",
                             "square_rp", "sweep_qkv", "sweep_o", "sweep_up", "sweep_down",
-                            "forward_g", "forward_r", "forward_rp"],
+                            "sweep_layer", "forward_g", "forward_r", "forward_rp"],
                    help="sweep (the 48-site whole-model pass, the largest configuration) is "
-                        "the headline; forward_* time the jittered forward (8 draws + the "
+                        "the headline; sweep_layer is one of its layers (4 sites, the same "
+                        "multi-site call); forward_* time the jittered forward (8 draws + the "
                         "clean output) of the up-projection layer; the others are single "
                         "layers (sweep_*: one site of each of the sweep's four shapes)")
     p.add_argument("--no-pipe-probe", action="store_true",
@@ -81,8 +82,8 @@ def parse_args(argv=None):
 
 
 # (timed steps, warm-up steps) per workload: about a second of timed work.
-DEFAULT_STEPS = {"sweep": (20, 3), "square_r": (100, 10), "square_g": (100, 10),
-                 "square_rp": (100, 10), "qkv": (300, 20)}
+DEFAULT_STEPS = {"sweep": (20, 3), "sweep_layer": (200, 10), "square_r": (100, 10),
+                 "square_g": (100, 10), "square_rp": (100, 10), "qkv": (300, 20)}
 
 
 # --------------------------------------------------------------- ranks ----
@@ -206,6 +207,7 @@ WORKLOADS = {
     "square_g": "square_4096_T32768_K64_gaussian",
     "square_rp": "square_4096_T32768_K64_rademacher_packed",
     "sweep": "sweep_12x4_sites_T65536_K32_gaussian",
+    "sweep_layer": "sweep_1x4_sites_T65536_K32_gaussian",
     "sweep_qkv": "sweep_site_qkv_512to1536_T65536_K32_gaussian_gamma0.9",
     "sweep_o": "sweep_site_o_512to512_T65536_K32_gaussian",
     "sweep_up": "sweep_site_up_512to2048_T65536_K32_gaussian",
@@ -225,6 +227,8 @@ def workload_sites(name):
     import workloads as wl
     if name == "sweep":
         return wl.sweep_sites()
+    if name == "sweep_layer":
+        return wl.sweep_sites()[:len(SWEEP_KINDS)]
     if name.startswith("sweep_"):
         return [wl.sweep_sites()[SWEEP_KINDS.index(name[len("sweep_"):])]]
     return [{"mlp_up": wl.MLP_UP, "toy": wl.TOY, "qkv": wl.QKV_DECAY, "square_r": wl.SQUARE_R,
@@ -444,10 +448,10 @@ def traffic_from_profiles(kernel, workload):
 
 
 def traffic_for(kernel, workload, sites):
-    """Per-launch DRAM traffic of `kernel` over a step: for the sweep, the
-    mean over its launches of the four site shapes' captured traffic (None
-    unless all four are current)."""
-    if workload != "sweep":
+    """Per-launch DRAM traffic of `kernel` over a step: for the sweep (or one
+    of its layers), the mean over its launches of the four site shapes'
+    captured traffic (None unless all four are current)."""
+    if workload not in ("sweep", "sweep_layer"):
         return traffic_from_profiles(kernel, workload)
     per = {k: traffic_from_profiles(kernel, "sweep_" + k) for k in SWEEP_KINDS}
     if any(v is None for v in per.values()):

@@ -141,3 +141,11 @@ def test_sweep_traffic_is_the_mean_over_its_launches(monkeypatch):
     assert bench.traffic_for("weight", "sweep", sites) == pytest.approx(3.0)
     per["sweep_o"] = None
     assert bench.traffic_for("weight", "sweep", sites) is None
+
+
+def test_one_sweep_layer_is_its_four_sites():
+    layer = bench.workload_sites("sweep_layer")
+    sweep = bench.workload_sites("sweep")
+    assert [bench.site_kind(w) for w in layer] == ["qkv", "o", "up", "down"]
+    assert [(w.d_in, w.d_out, w.T, w.K, w.gamma) for w in layer] == \
+        [(w.d_in, w.d_out, w.T, w.K, w.gamma) for w in sweep[:4]]
