@@ -648,8 +648,7 @@ cudaError_t launch_mt(const CUtensorMap& ta, const CUtensorMap& tb, int64_t T, i
     {
         ProfScope ps(kStageGemmTc, s);
         e = launch_pdl(k_gemm_tc<MT, FIT>, grid, dim3(threads_of(FIT)), C::kSmemBytes, s, ta, tb,
-                       d_in,
-                       d_out, T, slice, S_used > 1 ? partials : gW, scale, mode, st, stall);
+                       d_in, d_out, T, slice, S_used > 1 ? partials : gW, scale, mode, st, stall);
     }
     if (e != cudaSuccess) return e;
     e = hand_back(s, back, back_ev);
