@@ -281,3 +281,73 @@ def test_sweep_full_size_through_the_sites_call():
         g = got[i].double().cpu().numpy()
         assert np.all(np.isfinite(g))
         assert rel_fro(g[chan, col], want) <= 1e-2, i
+
+
+def test_many_mixed_sites():
+    """37 sites of mixed sizes (more than ten per lane), some with d_in or
+    d_out not a multiple of 8 (the CUDA-core contraction, which stays on the
+    lane), some with γ ≠ 0: every result equals its single-site call."""
+    import torch
+    dev = cuda()
+    rng = np.random.default_rng(77)
+    sites, wants = [], []
+    for i in range(37):
+        T = int(rng.integers(200, 1500))
+        d_in = int(rng.choice([64, 128, 60, 256]))
+        d_out = int(rng.choice([128, 256, 72, 100]))
+        K = int(rng.choice([4, 8, 16]))
+        gamma = float(rng.choice([0.0, 0.0, 0.9]))
+        X, delta, so = _inputs(200 + i, T, d_in, K, dev)
+        q = _site(X, delta, so, d_out, 1200 + i, gamma, dev)
+        wants.append(_single(q).cpu())
+        sites.append(q)
+    for _ in range(2):
+        for q in sites:
+            q["gW"].fill_(float("nan"))
+        torch.cuda.synchronize()
+        dust.dust_estimate_gW_sites(sites, dust.GAUSSIAN, 0, 1.0, dust.CENTER)
+        torch.cuda.synchronize()
+        assert dust.dust_last_error() == dust.OK
+        for i, (q, want) in enumerate(zip(sites, wants)):
+            assert torch.equal(q["gW"].cpu(), want), i
+
+
+def test_sites_from_two_host_threads():
+    """Two host threads each calling dust_estimate_gW_sites on their own
+    stream and buffers, several times: the calls share the library's lanes
+    (their enqueues are serialised on the host) and every result equals its
+    single-site call."""
+    import threading
+    import torch
+    dev = cuda()
+    groups, wants = [], []
+    for gi in range(2):
+        sites = []
+        for i, (T, d_in, d_out, K, gamma) in enumerate(SHAPES[:4]):
+            X, delta, so = _inputs(300 + 10 * gi + i, T, d_in, K, dev)
+            sites.append(_site(X, delta, so, d_out, 1500 + 10 * gi + i, gamma, dev))
+        wants.append([_single(q).cpu() for q in sites])
+        groups.append(sites)
+    torch.cuda.synchronize()
+    errors = []
+
+    def run(gi):
+        try:
+            st = torch.cuda.Stream()
+            arr = dust.SiteArray(groups[gi])
+            for _ in range(5):
+                dust.dust_estimate_gW_sites(arr, dust.GAUSSIAN, 0, 1.0, dust.CENTER, stream=st)
+            st.synchronize()
+        except Exception as e:  # reported by the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=run, args=(gi,)) for gi in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    assert dust.dust_last_error() == dust.OK
+    for gi in range(2):
+        for i, (q, want) in enumerate(zip(groups[gi], wants[gi])):
+            assert torch.equal(q["gW"].cpu(), want), (gi, i)
