@@ -818,6 +818,8 @@ def run_gb300(args):
                   for b, h in zip(bundles, hosts)]
 
     def e2e_step():
+        # returns (host enqueue, wait for the stream) in seconds
+        a = time.perf_counter()
         if len(bundles) > 1:
             dust.dust_estimate_gW_host_sites(host_sites, sites[0].kind, 0, 1.0, flags,
                                              stream=stream)
@@ -827,18 +829,20 @@ def run_gb300(args):
             dust.dust_estimate_gW_host(h["Xh"], h["Xs"], h["dh"], h["ds"], h["sh"], h["ss"],
                                        h["gh"], h["gs"], w.d_out, w.seed, w.kind, 0, w.sigma,
                                        w.gamma, 1.0, flags, workspace=b["ws"], stream=stream)
+        b_ = time.perf_counter()
         stream.synchronize()
+        return b_ - a, time.perf_counter() - b_
 
     n_e2e = max(3, min(args.e2e_steps, args.steps)) if len(sites) > 1 else args.e2e_steps
     for _ in range(3):
         e2e_step()
     barrier()
     torch.cuda.synchronize()
-    e2e_times = []
+    e2e_times, e2e_split = [], []
     t0 = time.perf_counter()
     for _ in range(n_e2e):
         a = time.perf_counter()
-        e2e_step()
+        e2e_split.append(e2e_step())
         e2e_times.append(time.perf_counter() - a)
     e2e_s = max_over_ranks(time.perf_counter() - t0)
     e2e_value = world * units * n_e2e / e2e_s
@@ -892,6 +896,10 @@ def run_gb300(args):
                                                    1000.0 * statistics.median(e2e_times),
                                                    1000.0 * max(e2e_times)],
                     "x_h2d_link_gbs": link_gbs,
+                    # every step, and the slowest step's host enqueue and wait (ms)
+                    "ms_per_step_all": [round(1000.0 * t, 2) for t in e2e_times],
+                    "slowest_step_enqueue_wait_ms": [
+                        round(1000.0 * x, 2) for x in e2e_split[e2e_times.index(max(e2e_times))]],
                     "entry_point": "dust_estimate_gW_host_sites" if len(sites) > 1
                     else "dust_estimate_gW_host"},
             "gpu_launches": int(round(launches_per_step * args.steps)),
