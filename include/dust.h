@@ -374,12 +374,13 @@ int32_t dust_estimate_gW_path(int64_t T, int64_t d_in, int64_t d_out, int64_t K,
  * bit-identical to such calls made one after another. What differs is the
  * order on the device: the sites run on internal compute lanes of the current
  * device (streams created on first use, never destroyed), site i on lane
- * i mod L, which start after everything enqueued on `stream` before this call
- * and which `stream` waits for at its end (on error paths too). So one site's
- * contraction (tensor cores) overlaps the next sites' weighting
- * (transcendental and integer pipes). The same delta or seq_offsets may serve
- * several sites (Dust's loss changes are one per token and draw for the whole
- * model).
+ * i mod L, each lane with a companion stream of the device's highest priority
+ * for its sites' contraction kernels. All of them start after everything
+ * enqueued on `stream` before this call, and `stream` waits for all of them
+ * at its end (on error paths too). So one site's contraction (tensor cores)
+ * runs beside later sites' weighting (transcendental and integer pipes). The
+ * same delta or seq_offsets may serve several sites (Dust's loss changes are
+ * one per token and draw for the whole model).
  *
  * Because sites run concurrently, what a site writes (its gW, and its
  * workspace) must not overlap any buffer of another site (X, delta,
@@ -388,8 +389,10 @@ int32_t dust_estimate_gW_path(int64_t T, int64_t d_in, int64_t d_out, int64_t K,
  * enqueued. At most 4096 sites (DUST_ERR_RANGE). Graph replay as for
  * dust_estimate_gW: from the second call with identical arguments (the whole
  * site array included), the call is captured once into a CUDA graph, lanes
- * and all, and later calls launch that graph on `stream`. Concurrent calls
- * on one device are serialised on the host while they enqueue.
+ * and all, and later calls launch that graph on `stream`; the graph keeps
+ * each kernel's stream priority (the lanes' and the contraction streams'),
+ * whatever the priority of `stream`. Concurrent calls on one device are
+ * serialised on the host while they enqueue.
  */
 typedef struct {
     const void* X;                   /* device [T][d_in], x_dtype */
