@@ -351,3 +351,29 @@ def test_sites_from_two_host_threads():
     for gi in range(2):
         for i, (q, want) in enumerate(zip(groups[gi], wants[gi])):
             assert torch.equal(q["gW"].cpu(), want), (gi, i)
+
+
+@pytest.mark.parametrize("flags", [dust.CENTER, dust.CENTER | dust.ACCUMULATE])
+def test_sites_wide_tiles_in_cluster(flags):
+    """Sites whose contraction takes 256-channel tiles and reduces its token
+    slices inside a cluster (16,384 tokens, 1024 -> 2048: 32 tiles, 4 slices of
+    4096 tokens), next to one with 128-channel tiles, in the 32-register build
+    of the lanes: each equals dust_estimate_gW's result (which takes the
+    192-thread build), overwritten or accumulated."""
+    import torch
+    dev = cuda()
+    shapes = [(16384, 1024, 2048, 8, 0.0), (16384, 1024, 2048, 8, 0.9), (16384, 512, 2048, 8, 0.0)]
+    sites, wants = [], []
+    for i, (T, d_in, d_out, K, gamma) in enumerate(shapes):
+        X, delta, so = _inputs(160 + i, T, d_in, K, dev)
+        q = _site(X, delta, so, d_out, 1700 + i, gamma, dev)
+        base = torch.randn((d_out, d_in), device=dev)
+        q["gW"].copy_(base)
+        wants.append(_single(q, flags, gW=base.clone()).cpu())
+        sites.append(q)
+    torch.cuda.synchronize()
+    dust.dust_estimate_gW_sites(sites, dust.GAUSSIAN, 0, 1.0, flags)
+    torch.cuda.synchronize()
+    assert dust.dust_last_error() == dust.OK
+    for i, (q, want) in enumerate(zip(sites, wants)):
+        assert torch.equal(q["gW"].cpu(), want), i
